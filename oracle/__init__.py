@@ -1,0 +1,248 @@
+"""CPU oracle for the MoE expert-parallel token pipeline (numpy front end).
+
+TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only ``tests/``, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import this
+package.  The product library never calls it and shares no code with it.
+
+The arithmetic lives in ``moe_oracle.c`` (plain single-threaded C, one IEEE
+rounding per fp32 operation); this module only marshals numpy arrays.
+Stages follow the "EP Normal" pipeline of the UMDK/CAM deep-analysis page
+(v2), section 2: 2.3 dispatch layout, 2.4 notify, 2.5 dispatch with dynamic
+INT8 quantisation, 2.6 combine.
+
+Arrays of 16-bit floats (bf16 / fp16) are passed as ``np.uint16`` bit
+patterns; ``dtype`` is 0 for bf16 and 1 for fp16.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_f32p = ctypes.POINTER(ctypes.c_float)
+
+
+def lib():
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        i, i64 = ctypes.c_int, ctypes.c_int64
+        for name in ("oracle_bf16_to_f32", "oracle_f16_to_f32"):
+            getattr(L, name).argtypes = [_u16p, _f32p, i64]
+        for name in ("oracle_f32_to_bf16", "oracle_f32_to_f16"):
+            getattr(L, name).argtypes = [_f32p, _u16p, i64]
+        L.oracle_layout.argtypes = [i, i, i, i, _i32p, _i32p, _i32p, _i32p]
+        L.oracle_notify.argtypes = [i, i, i, _i32p, _i32p, _i32p, _i64p,
+                                    _i32p, _i32p]
+        L.oracle_dst_row.argtypes = [i, i, i, i, _i32p, _i32p, _i32p, _i64p,
+                                     i64, i]
+        L.oracle_dst_row.restype = i64
+        L.oracle_row_bytes.argtypes = [i, i]
+        L.oracle_row_bytes.restype = i64
+        L.oracle_quant_row.argtypes = [i, i, _u16p, _u8p]
+        L.oracle_dispatch.argtypes = [i, i, i, i, i, i, i, _u16p, _i32p,
+                                      _i32p, _i32p, _i64p, _u8p, i64]
+        L.oracle_dispatch_tokens.argtypes = [i, i, i, i, i, i, i, _u16p,
+                                             _i32p, _i32p, _i32p, _i64p,
+                                             _i64p, i64, _u8p, _i64p]
+        L.oracle_combine_tokens.argtypes = [i, i, i, i, i, i, _u16p, i64,
+                                            _i32p, _f32p, _i32p, _i32p,
+                                            _i64p, _i64p, i64, _u16p]
+        _lib = L
+    return _lib
+
+
+def use_library(path):
+    """Swap in another build of the oracle (tests use this to run the pins
+    against deliberately broken copies); returns the previous library."""
+    global _lib
+    prev = lib()
+    _lib = None
+    saved = _build.build
+    try:
+        _build.build = lambda: path
+        lib()
+    finally:
+        _build.build = saved
+    return prev
+
+
+def restore_library(prev):
+    global _lib
+    _lib = prev
+
+
+def _p(a, ptype):
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ptype)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def row_bytes(H, quant):
+    """Receive-row size in bytes: align32(H) + 32 for INT8 rows, else 2H."""
+    return int(lib().oracle_row_bytes(int(H), int(bool(quant))))
+
+
+# ---- number conversions (exported for pinning) ---------------------------
+
+def to_f32(bits, dtype):
+    bits = _c(bits, np.uint16)
+    out = np.empty(bits.shape, np.float32)
+    fn = lib().oracle_bf16_to_f32 if dtype == 0 else lib().oracle_f16_to_f32
+    fn(_p(bits, _u16p), _p(out, _f32p), bits.size)
+    return out
+
+
+def from_f32(vals, dtype):
+    vals = _c(vals, np.float32)
+    out = np.empty(vals.shape, np.uint16)
+    fn = lib().oracle_f32_to_bf16 if dtype == 0 else lib().oracle_f32_to_f16
+    fn(_p(vals, _f32p), _p(out, _u16p), vals.size)
+    return out
+
+
+# ---- the four stages -----------------------------------------------------
+
+def layout(topk_idx, R, epr):
+    """Stage 1.  topk_idx int32 [T, k] (T = R*bs) -> dict(count [R,E],
+    rank_send [R,R], send_idx [T,k], status)."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    bs = T // R
+    assert bs * R == T
+    E = R * epr
+    count = np.zeros((R, E), np.int32)
+    rank_send = np.zeros((R, R), np.int32)
+    send_idx = np.zeros((T, k), np.int32)
+    st = lib().oracle_layout(R, bs, k, epr, _p(idx, _i32p), _p(count, _i32p),
+                             _p(rank_send, _i32p), _p(send_idx, _i32p))
+    return dict(count=count, rank_send=rank_send, send_idx=send_idx,
+                status=st)
+
+
+def notify(count, R, bs, epr):
+    """Stage 2.  count int32 [R, E] -> dict(put_offset [E*R],
+    total_recv [R], rank_recv_base [R+1] int64, recv_per_expert [E],
+    max_bs, status)."""
+    count = _c(count, np.int32)
+    E = R * epr
+    assert count.shape == (R, E)
+    put_offset = np.zeros(E * R, np.int32)
+    total_recv = np.zeros(R, np.int32)
+    base = np.zeros(R + 1, np.int64)
+    rpe = np.zeros(E, np.int32)
+    max_bs = np.zeros(1, np.int32)
+    st = lib().oracle_notify(R, bs, epr, _p(count, _i32p),
+                             _p(put_offset, _i32p), _p(total_recv, _i32p),
+                             _p(base, _i64p), _p(rpe, _i32p),
+                             _p(max_bs, _i32p))
+    return dict(put_offset=put_offset, total_recv=total_recv,
+                rank_recv_base=base, recv_per_expert=rpe,
+                max_bs=int(max_bs[0]), status=st)
+
+
+def dst_rows(topk_idx, send_idx, put_offset, rank_recv_base, R, epr):
+    """Row id of every pair, int64 [T, k] (-1 for a bad expert id)."""
+    idx = _c(topk_idx, np.int32)
+    sidx = _c(send_idx, np.int32)
+    po = _c(put_offset, np.int32)
+    base = _c(rank_recv_base, np.int64)
+    T, k = idx.shape
+    bs = T // R
+    out = np.empty((T, k), np.int64)
+    L = lib()
+    for g in range(T):
+        for kk in range(k):
+            out[g, kk] = L.oracle_dst_row(R, bs, k, epr, _p(idx, _i32p),
+                                          _p(sidx, _i32p), _p(po, _i32p),
+                                          _p(base, _i64p), g, kk)
+    return out
+
+
+def quant_row(xrow_bits, dtype):
+    """One row's INT8 receive image (uint8, align32(H) + 32 bytes)."""
+    xrow = _c(xrow_bits, np.uint16)
+    H = xrow.size
+    out = np.zeros(row_bytes(H, 1), np.uint8)
+    lib().oracle_quant_row(H, dtype, _p(xrow, _u16p), _p(out, _u8p))
+    return out
+
+
+def dispatch(x_bits, topk_idx, send_idx, put_offset, rank_recv_base, R, epr,
+             dtype, quant, capacity_rows=None):
+    """Stage 3 over all tokens.  Returns (recv uint8 [rows, S], status)."""
+    x = _c(x_bits, np.uint16)
+    idx = _c(topk_idx, np.int32)
+    T, H = x.shape
+    k = idx.shape[1]
+    bs = T // R
+    base = _c(rank_recv_base, np.int64)
+    rows = int(base[R]) if capacity_rows is None else int(capacity_rows)
+    S = row_bytes(H, quant)
+    recv = np.zeros((rows, S), np.uint8)
+    st = lib().oracle_dispatch(R, bs, k, epr, H, dtype, int(bool(quant)),
+                               _p(x, _u16p), _p(idx, _i32p),
+                               _p(_c(send_idx, np.int32), _i32p),
+                               _p(_c(put_offset, np.int32), _i32p),
+                               _p(base, _i64p), _p(recv, _u8p), rows)
+    return recv, st
+
+
+def dispatch_tokens(x_bits, topk_idx, send_idx, put_offset, rank_recv_base,
+                    R, epr, dtype, quant, tokens):
+    """Stage 3 for the listed tokens only.  Returns (images uint8
+    [n, k, S], row_ids int64 [n, k], status)."""
+    x = _c(x_bits, np.uint16)
+    idx = _c(topk_idx, np.int32)
+    T, H = x.shape
+    k = idx.shape[1]
+    bs = T // R
+    toks = _c(tokens, np.int64)
+    S = row_bytes(H, quant)
+    images = np.zeros((toks.size, k, S), np.uint8)
+    row_ids = np.zeros((toks.size, k), np.int64)
+    st = lib().oracle_dispatch_tokens(
+        R, bs, k, epr, H, dtype, int(bool(quant)), _p(x, _u16p),
+        _p(idx, _i32p), _p(_c(send_idx, np.int32), _i32p),
+        _p(_c(put_offset, np.int32), _i32p),
+        _p(_c(rank_recv_base, np.int64), _i64p), _p(toks, _i64p), toks.size,
+        _p(images, _u8p), _p(row_ids, _i64p))
+    return images, row_ids, st
+
+
+def combine(y_bits, topk_idx, topk_weights, send_idx, put_offset,
+            rank_recv_base, R, epr, dtype, tokens=None):
+    """Stage 4.  y uint16 [rows, H]; returns (out uint16 [n, H], status),
+    n = T when ``tokens`` is None, else len(tokens)."""
+    y = _c(y_bits, np.uint16)
+    idx = _c(topk_idx, np.int32)
+    w = _c(topk_weights, np.float32)
+    T, k = idx.shape
+    H = y.shape[1]
+    bs = T // R
+    if tokens is None:
+        toks = None
+        n = T
+    else:
+        toks = _c(tokens, np.int64)
+        n = toks.size
+    out = np.zeros((n, H), np.uint16)
+    st = lib().oracle_combine_tokens(
+        R, bs, k, epr, H, dtype, _p(y, _u16p), y.shape[0], _p(idx, _i32p),
+        _p(w, _f32p), _p(_c(send_idx, np.int32), _i32p),
+        _p(_c(put_offset, np.int32), _i32p),
+        _p(_c(rank_recv_base, np.int64), _i64p),
+        None if toks is None else _p(toks, _i64p), n, _p(out, _u16p))
+    return out, st

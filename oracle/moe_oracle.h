@@ -1,0 +1,109 @@
+/*
+ * moe_oracle.h -- CPU oracle for the MoE expert-parallel token pipeline.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the tests, the smoke check and
+ * the benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or helper with the CUDA library; the only thing both sides
+ * share is the seeded input generator (workloads.py), which holds none of the
+ * method's arithmetic.
+ *
+ * Every function is the plain definition of what a stage of the "EP Normal"
+ * pipeline computes (UMDK/CAM analysis v2, section 2.1 "overall architecture",
+ * sections 2.3-2.6 for the four stages).  Single-threaded, no blocking, no
+ * reordering.  Build with -ffp-contract=off and without -ffast-math so that
+ * each fp32 multiply and add rounds once, as the page's vector ops do.
+ *
+ * Notation (shared with the pages): R ranks, epr experts per rank, E = R*epr,
+ * bs tokens per rank, k = top-k, H hidden size, T = R*bs tokens,
+ * global token g = s*bs + t for source rank s and local token t,
+ * dst(e) = e / epr.
+ *
+ * Return codes match the library's public status values by number:
+ * 0 ok, 2 an expert id outside [0,E), 3 a destination row outside the
+ * receive buffer, 1 an invalid argument.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype codes: 0 = bf16, 1 = fp16 (rows of 16-bit words). */
+
+/* Number conversions, exported so tests can pin them against numpy/torch. */
+void oracle_bf16_to_f32(const uint16_t* in, float* out, int64_t n);
+void oracle_f16_to_f32(const uint16_t* in, float* out, int64_t n);
+void oracle_f32_to_bf16(const float* in, uint16_t* out, int64_t n);
+void oracle_f32_to_f16(const float* in, uint16_t* out, int64_t n);
+
+/* Stage 1, dispatch layout (section 2.3).  topk_idx [R][bs][k].
+ * count [R][E]: pairs of rank s routed to expert e.
+ * rank_send [R][R]: pairs of rank s routed to any expert of rank r.
+ * send_idx [R][bs][k]: index of the pair among the pairs of (s, e), in
+ * (t, k) order.  An id outside [0,E) is not counted, gets send_idx -1, and
+ * makes the call return 2. */
+int oracle_layout(int R, int bs, int k, int epr, const int32_t* topk_idx,
+                  int32_t* count, int32_t* rank_send, int32_t* send_idx);
+
+/* Stage 2, notify (section 2.4).  count [R][E] (already "gathered").
+ * put_offset [E][R]: exclusive prefix sum, per destination rank r, over the
+ * (local expert j, source rank s) order; index e*R + s.
+ * total_recv [R], rank_recv_base [R+1] (exclusive scan of total_recv; the
+ * last entry is the number of rows), recv_per_expert [E], max_bs [1]. */
+int oracle_notify(int R, int bs, int epr, const int32_t* count,
+                  int32_t* put_offset, int32_t* total_recv,
+                  int64_t* rank_recv_base, int32_t* recv_per_expert,
+                  int32_t* max_bs);
+
+/* Receive-buffer row of pair (g, kk) (section 2.6 addressing), or -1 when
+ * the expert id is outside [0,E). */
+int64_t oracle_dst_row(int R, int bs, int k, int epr, const int32_t* topk_idx,
+                       const int32_t* send_idx, const int32_t* put_offset,
+                       const int64_t* rank_recv_base, int64_t g, int kk);
+
+/* Bytes per receive row: quant -> align32(H) + 32, else H*2. */
+int64_t oracle_row_bytes(int H, int quant);
+
+/* Dynamic INT8 quantisation of one row (section 2.5 QuantProcess) into a
+ * receive-row image of oracle_row_bytes(H,1) bytes. */
+void oracle_quant_row(int H, int dtype, const uint16_t* xrow, uint8_t* out);
+
+/* Stage 3, dispatch (section 2.5): every pair's row written into recv.
+ * recv holds capacity_rows rows of oracle_row_bytes(H, quant) bytes.
+ * Pairs with a bad id or a row >= capacity_rows are skipped (return 2/3). */
+int oracle_dispatch(int R, int bs, int k, int epr, int H, int dtype, int quant,
+                    const uint16_t* x, const int32_t* topk_idx,
+                    const int32_t* send_idx, const int32_t* put_offset,
+                    const int64_t* rank_recv_base, uint8_t* recv,
+                    int64_t capacity_rows);
+
+/* Dispatch restricted to the listed tokens: for each listed token and each
+ * kk, the row image goes to rows_out[(i*k + kk) * row_bytes] and its row id
+ * to row_ids[i*k + kk] (-1 for a bad id; the image is then left zero). */
+int oracle_dispatch_tokens(int R, int bs, int k, int epr, int H, int dtype,
+                           int quant, const uint16_t* x,
+                           const int32_t* topk_idx, const int32_t* send_idx,
+                           const int32_t* put_offset,
+                           const int64_t* rank_recv_base,
+                           const int64_t* tokens, int64_t ntok,
+                           uint8_t* rows_out, int64_t* row_ids);
+
+/* Stage 4, combine (section 2.6) for the listed tokens: out[i][h] =
+ * RNE(sum over kk in order of fp32(y[row(g,kk)][h]) * w[g][kk]).
+ * y has y_rows rows of H 16-bit words.  Pass tokens = NULL for all T tokens
+ * (out is then [T][H]). */
+int oracle_combine_tokens(int R, int bs, int k, int epr, int H, int dtype,
+                          const uint16_t* y, int64_t y_rows,
+                          const int32_t* topk_idx, const float* topk_weights,
+                          const int32_t* send_idx, const int32_t* put_offset,
+                          const int64_t* rank_recv_base,
+                          const int64_t* tokens, int64_t ntok, uint16_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

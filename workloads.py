@@ -1,0 +1,164 @@
+"""Seeded synthetic workloads for the MoE expert-parallel token pipeline.
+
+This module only draws inputs: routing (``topk_idx``), gating weights
+(``topk_weights``), token rows ``x`` and expert outputs ``y``.  It holds none
+of the pipeline's arithmetic, so both the CUDA path and the CPU oracle can
+take their inputs from it.  Everything is drawn on the host with
+``torch.Generator`` (CPU), one generator per input stream, so the same seed
+gives the same tensors whatever else is drawn.
+
+The five named workloads are the pipeline's benchmark shapes: a tiny case, a
+DeepSeek-V3-shaped case, a Zipf-skewed case, an fp16 case without
+quantisation and the 384-rank case (CAM_MAX_RANK_SIZE on the UMDK/CAM page).
+No public dataset is involved: the shapes and distributions are the recipe.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+import torch
+
+BF16, FP16 = 0, 1
+_TORCH_DTYPE = {BF16: torch.bfloat16, FP16: torch.float16}
+
+# Input streams: each has its own generator seeded from (seed, stream).
+_S_ROUTE, _S_WEIGHT, _S_X, _S_OUTLIER, _S_Y = range(5)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    R: int                 # logical EP ranks
+    epr: int               # experts per rank
+    bs: int                # tokens per rank
+    H: int                 # hidden size
+    k: int                 # top-k
+    dtype: int = BF16      # token dtype (BF16 or FP16)
+    quant: bool = True     # dynamic INT8 quantisation in dispatch
+    x_dist: str = "normal"     # "normal" (x_scale = std) or "uniform" (+-x_scale)
+    x_scale: float = 1.0
+    outlier_p: float = 0.0     # fraction of x elements multiplied by outlier_mult
+    outlier_mult: float = 20.0
+    routing: str = "uniform"   # "uniform" (k distinct) or "zipf" (w/o replacement)
+    zipf_s: float = 1.2
+    weights: str = "softmax"   # "softmax" or "sigmoid" (sigmoid, normalised)
+    seed: int = 1234
+
+    @property
+    def E(self) -> int:
+        return self.R * self.epr
+
+    @property
+    def T(self) -> int:
+        return self.R * self.bs
+
+    @property
+    def P(self) -> int:
+        return self.T * self.k
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+# The five benchmark workloads (seed = 1234 + index).
+WORKLOADS = {
+    "tiny": Workload("tiny", R=2, epr=4, bs=16, H=128, k=2, seed=1234),
+    "dsv3": Workload("dsv3", R=8, epr=32, bs=4096, H=7168, k=8,
+                     outlier_p=0.01, seed=1235),
+    "skew": Workload("skew", R=16, epr=4, bs=2048, H=4096, k=6, x_scale=2.0,
+                     routing="zipf", weights="sigmoid", seed=1236),
+    "fp16": Workload("fp16", R=32, epr=4, bs=1024, H=2048, k=8, dtype=FP16,
+                     quant=False, x_dist="uniform", x_scale=4.0, seed=1237),
+    "maxrank": Workload("maxrank", R=384, epr=2, bs=128, H=7168, k=8,
+                        seed=1238),
+}
+ORDER = ["tiny", "dsv3", "skew", "fp16", "maxrank"]
+
+
+def _gen(seed: int, stream: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed * 16 + stream)
+    return g
+
+
+def routing(w: Workload):
+    """topk_idx int32 [T, k] and topk_weights float32 [T, k] (CPU tensors).
+
+    uniform: each token picks k distinct experts uniformly at random, in a
+    random order.  zipf: expert e has weight (e+1)^-s and the k experts are
+    drawn one after another without replacement.
+    """
+    T, E, k = w.T, w.E, w.k
+    g = _gen(w.seed, _S_ROUTE)
+    if T == 0:
+        idx = torch.zeros((0, k), dtype=torch.int64)
+    elif w.routing == "uniform":
+        # k largest of E iid uniform keys = a uniform k-subset in random order
+        idx = torch.rand((T, E), generator=g).topk(k, dim=1).indices
+    elif w.routing == "zipf":
+        p = (torch.arange(E, dtype=torch.float64) + 1.0) ** (-w.zipf_s)
+        p = (p / p.sum()).to(torch.float32)
+        idx = torch.multinomial(p.expand(T, E).contiguous(), k,
+                                replacement=False, generator=g)
+    else:
+        raise ValueError(w.routing)
+    gw = _gen(w.seed, _S_WEIGHT)
+    z = torch.randn((T, k), generator=gw, dtype=torch.float32)
+    if w.weights == "softmax":
+        wt = torch.softmax(z, dim=1)
+    elif w.weights == "sigmoid":
+        sg = torch.sigmoid(z)
+        wt = sg / sg.sum(dim=1, keepdim=True)
+    else:
+        raise ValueError(w.weights)
+    return idx.to(torch.int32).contiguous(), wt.to(torch.float32).contiguous()
+
+
+def _rows(n_rows: int, H: int, dtype: int, dist: str, scale: float,
+          g: torch.Generator, outlier_p: float = 0.0, outlier_mult: float = 1.0,
+          g_out: Optional[torch.Generator] = None,
+          chunk_elems: int = 1 << 26) -> torch.Tensor:
+    out = torch.empty((n_rows, H), dtype=_TORCH_DTYPE[dtype])
+    rows_per_chunk = max(1, chunk_elems // max(H, 1))
+    for r0 in range(0, n_rows, rows_per_chunk):
+        r1 = min(n_rows, r0 + rows_per_chunk)
+        if dist == "normal":
+            v = torch.randn((r1 - r0, H), generator=g) * scale
+        elif dist == "uniform":
+            v = (torch.rand((r1 - r0, H), generator=g) * 2.0 - 1.0) * scale
+        else:
+            raise ValueError(dist)
+        if outlier_p > 0.0:
+            m = torch.rand((r1 - r0, H), generator=g_out) < outlier_p
+            v = torch.where(m, v * outlier_mult, v)
+        out[r0:r1] = v.to(out.dtype)  # round to nearest even
+    return out
+
+
+def tokens(w: Workload) -> torch.Tensor:
+    """x [T, H] in the workload's dtype (CPU tensor)."""
+    return _rows(w.T, w.H, w.dtype, w.x_dist, w.x_scale, _gen(w.seed, _S_X),
+                 w.outlier_p, w.outlier_mult, _gen(w.seed, _S_OUTLIER))
+
+
+def expert_outputs(w: Workload, rows: Optional[int] = None) -> torch.Tensor:
+    """Synthetic expert outputs y [rows, H] ~ N(0,1) in the token dtype.
+
+    ``rows`` defaults to T*k, the number of receive rows when every expert id
+    is valid.  They stand for the grouped expert GEMM's output, which sits in
+    the same row positions as the dispatched rows.
+    """
+    n = w.P if rows is None else rows
+    return _rows(n, w.H, w.dtype, "normal", 1.0, _gen(w.seed, _S_Y))
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """uint16 bit patterns of a bf16/fp16 CPU tensor (no copy)."""
+    assert t.dtype in (torch.bfloat16, torch.float16)
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def torch_dtype(dtype: int) -> torch.dtype:
+    return _TORCH_DTYPE[dtype]
