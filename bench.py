@@ -1,0 +1,508 @@
+"""Benchmark of the EP Normal MoE token pipeline on GB300.
+
+One step = the whole hot path on one synthetic batch: dispatch layout ->
+notify -> dispatch (INT8 quantisation when the workload has it) -> combine,
+with inputs already resident in HBM.  ``value`` is tokens per second over
+the step (T tokens per step, summed over ranks); per-stage times, achieved
+HBM bandwidth and the roofline fraction of the dominant kernel (combine) are
+reported next to it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dsv3]
+    python bench.py --impl reference ...   # the CPU oracle, as it stands
+
+Multi-GPU runs (torchrun, one rank per GPU) are independent replicas: each
+rank runs the full R-logical-rank problem on its own GPU and there is no
+data-path collective; ranks only meet in a barrier and a max-reduction of
+the step time ("weak" scaling).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20          # > 129 MB of L2
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = {                  # kernel -> source file (traffic staleness)
+    "combine": "combine_moe_dispatch_layout_gb300/csrc/combine.cu",
+    "dispatch": "combine_moe_dispatch_layout_gb300/csrc/dispatch.cu",
+}
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+               "clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,"
+               "clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,"
+               "clocks_event_reasons.sw_power_cap")
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what each stage must move at minimum)
+# ---------------------------------------------------------------------------
+
+def row_bytes(w):
+    return ((w.H + 31) // 32 * 32 + 32) if w.quant else 2 * w.H
+
+
+def alg_bytes(w):
+    """Per launch: x read once + k rows written (+ indices) for dispatch;
+    k rows read + one row written (+ indices, weights) for combine."""
+    es = 2
+    dispatch = (w.T * w.H * es + w.P * row_bytes(w) + w.P * 8
+                + w.E * w.R * 4 + (w.R + 1) * 8)
+    combine = w.P * w.H * es + w.P * 12 + w.T * w.H * es
+    layout = w.P * 8 + w.R * w.E * 4 + w.R * w.R * 4
+    notify = 2 * w.R * w.E * 4 + w.E * 4 + w.R * 4 + (w.R + 1) * 8
+    return dict(layout=layout, notify=notify, dispatch=dispatch,
+                combine=combine)
+
+
+def workload_desc(w):
+    return ("%s: R=%d E=%d (%d/rank) bs=%d T=%d H=%d k=%d %s %s" % (
+        w.name, w.R, w.E, w.epr, w.bs, w.T, w.H, w.k,
+        "bf16" if w.dtype == W.BF16 else "fp16",
+        "int8-quant" if w.quant else "verbatim"))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _file_hash(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        ent = d[kernel][workload]
+        if ent["source_sha256_16"] != _file_hash(KERNEL_SOURCES[kernel]):
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas: a barrier and a max of the step time)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def reduce_max(value, world, device=None):
+    """Max of a float over ranks (value on every rank)."""
+    if world == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_tokens_per_s(tokens_per_rank, world, max_seconds):
+    """Whole-job throughput: the tokens all ranks processed over the slowest
+    rank's time."""
+    return tokens_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv") \
+            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else \
+            "/tmp/moe_ep_clocks_%d.csv" % os.getpid()
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + CLOCK_QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, w):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    import combine_moe_dispatch_layout_gb300 as ep  # noqa: F401 (loads the .so)
+    from combine_moe_dispatch_layout_gb300 import pipeline as pl
+    dev = torch.device("cuda", local)
+
+    idx_h, wt_h = W.routing(w)
+    x_h = W.tokens(w)
+    y_h = W.expert_outputs(w)
+    idx, wt, x = idx_h.to(dev), wt_h.to(dev), x_h.to(dev)
+    y = y_h.to(dev)
+    b = pl.PipelineBuffers(w.R, w.bs, w.k, w.epr, w.H, w.dtype, w.quant,
+                           device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        pl.moe_dispatch_layout(b.shape, idx, b.count, b.rank_send, b.send_idx,
+                               b.workspace, b.dev_status, stream)
+        if evs:
+            evs[1].record(stream)
+        pl.moe_notify_dispatch(b.shape, b.count, b.put_offset, b.total_recv,
+                               b.rank_recv_base, b.recv_per_expert, b.max_bs,
+                               b.dev_status, stream)
+        if evs:
+            evs[2].record(stream)
+        pl.run_dispatch(b, x, idx, stream)
+        if evs:
+            evs[3].record(stream)
+        pl.run_combine(b, y, idx, wt, stream)
+        if evs:
+            evs[4].record(stream)
+
+    for i in range(args.warmup):
+        flush.fill_(i & 0xff)
+        step()
+    torch.cuda.synchronize()
+    if b.status() != 0:
+        raise RuntimeError("device status %d after warm-up" % b.status())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)        # between steps, outside the events
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    if b.status() != 0:
+        raise RuntimeError("device status %d after timed steps" % b.status())
+
+    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1])
+                          for j in range(4)] for i in range(args.steps)])
+    step_ms = stage_ms.sum(axis=1)
+    mean_step_ms = float(step_ms.mean())
+    max_step_ms = reduce_max(mean_step_ms, world, dev)
+    value = aggregate_tokens_per_s(w.T, world, max_step_ms / 1e3)
+    stage_mean = stage_ms.mean(axis=0)
+    ab = alg_bytes(w)
+    names = ["layout", "notify", "dispatch", "combine"]
+    peak, peak_kind = measured_peaks()
+    gbs = {n: ab[n] / (stage_mean[j] * 1e-3) / 1e9 for j, n in enumerate(names)}
+
+    # ---- end to end through the public API with host buffers --------------
+    e2e = run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush)
+    e2e_max_ms = reduce_max(e2e["ms_per_step"], world, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, idx_h, wt_h, x_h, y_h, args.cpu_seconds)
+
+    if rank != 0:
+        return None
+    comb_ms = float(stage_mean[3])
+    rec = {
+        "metric": "dispatch+combine tokens/s",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": max_step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": workload_desc(w),
+            "step": "layout+notify+dispatch+combine, inputs resident in HBM",
+            "l2": "flushed between steps (256 MiB write outside the step events)",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "io_dtype": "bf16" if w.dtype == W.BF16 else "fp16",
+            "recv_rows": "int8 + fp32 1/scale" if w.quant else "verbatim",
+        },
+        "roofline": {
+            "kernel": "combine",
+            "bound": "hbm",
+            "achieved": gbs["combine"],
+            "peak": peak,
+            "peak_source": peak_kind,
+            "unit": "GB/s",
+            "frac": gbs["combine"] / peak,
+            "traffic": recorded_traffic("combine", w.name),
+            "algorithmic_bytes": ab["combine"],
+            "avg_launch_ms": comb_ms,
+        },
+        "roofline_dispatch": {
+            "bound": "hbm", "achieved": gbs["dispatch"], "peak": peak,
+            "unit": "GB/s", "frac": gbs["dispatch"] / peak,
+            "traffic": recorded_traffic("dispatch", w.name),
+            "algorithmic_bytes": ab["dispatch"],
+            "avg_launch_ms": float(stage_mean[2]),
+        },
+        "stages_us": {n: float(stage_mean[j] * 1e3) for j, n in enumerate(names)},
+        "stages_gbs": gbs,
+        "dispatch_combine_tokens_per_s": w.T / ((stage_mean[2] + stage_mean[3]) * 1e-3),
+        "e2e": {"value": aggregate_tokens_per_s(w.T, world, e2e_max_ms / 1e3),
+                "unit": "tokens/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "ms_per_step": e2e_max_ms, "steps": e2e["steps"],
+                "note": "x, topk_idx, topk_weights copied from pinned host memory "
+                        "and out copied back inside the timed region; expert "
+                        "outputs y stay on the device (they are produced there)"},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+        "cpu_baseline": cpu,
+    }
+    return rec
+
+
+def run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush):
+    x_p = x_h.pin_memory()
+    idx_p = idx_h.pin_memory()
+    wt_p = wt_h.pin_memory()
+    out_p = torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory()
+    x_d = torch.empty_like(x_p, device=dev)
+    idx_d = torch.empty_like(idx_p, device=dev)
+    wt_d = torch.empty_like(wt_p, device=dev)
+    steps = max(3, min(args.steps, args.e2e_steps))
+
+    def one(e0=None, e1=None):
+        if e0 is not None:
+            e0.record(stream)
+        x_d.copy_(x_p, non_blocking=True)
+        idx_d.copy_(idx_p, non_blocking=True)
+        wt_d.copy_(wt_p, non_blocking=True)
+        pl.run_pipeline(b, x_d, idx_d, wt_d, y, stream)
+        out_p.copy_(b.out, non_blocking=True)
+        if e1 is not None:
+            e1.record(stream)
+
+    for i in range(max(3, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    ms = []
+    for i in range(steps):
+        flush.fill_(i & 0xff)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        one(e0, e1)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    if b.status() != 0:
+        raise RuntimeError("device status %d in e2e" % b.status())
+    h2d = (x_p.numel() * x_p.element_size() + idx_p.numel() * 4
+           + wt_p.numel() * 4)
+    d2h = out_p.numel() * out_p.element_size()
+    return {"ms_per_step": float(np.mean(ms)), "h2d": h2d, "d2h": d2h,
+            "steps": steps}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def _oracle_step(o, w, idx_np, wt_np, x_bits, y_bits, tokens):
+    """One bounded sample: layout + notify over the whole batch, then
+    dispatch and combine of the sampled tokens.  Returns seconds per phase."""
+    t0 = time.perf_counter()
+    L = o.layout(idx_np, w.R, w.epr)
+    N = o.notify(L["count"], w.R, w.bs, w.epr)
+    t1 = time.perf_counter()
+    o.dispatch_tokens(x_bits, idx_np, L["send_idx"], N["put_offset"],
+                      N["rank_recv_base"], w.R, w.epr, w.dtype, w.quant, tokens)
+    o.combine(y_bits, idx_np, wt_np, L["send_idx"], N["put_offset"],
+              N["rank_recv_base"], w.R, w.epr, w.dtype, tokens=tokens)
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1
+
+
+def _oracle_tokens_per_s(w, t_ln, t_dc, n):
+    """Full-batch tokens/s extrapolated from the sample: layout+notify ran on
+    all T tokens, dispatch+combine on n of them."""
+    return w.T / (t_ln + t_dc * w.T / n)
+
+
+def cpu_baseline(w, idx_h, wt_h, x_h, y_h, seconds):
+    import oracle as o
+    idx_np, wt_np = idx_h.numpy(), wt_h.numpy()
+    x_bits, y_bits = W.bits(x_h), W.bits(y_h)
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(w.T, size=min(w.T, 64), replace=False))
+    t_ln, t_dc = _oracle_step(o, w, idx_np, wt_np, x_bits, y_bits, probe)
+    per_tok = t_dc / len(probe)
+    n = int(min(w.T, max(64, (seconds - t_ln) / max(per_tok, 1e-9))))
+    tokens = np.sort(rng.choice(w.T, size=n, replace=False))
+    t_ln, t_dc = _oracle_step(o, w, idx_np, wt_np, x_bits, y_bits, tokens)
+    return {"value": _oracle_tokens_per_s(w, t_ln, t_dc, n), "unit": "tokens/s",
+            "cores": 1, "kind": "oracle",
+            "sample": "layout+notify on all %d tokens (%.3f s), dispatch+combine "
+                      "on %d random tokens (%.2f s), scaled to the full batch"
+                      % (w.T, t_ln, n, t_dc)}
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None                       # rank 0 alone runs the oracle
+    import oracle as o
+    idx_h, wt_h = W.routing(w)
+    x_h = W.tokens(w)
+    y_h = W.expert_outputs(w)
+    idx_np, wt_np = idx_h.numpy(), wt_h.numpy()
+    x_bits, y_bits = W.bits(x_h), W.bits(y_h)
+    rng = np.random.default_rng(1)
+    n = min(w.T, args.ref_tokens)
+    samples = [np.sort(rng.choice(w.T, size=n, replace=False))
+               for _ in range(args.warmup + args.steps)]
+    for i in range(args.warmup):
+        _oracle_step(o, w, idx_np, wt_np, x_bits, y_bits, samples[i])
+    secs = []
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        t_ln, t_dc = _oracle_step(o, w, idx_np, wt_np, x_bits, y_bits,
+                                  samples[args.warmup + i])
+        secs.append(t_ln + t_dc * w.T / n)
+    wall = time.perf_counter() - t0
+    step_s = float(np.mean(secs))
+    value = w.T / step_s
+    return {
+        "impl": "reference",
+        "metric": "dispatch+combine tokens/s",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(w),
+                   "step": "layout+notify+dispatch+combine (CPU oracle)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": "each step: layout+notify on all %d tokens, "
+                                   "dispatch+combine on %d random tokens, "
+                                   "scaled to the full batch" % (w.T, n)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+        "wall_s_timed_region": wall,
+    }
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--workload", default="dsv3", choices=W.ORDER)
+    p.add_argument("--impl", default="moe_ep", choices=["moe_ep", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=30)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--ref-tokens", type=int, default=32)
+    return p.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    w = W.WORKLOADS[args.workload]
+    world, rank, _ = dist_env()
+    if world != args.gpus and not (world == 1 and args.gpus == 1):
+        raise SystemExit("--gpus %d but WORLD_SIZE=%d; launch N>1 with torchrun"
+                         % (args.gpus, world))
+    rec = run_reference(args, w) if args.impl == "reference" else run_gpu(args, w)
+    if rec is not None and rank == 0:
+        print(json.dumps(rec), flush=True)
+    if args.impl != "reference" and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

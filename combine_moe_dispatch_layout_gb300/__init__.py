@@ -1,0 +1,202 @@
+"""Python binding of ``libmoe_ep.so`` (the C ABI in ``include/moe_ep.h``).
+
+Argument marshalling only: every stage runs in the library's sm_103a
+kernels.  Tensors must be CUDA tensors of the stated dtype, contiguous, on
+the current device; they are passed to the C ABI as raw device pointers
+with the current (or given) torch stream.  There is no CPU fallback: if the
+shared library has not been built, importing this package raises.
+
+Stages (UMDK/CAM deep analysis v2, section 2 "EP Normal"):
+``moe_dispatch_layout`` (2.3), ``moe_notify_dispatch`` (2.4),
+``moe_dispatch`` (2.5, optional INT8 quantisation), ``moe_combine`` (2.6).
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_ep.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_EXPERT_ID = 2
+MOE_ERR_CAPACITY = 3
+MOE_ERR_TIMEOUT = 4
+MOE_ERR_CUDA = 5
+MOE_ERR_WORKSPACE = 6
+MOE_BF16 = 0
+MOE_FP16 = 1
+
+_DTYPE = {torch.bfloat16: MOE_BF16, torch.float16: MOE_FP16}
+
+
+class moe_shape(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int32), ("bs", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("experts_per_rank", ctypes.c_int32),
+                ("H", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status, what):
+        super().__init__("%s: %s (status %d)" % (what, status_string(status),
+                                                 status))
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            "libmoe_ep.so is not built (%s); run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` first"
+            % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    sp = ctypes.POINTER(moe_shape)
+    L.moe_status_string.argtypes = [ctypes.c_int]
+    L.moe_status_string.restype = ctypes.c_char_p
+    L.moe_recv_row_bytes.argtypes = [sp, ctypes.c_int]
+    L.moe_recv_row_bytes.restype = i64
+    L.moe_layout_workspace_bytes.argtypes = [sp]
+    L.moe_layout_workspace_bytes.restype = ctypes.c_size_t
+    L.moe_dispatch_layout.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_notify_dispatch.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_dispatch.argtypes = [sp, vp, vp, vp, vp, vp, ctypes.c_int, vp, i64,
+                               vp, vp]
+    L.moe_combine.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+    for name in ("moe_dispatch_layout", "moe_notify_dispatch", "moe_dispatch",
+                 "moe_combine"):
+        getattr(L, name).restype = ctypes.c_int
+    return L
+
+
+_lib = _load()
+
+
+def lib():
+    """The loaded ``ctypes.CDLL`` of libmoe_ep.so."""
+    return _lib
+
+
+def make_shape(R, bs, k, experts_per_rank, H, dtype=MOE_BF16):
+    if isinstance(dtype, torch.dtype):
+        dtype = _DTYPE[dtype]
+    return moe_shape(int(R), int(bs), int(k), int(experts_per_rank), int(H),
+                     int(dtype))
+
+
+def status_string(status):
+    return _lib.moe_status_string(int(status)).decode()
+
+
+def recv_row_bytes(shape, quant):
+    return int(_lib.moe_recv_row_bytes(ctypes.byref(shape), int(bool(quant))))
+
+
+def layout_workspace_bytes(shape):
+    return int(_lib.moe_layout_workspace_bytes(ctypes.byref(shape)))
+
+
+def _ptr(t, dtype=None, numel=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype not in (
+            dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError("%s must have dtype %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if numel is not None and t.numel() < numel:
+        raise ValueError("%s holds %d elements, needs %d" % (name, t.numel(),
+                                                             numel))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status, what):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+    return status
+
+
+def moe_dispatch_layout(shape, topk_idx, count, rank_send, send_idx,
+                        workspace, dev_status, stream=None):
+    """Stage 1: counts per (source rank, expert), per (source, destination)
+    rank, and the stable send index of every (token, k) pair."""
+    R, E = shape.R, shape.R * shape.experts_per_rank
+    P = shape.R * shape.bs * shape.k
+    st = _lib.moe_dispatch_layout(
+        ctypes.byref(shape), _ptr(topk_idx, torch.int32, P, "topk_idx"),
+        _ptr(count, torch.int32, R * E, "count"),
+        _ptr(rank_send, torch.int32, R * R, "rank_send"),
+        _ptr(send_idx, torch.int32, P, "send_idx"),
+        _ptr(workspace, None, None, "workspace"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_dispatch_layout")
+
+
+def moe_notify_dispatch(shape, count, put_offset, total_recv, rank_recv_base,
+                        recv_per_expert, max_bs, dev_status, stream=None):
+    """Stage 2: putOffset (exclusive prefix per destination rank), receive
+    totals, partition bases, rows per expert and maxBs."""
+    R, E = shape.R, shape.R * shape.experts_per_rank
+    st = _lib.moe_notify_dispatch(
+        ctypes.byref(shape), _ptr(count, torch.int32, R * E, "count"),
+        _ptr(put_offset, torch.int32, E * R, "put_offset"),
+        _ptr(total_recv, torch.int32, R, "total_recv"),
+        _ptr(rank_recv_base, torch.int64, R + 1, "rank_recv_base"),
+        _ptr(recv_per_expert, torch.int32, E, "recv_per_expert"),
+        _ptr(max_bs, torch.int32, 1, "max_bs"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_notify_dispatch")
+
+
+def moe_dispatch(shape, x, topk_idx, send_idx, put_offset, rank_recv_base,
+                 quant, recv, recv_capacity_rows, dev_status, stream=None):
+    """Stage 3: scatter token rows (optionally INT8-quantised) into the
+    expert-grouped receive buffer."""
+    R, E = shape.R, shape.R * shape.experts_per_rank
+    T, P = shape.R * shape.bs, shape.R * shape.bs * shape.k
+    rb = recv_row_bytes(shape, quant)
+    if recv is not None and recv.numel() * recv.element_size() < \
+            rb * int(recv_capacity_rows):
+        raise ValueError("recv is smaller than recv_capacity_rows rows")
+    st = _lib.moe_dispatch(
+        ctypes.byref(shape),
+        _ptr(x, (torch.bfloat16, torch.float16), T * shape.H, "x"),
+        _ptr(topk_idx, torch.int32, P, "topk_idx"),
+        _ptr(send_idx, torch.int32, P, "send_idx"),
+        _ptr(put_offset, torch.int32, E * R, "put_offset"),
+        _ptr(rank_recv_base, torch.int64, R + 1, "rank_recv_base"),
+        int(bool(quant)),
+        _ptr(recv, None, None, "recv"), int(recv_capacity_rows),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_dispatch")
+
+
+def moe_combine(shape, expert_out, expert_out_rows, topk_idx, topk_weights,
+                send_idx, put_offset, rank_recv_base, out, dev_status,
+                stream=None):
+    """Stage 4: per token, the fp32 weighted sum of its k expert outputs,
+    rounded to the token dtype."""
+    R, E = shape.R, shape.R * shape.experts_per_rank
+    T, P = shape.R * shape.bs, shape.R * shape.bs * shape.k
+    st = _lib.moe_combine(
+        ctypes.byref(shape),
+        _ptr(expert_out, (torch.bfloat16, torch.float16),
+             int(expert_out_rows) * shape.H, "expert_out"),
+        int(expert_out_rows),
+        _ptr(topk_idx, torch.int32, P, "topk_idx"),
+        _ptr(topk_weights, torch.float32, P, "topk_weights"),
+        _ptr(send_idx, torch.int32, P, "send_idx"),
+        _ptr(put_offset, torch.int32, E * R, "put_offset"),
+        _ptr(rank_recv_base, torch.int64, R + 1, "rank_recv_base"),
+        _ptr(out, (torch.bfloat16, torch.float16), T * shape.H, "out"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_combine")

@@ -1,0 +1,152 @@
+// api.cu -- extern "C" entry points of libmoe_ep.so (declared in
+// include/moe_ep.h): argument validation, then one launch per stage.
+// Every check here is a host-side check; nothing touches the GPU before the
+// arguments have been accepted.
+#include <cstdint>
+
+#include "moe_ep_internal.cuh"
+
+namespace {
+
+using moe_ep::Shape;
+
+bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+// Shape limits of include/moe_ep.h.
+bool valid_shape(const moe_shape* sh, Shape* out) {
+  if (sh == nullptr) return false;
+  const int64_t R = sh->R, bs = sh->bs, k = sh->k, epr = sh->experts_per_rank,
+                H = sh->H;
+  if (R < 1 || R > MOE_EP_MAX_RANKS) return false;
+  if (epr < 1 || R * epr > MOE_EP_MAX_EXPERTS) return false;
+  if (k < 1 || k > MOE_EP_MAX_TOPK || k > R * epr) return false;
+  if (bs < 0 || R * bs * k >= (int64_t(1) << 31)) return false;
+  if (H < 8 || H > MOE_EP_MAX_HIDDEN || H % 8 != 0) return false;
+  if (sh->dtype != MOE_BF16 && sh->dtype != MOE_FP16) return false;
+  *out = Shape{int(R), int(bs), int(k), int(epr), int(H), int(sh->dtype)};
+  return true;
+}
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_EXPERT_ID: return "expert id out of range";
+    case MOE_ERR_CAPACITY: return "row outside the receive buffer";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_WORKSPACE: return "layout workspace not zero-filled or shared by overlapping calls";
+    default: return "unknown status";
+  }
+}
+
+int64_t moe_recv_row_bytes(const moe_shape* shape, int quant) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return -1;
+  return quant ? moe_ep::align_up(s.H, 32) + 32 : int64_t(s.H) * 2;
+}
+
+size_t moe_layout_workspace_bytes(const moe_shape* shape) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return 0;
+  return moe_ep::layout_workspace_bytes(s);
+}
+
+moe_status moe_dispatch_layout(const moe_shape* shape, const int32_t* topk_idx,
+                               int32_t* count, int32_t* rank_send,
+                               int32_t* send_idx, void* workspace,
+                               int32_t* dev_status, void* stream) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return MOE_ERR_INVALID_ARG;
+  if (!count || !rank_send || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (!aligned(count, 4) || !aligned(rank_send, 4) || !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (s.P() == 0) {
+    cudaError_t e = cudaMemsetAsync(count, 0, sizeof(int32_t) * size_t(s.R) * s.E(), st);
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(rank_send, 0, sizeof(int32_t) * size_t(s.R) * s.R, st);
+    return from_cuda(e);
+  }
+  if (!topk_idx || !send_idx || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(topk_idx, 4) || !aligned(send_idx, 4) || !aligned(workspace, 16))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_layout(s, topk_idx, count, rank_send, send_idx,
+                                         workspace, dev_status, st));
+}
+
+moe_status moe_notify_dispatch(const moe_shape* shape, const int32_t* count,
+                               int32_t* put_offset, int32_t* total_recv,
+                               int64_t* rank_recv_base,
+                               int32_t* recv_per_expert, int32_t* max_bs,
+                               int32_t* dev_status, void* stream) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return MOE_ERR_INVALID_ARG;
+  if (!count || !put_offset || !total_recv || !rank_recv_base ||
+      !recv_per_expert || !max_bs || !dev_status)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(count, 4) || !aligned(put_offset, 4) || !aligned(total_recv, 4) ||
+      !aligned(rank_recv_base, 8) || !aligned(recv_per_expert, 4) ||
+      !aligned(max_bs, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_notify(s, count, put_offset, total_recv,
+                                         rank_recv_base, recv_per_expert,
+                                         max_bs, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch(const moe_shape* shape, const void* x,
+                        const int32_t* topk_idx, const int32_t* send_idx,
+                        const int32_t* put_offset,
+                        const int64_t* rank_recv_base, int quant, void* recv,
+                        int64_t recv_capacity_rows, int32_t* dev_status,
+                        void* stream) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return MOE_ERR_INVALID_ARG;
+  if (recv_capacity_rows < 0 || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (s.T() == 0) return MOE_OK;
+  if (!x || !topk_idx || !send_idx || !put_offset || !rank_recv_base ||
+      (!recv && recv_capacity_rows > 0))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(topk_idx, 4) ||
+      !aligned(send_idx, 4) || !aligned(put_offset, 4) ||
+      !aligned(rank_recv_base, 8) || !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t row_bytes = quant ? moe_ep::align_up(s.H, 32) + 32 : int64_t(s.H) * 2;
+  return from_cuda(moe_ep::launch_dispatch(
+      s, x, topk_idx, send_idx, put_offset, rank_recv_base, quant != 0, recv,
+      row_bytes, recv_capacity_rows, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine(const moe_shape* shape, const void* expert_out,
+                       int64_t expert_out_rows, const int32_t* topk_idx,
+                       const float* topk_weights, const int32_t* send_idx,
+                       const int32_t* put_offset,
+                       const int64_t* rank_recv_base, void* out,
+                       int32_t* dev_status, void* stream) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return MOE_ERR_INVALID_ARG;
+  if (expert_out_rows < 0 || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (s.T() == 0) return MOE_OK;
+  if ((!expert_out && expert_out_rows > 0) || !topk_idx || !topk_weights ||
+      !send_idx || !put_offset || !rank_recv_base || !out)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(expert_out, 16) || !aligned(out, 16) || !aligned(topk_idx, 4) ||
+      !aligned(topk_weights, 4) || !aligned(send_idx, 4) ||
+      !aligned(put_offset, 4) || !aligned(rank_recv_base, 8) ||
+      !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_combine(s, expert_out, expert_out_rows,
+                                          topk_idx, topk_weights, send_idx,
+                                          put_offset, rank_recv_base, out,
+                                          dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,280 @@
+// layout.cu -- stage 1, dispatch layout (UMDK/CAM deep analysis v2, section
+// 2.3 moe_dispatch_layout_zb).
+//
+// The page counts tokens per rank/expert with cross-core atomics and a
+// SyncAll per round, then computes each pair's send index in a second pass.
+// Here one launch does both, deterministically, without order-dependent
+// atomics:
+//
+//   * the pairs of each source rank are cut into tiles of TILE pairs; a CTA
+//     takes the next tile from an atomic ticket, so a tile only ever waits
+//     for tiles that started before it (forward progress without assuming
+//     co-residency);
+//   * inside a tile each warp walks its contiguous 256-pair segment 32 pairs
+//     at a time; __match_any_sync groups the lanes holding the same expert,
+//     so a lane's rank inside the warp segment is a shared-memory counter
+//     plus the popcount of its lower group-mates (stable order);
+//   * a column scan over the 16 warp counters gives each warp's offset and
+//     the tile histogram;
+//   * decoupled look-back across the tiles of the same source rank turns the
+//     tile histograms into exclusive prefixes (vector-valued: one entry per
+//     expert).  Status words carry a per-launch epoch (the page's "magic"
+//     counter, section 2.2.2) so the workspace never needs clearing between
+//     calls; the last CTA to finish advances the epoch and resets the
+//     ticket.
+//
+// send_idx[p] = tile prefix[e] + warp offset[e] + rank in warp; the last tile
+// of each rank also writes count[s][:] and rank_send[s][:].
+#include "moe_ep_internal.cuh"
+
+namespace moe_ep {
+namespace {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRounds = 8;                       // 32-pair rounds per warp
+constexpr int kSegment = kRounds * 32;           // pairs per warp
+constexpr int kTile = kWarps * kSegment;         // pairs per tile (4096)
+
+constexpr uint32_t kStateAgg = 1;   // tile aggregate published
+constexpr uint32_t kStateInc = 2;   // inclusive prefix published
+constexpr uint32_t kSpinLimit = 1u << 22;   // ~0.3 s of 64 ns sleeps
+
+struct WsHeader {
+  uint32_t ticket;   // next tile id
+  uint32_t done;     // CTAs finished in this launch
+  uint32_t magic;    // launch counter; epoch = magic % 0x3fffffff + 1
+  uint32_t pad[13];
+};
+static_assert(sizeof(WsHeader) == 64, "header is one 64-byte line");
+
+struct WsView {
+  WsHeader* hdr;
+  uint32_t* status;   // [num_tiles]
+  int32_t* agg;       // [num_tiles][E]
+  int32_t* inc;       // [num_tiles][E]
+};
+
+__host__ __device__ inline WsView ws_view(void* ws, int num_tiles, int E) {
+  char* b = static_cast<char*>(ws);
+  WsView v;
+  v.hdr = reinterpret_cast<WsHeader*>(b);
+  v.status = reinterpret_cast<uint32_t*>(b + 64);
+  const int64_t vec_off = 64 + align_up(int64_t(num_tiles) * 4, 64);
+  v.agg = reinterpret_cast<int32_t*>(b + vec_off);
+  v.inc = v.agg + int64_t(num_tiles) * E;
+  return v;
+}
+
+__device__ __forceinline__ uint32_t make_status(uint32_t epoch, uint32_t st) {
+  return (epoch << 2) | st;
+}
+
+// Called by one thread of every CTA as its last action: the last CTA of the
+// launch advances the epoch (so this launch's status words look stale to the
+// next one) and resets the ticket and done counters.
+__device__ __forceinline__ void finish_launch(WsHeader* hdr, int num_tiles) {
+  __threadfence();
+  const uint32_t d = atomicAdd(&hdr->done, 1u);
+  if (d == static_cast<uint32_t>(num_tiles) - 1u) {
+    hdr->magic = hdr->magic + 1u;
+    hdr->ticket = 0u;
+    hdr->done = 0u;
+    __threadfence();
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+layout_kernel(const int32_t* __restrict__ topk_idx, int R, int epr,
+              int64_t pairs_per_rank, int tiles_per_rank, int num_tiles,
+              int32_t* __restrict__ count, int32_t* __restrict__ rank_send,
+              int32_t* __restrict__ send_idx, void* workspace,
+              int32_t* dev_status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int E = R * epr;
+  uint16_t* wcnt = reinterpret_cast<uint16_t*>(smem);            // [16][E]
+  int32_t* excl = reinterpret_cast<int32_t*>(smem + align_up(2 * kWarps * E, 16));
+  int32_t* tagg = excl + E;                                      // [E]
+  __shared__ uint32_t s_tile, s_epoch, s_state;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  WsView ws = ws_view(workspace, num_tiles, E);
+
+  if (tid == 0) {
+    s_tile = atomicAdd(&ws.hdr->ticket, 1u);
+    s_epoch = __ldcg(&ws.hdr->magic) % 0x3fffffffu + 1u;
+  }
+  for (int i = tid; i < kWarps * E / 2; i += kThreads)
+    reinterpret_cast<uint32_t*>(wcnt)[i] = 0u;
+  __syncthreads();
+
+  if (s_tile >= static_cast<uint32_t>(num_tiles)) {
+    // a ticket past the grid means the workspace was not zero-filled (or is
+    // shared with an overlapping call): touch nothing but the counters
+    if (tid == 0) {
+      set_status(dev_status, MOE_ERR_WORKSPACE);
+      finish_launch(ws.hdr, num_tiles);
+    }
+    return;
+  }
+  const int tile = static_cast<int>(s_tile);
+  const uint32_t epoch = s_epoch;
+  const int s = tile / tiles_per_rank;
+  const int c = tile - s * tiles_per_rank;
+  const int64_t p0 = int64_t(c) * kTile;
+  const int64_t p_end = min(p0 + kTile, pairs_per_rank);
+  const int32_t* idx_rank = topk_idx + int64_t(s) * pairs_per_rank;
+  int32_t* out_rank = send_idx + int64_t(s) * pairs_per_rank;
+  const int64_t seg0 = p0 + int64_t(warp) * kSegment;
+
+  // ---- per-warp stable ranks ------------------------------------------------
+  int ev[kRounds];
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int64_t p = seg0 + r * 32 + lane;
+    ev[r] = (p < p_end) ? __ldg(idx_rank + p) : -1;
+  }
+  int rk[kRounds];
+  const unsigned lt = lanemask_lt();
+  uint16_t* my_cnt = wcnt + warp * E;
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int64_t p = seg0 + r * 32 + lane;
+    const int e = ev[r];
+    const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+    if (p < p_end && !valid) set_status(dev_status, MOE_ERR_EXPERT_ID);
+    const int key = valid ? e : -1 - lane;   // invalid lanes never group
+    const unsigned grp = __match_any_sync(0xffffffffu, key);
+    const int lrank = __popc(grp & lt);
+    const int base = valid ? my_cnt[e] : 0;
+    __syncwarp();
+    if (valid && lrank == 0) my_cnt[e] = static_cast<uint16_t>(base + __popc(grp));
+    __syncwarp();
+    rk[r] = valid ? base + lrank : -1;
+  }
+  __syncthreads();
+
+  // ---- warp offsets and tile histogram ---------------------------------------
+  for (int e = tid; e < E; e += kThreads) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int v = wcnt[w * E + e];
+      wcnt[w * E + e] = static_cast<uint16_t>(run);
+      run += v;
+    }
+    tagg[e] = run;
+    excl[e] = 0;
+  }
+  __syncthreads();
+
+  // ---- decoupled look-back over the tiles of this source rank ---------------
+  if (tiles_per_rank > 1) {
+    int32_t* my_vec = (c == 0 ? ws.inc : ws.agg) + int64_t(tile) * E;
+    for (int e = tid; e < E; e += kThreads) my_vec[e] = tagg[e];
+    __threadfence();
+    __syncthreads();
+    if (tid == 0)
+      st_release_gpu(ws.status + tile, make_status(epoch, c == 0 ? kStateInc : kStateAgg));
+
+    if (c > 0) {
+      int pred = tile - 1;
+      while (true) {
+        if (tid == 0) {
+          uint32_t st = 0, spins = 0;
+          while (true) {
+            const uint32_t v = ld_acquire_gpu(ws.status + pred);
+            if ((v >> 2) == epoch && (v & 3u) != 0) { st = v & 3u; break; }
+            if (++spins >= kSpinLimit) break;
+            __nanosleep(64);
+          }
+          if (st == 0) set_status(dev_status, MOE_ERR_TIMEOUT);
+          s_state = st;
+        }
+        __syncthreads();
+        const uint32_t st = s_state;
+        if (st != 0) {
+          const int32_t* src = (st == kStateInc ? ws.inc : ws.agg) + int64_t(pred) * E;
+          for (int e = tid; e < E; e += kThreads) excl[e] += __ldcg(src + e);
+        }
+        __syncthreads();   // s_state is rewritten by the next iteration
+        if (st != kStateAgg) break;      // inclusive prefix found, or timeout
+        --pred;   // pred's own tile index in the rank is > 0 here, so pred-1 is still in rank s
+      }
+      if (c < tiles_per_rank - 1) {
+        int32_t* inc = ws.inc + int64_t(tile) * E;
+        for (int e = tid; e < E; e += kThreads) inc[e] = excl[e] + tagg[e];
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release_gpu(ws.status + tile, make_status(epoch, kStateInc));
+      }
+    }
+  }
+
+  // ---- send indices -----------------------------------------------------------
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int64_t p = seg0 + r * 32 + lane;
+    if (p < p_end) {
+      const int e = ev[r];
+      out_rank[p] = rk[r] < 0 ? -1 : excl[e] + my_cnt[e] + rk[r];
+    }
+  }
+
+  // ---- per-rank totals from the last tile of the rank -----------------------
+  if (c == tiles_per_rank - 1) {
+    for (int e = tid; e < E; e += kThreads) {
+      const int v = excl[e] + tagg[e];
+      count[int64_t(s) * E + e] = v;
+      tagg[e] = v;
+    }
+    __syncthreads();
+    for (int r = tid; r < R; r += kThreads) {
+      int sum = 0;
+      for (int j = 0; j < epr; ++j) sum += tagg[r * epr + j];
+      rank_send[int64_t(s) * R + r] = sum;
+    }
+  }
+
+  // ---- the last CTA out advances the epoch and resets the ticket -------------
+  __syncthreads();
+  if (tid == 0) finish_launch(ws.hdr, num_tiles);
+}
+
+int tiles_per_rank_of(const Shape& s) {
+  return static_cast<int>((int64_t(s.bs) * s.k + kTile - 1) / kTile);
+}
+
+size_t smem_bytes(int E) {
+  return static_cast<size_t>(align_up(2 * kWarps * E, 16) + 8 * int64_t(E));
+}
+
+}  // namespace
+
+size_t layout_workspace_bytes(const Shape& s) {
+  const int tpr = tiles_per_rank_of(s);
+  const int64_t num_tiles = int64_t(s.R) * tpr;
+  const int64_t vec = tpr > 1 ? 2 * num_tiles * s.E() * 4 : 0;
+  return static_cast<size_t>(64 + align_up(num_tiles * 4, 64) + vec);
+}
+
+cudaError_t launch_layout(const Shape& s, const int32_t* topk_idx,
+                          int32_t* count, int32_t* rank_send,
+                          int32_t* send_idx, void* workspace,
+                          int32_t* dev_status, cudaStream_t st) {
+  const int tpr = tiles_per_rank_of(s);
+  const int num_tiles = s.R * tpr;
+  const size_t smem = smem_bytes(s.E());
+  if (smem > 48 * 1024) {   // opt in to more than 48 KB (large E only)
+    cudaError_t e = cudaFuncSetAttribute(
+        layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  layout_kernel<<<num_tiles, kThreads, smem, st>>>(
+      topk_idx, s.R, s.epr, int64_t(s.bs) * s.k, tpr, num_tiles, count,
+      rank_send, send_idx, workspace, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe_ep

@@ -1,0 +1,129 @@
+// moe_ep_internal.cuh -- device helpers and launcher declarations shared by
+// the translation units of libmoe_ep.so (never by the CPU oracle).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_ep.h"
+
+namespace moe_ep {
+
+// ---- small utilities -------------------------------------------------------
+
+__host__ __device__ constexpr int64_t align_up(int64_t v, int64_t a) {
+  return (v + a - 1) / a * a;
+}
+
+// Records the first error of a launch sequence: 0 -> code, later codes lost.
+__device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
+  if (*reinterpret_cast<volatile int32_t*>(st) == 0) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Streaming 16-byte load that does not allocate in L1 (each x / expert-output
+// row is read by exactly one CTA).
+__device__ __forceinline__ uint4 ld_stream_16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// 16-bit float <-> fp32.  Widening is exact; narrowing is round to nearest
+// even (IEEE), subnormals kept.
+template <int DT>
+__device__ __forceinline__ float widen(uint32_t bits16);
+template <>
+__device__ __forceinline__ float widen<MOE_BF16>(uint32_t b) {
+  return __uint_as_float(b << 16);
+}
+template <>
+__device__ __forceinline__ float widen<MOE_FP16>(uint32_t b) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(b)));
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t narrow_rn(float f);
+template <>
+__device__ __forceinline__ uint32_t narrow_rn<MOE_BF16>(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+template <>
+__device__ __forceinline__ uint32_t narrow_rn<MOE_FP16>(float f) {
+  return __half_as_ushort(__float2half_rn(f));
+}
+
+// The 8 elements of a 16-byte chunk, widened to fp32.
+template <int DT>
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = widen<DT>(w[i] & 0xffffu);
+    f[2 * i + 1] = widen<DT>(w[i] >> 16);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = narrow_rn<DT>(f[2 * i]) | (narrow_rn<DT>(f[2 * i + 1]) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ---- launchers (one per translation unit) ----------------------------------
+
+struct Shape {
+  int R, bs, k, epr, H, dtype;
+  int E() const { return R * epr; }
+  int64_t T() const { return int64_t(R) * bs; }
+  int64_t P() const { return T() * k; }
+};
+
+size_t layout_workspace_bytes(const Shape& s);
+cudaError_t launch_layout(const Shape& s, const int32_t* topk_idx,
+                          int32_t* count, int32_t* rank_send,
+                          int32_t* send_idx, void* workspace,
+                          int32_t* dev_status, cudaStream_t st);
+
+cudaError_t launch_notify(const Shape& s, const int32_t* count,
+                          int32_t* put_offset, int32_t* total_recv,
+                          int64_t* rank_recv_base, int32_t* recv_per_expert,
+                          int32_t* max_bs, cudaStream_t st);
+
+cudaError_t launch_dispatch(const Shape& s, const void* x,
+                            const int32_t* topk_idx, const int32_t* send_idx,
+                            const int32_t* put_offset,
+                            const int64_t* rank_recv_base, bool quant,
+                            void* recv, int64_t row_bytes,
+                            int64_t capacity_rows, int32_t* dev_status,
+                            cudaStream_t st);
+
+cudaError_t launch_combine(const Shape& s, const void* y, int64_t y_rows,
+                           const int32_t* topk_idx, const float* weights,
+                           const int32_t* send_idx, const int32_t* put_offset,
+                           const int64_t* rank_recv_base, void* out,
+                           int32_t* dev_status, cudaStream_t st);
+
+}  // namespace moe_ep

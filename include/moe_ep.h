@@ -1,0 +1,177 @@
+/*
+ * moe_ep.h -- C ABI of libmoe_ep.so: the "EP Normal" MoE expert-parallel
+ * token pipeline on one GB300 GPU (sm_103a).
+ *
+ * The pipeline is the one the UMDK/CAM deep-analysis page (v2) describes in
+ * section 2 ("EP Normal" communication operators): (1) dispatch layout,
+ * (2) notify dispatch, (3) dispatch with optional dynamic INT8 quantisation,
+ * (4) combine (fp32 weighted sum).  The EP world of R ranks is modelled as R
+ * logical ranks whose buffers are partitions of one GPU's HBM, so the
+ * page's AllGather / shmem exchanges are ordinary global-memory traffic and
+ * its BarrierAll / magic-counter protocol (section 2.7) is replaced by
+ * stream order between the four calls.
+ *
+ * Notation: R ranks, epr experts per rank, E = R*epr experts, bs tokens per
+ * rank, T = R*bs tokens, k experts per token, P = T*k (token, k) pairs,
+ * H hidden size.  Token g = s*bs + t belongs to source rank s; expert e
+ * belongs to rank e / epr.
+ *
+ * Conventions for every entry point:
+ *  - All array arguments are DEVICE pointers, allocated and owned by the
+ *    caller; the library allocates nothing, keeps no global state, and
+ *    never synchronises.  Work is enqueued on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream) and returns immediately.
+ *  - Host-checkable problems (NULL or misaligned pointers, sizes out of
+ *    range) are reported synchronously by the return value and nothing is
+ *    enqueued.  A failed launch returns MOE_ERR_CUDA.
+ *  - Data-dependent problems found by a kernel (an expert id outside
+ *    [0,E), a row outside the receive buffer, a wait that timed out) are
+ *    written to *dev_status (an int32 in device memory that the caller sets
+ *    to 0 beforehand; the first error code wins) after the kernel skips the
+ *    offending writes.  Read it after the stream has been synchronised.
+ *  - Results are deterministic: integer outputs are bit-exact functions of
+ *    the inputs, and floating-point ones use a fixed operation order.
+ */
+#ifndef MOE_EP_H
+#define MOE_EP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* bad size, NULL or misaligned pointer */
+  MOE_ERR_EXPERT_ID = 2,   /* (device) an expert id outside [0, E) */
+  MOE_ERR_CAPACITY = 3,    /* (device) a row outside the receive buffer */
+  MOE_ERR_TIMEOUT = 4,     /* (device) a bounded wait gave up */
+  MOE_ERR_CUDA = 5,        /* a CUDA launch or runtime call failed */
+  MOE_ERR_WORKSPACE = 6    /* (device) the layout workspace was not zero-filled
+                              before first use, or overlapping calls share it */
+} moe_status;
+
+typedef enum { MOE_BF16 = 0, MOE_FP16 = 1 } moe_dtype;
+
+/* Limits.  R <= 384 is CAM_MAX_RANK_SIZE (comm_args.h, section 2.2.1). */
+#define MOE_EP_MAX_RANKS 384
+#define MOE_EP_MAX_EXPERTS 4096
+#define MOE_EP_MAX_TOPK 64
+#define MOE_EP_MAX_HIDDEN 65536
+
+/* Problem shape (the page's CommArgs fields rankSize, expertNumPerRank,
+ * topk, batchSize, hiddenSize; section 2.2.1).  Valid when
+ * 1 <= R <= 384, epr >= 1, E = R*epr <= 4096, 1 <= k <= min(E, 64),
+ * bs >= 0, T*k < 2^31, 8 <= H <= 65536 with H % 8 == 0, dtype a moe_dtype. */
+typedef struct {
+  int32_t R;
+  int32_t bs;
+  int32_t k;
+  int32_t experts_per_rank;
+  int32_t H;
+  int32_t dtype;
+} moe_shape;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* moe_status_string(int status);
+
+/* Bytes per receive row.  quant != 0: H int8 codes, zeros up to the next
+ * multiple of 32 bytes, the fp32 1/scale there, zeros to the end:
+ * align32(H) + 32 bytes (the page stores 1/scale at hUBAlignSize, with
+ * UB_ALIGN_SIZE = 32; section 2.5).  quant == 0: the row copied verbatim,
+ * 2*H bytes.  Returns -1 for an invalid shape. */
+int64_t moe_recv_row_bytes(const moe_shape* shape, int quant);
+
+/* Bytes of device workspace moe_dispatch_layout needs (0 for an invalid
+ * shape).  The workspace must be zero-filled once before its first use;
+ * every call leaves it ready for the next one.  Calls that share a
+ * workspace must not overlap on the GPU. */
+size_t moe_layout_workspace_bytes(const moe_shape* shape);
+
+/* (1) Dispatch layout -- moe_dispatch_layout_zb, section 2.3 (phase 1:
+ * per-rank/expert token counts; phase 2: send index of every pair).
+ *   topk_idx  int32 [R][bs][k]  expert id of each (token, k) pair (read)
+ *   count     int32 [R][E]      pairs of source rank s routed to expert e
+ *   rank_send int32 [R][R]      pairs of source rank s routed to rank r
+ *   send_idx  int32 [R][bs][k]  position of the pair among the pairs of its
+ *                               (source rank, expert), in (token, k) order
+ *   workspace moe_layout_workspace_bytes() bytes, 16-byte aligned
+ * An id outside [0,E) is not counted, gets send_idx -1, and sets
+ * MOE_ERR_EXPERT_ID.  A layout wait that exceeds its bound (~0.3 s)
+ * sets MOE_ERR_TIMEOUT; a workspace in an unexpected state sets
+ * MOE_ERR_WORKSPACE (the CTA that notices skips its tile).  One kernel
+ * launch (none when T*k == 0: count and rank_send are then zeroed with
+ * cudaMemsetAsync). */
+moe_status moe_dispatch_layout(const moe_shape* shape, const int32_t* topk_idx,
+                               int32_t* count, int32_t* rank_send,
+                               int32_t* send_idx, void* workspace,
+                               int32_t* dev_status, void* stream);
+
+/* (2) Notify -- moe_notify_dispatch_zb, section 2.4.  The AllGather of every
+ * rank's tokenPerExpert is the identity (count is already the whole R x E
+ * matrix); then BuildTotalRecvCount / BuildMaxBs / BuildTotalRecvTokens /
+ * BuildRecvTokenPerExp.
+ *   count           int32 [R][E]  from moe_dispatch_layout (read)
+ *   put_offset      int32 [E][R]  put_offset[e*R + s]: exclusive prefix sum,
+ *                                 per destination rank r = e/epr, of count
+ *                                 walked expert by expert and, inside an
+ *                                 expert, source rank by source rank (the
+ *                                 index the combine reads, section 2.6)
+ *   total_recv      int32 [R]     rows rank r receives
+ *   rank_recv_base  int64 [R+1]   first row of rank r's partition;
+ *                                 rank_recv_base[R] = total rows (= T*k
+ *                                 when every id is valid)
+ *   recv_per_expert int32 [E]     rows expert e receives
+ *   max_bs          int32 [1]     tokens per rank (bs)
+ * One launch (a cluster of 8 CTAs). */
+moe_status moe_notify_dispatch(const moe_shape* shape, const int32_t* count,
+                               int32_t* put_offset, int32_t* total_recv,
+                               int64_t* rank_recv_base,
+                               int32_t* recv_per_expert, int32_t* max_bs,
+                               int32_t* dev_status, void* stream);
+
+/* (3) Dispatch -- moe_dispatch_normal_zb + QuantProcess, section 2.5.
+ * Pair (g, k) with expert e goes to row
+ *     rank_recv_base[e/epr] + put_offset[e*R + s] + send_idx[g][k]
+ * of recv.  quant == 0 copies x[g] verbatim; quant != 0 writes the dynamic
+ * INT8 image: scale = 127 / (max|x[g]| + 1e-12f) in fp32 (IEEE division),
+ * q = round-half-even(x * scale), 1/scale after the codes (see
+ * moe_recv_row_bytes).
+ *   x          [T][H] bf16/fp16 (shape->dtype), 16-byte aligned (read)
+ *   topk_idx, send_idx, put_offset, rank_recv_base: as above (read)
+ *   recv       recv_capacity_rows rows of moe_recv_row_bytes(shape, quant)
+ *              bytes, 16-byte aligned
+ * A row >= recv_capacity_rows is skipped and sets MOE_ERR_CAPACITY; a bad
+ * id is skipped and sets MOE_ERR_EXPERT_ID.  Rows no pair maps to are left
+ * untouched.  One launch. */
+moe_status moe_dispatch(const moe_shape* shape, const void* x,
+                        const int32_t* topk_idx, const int32_t* send_idx,
+                        const int32_t* put_offset,
+                        const int64_t* rank_recv_base, int quant, void* recv,
+                        int64_t recv_capacity_rows, int32_t* dev_status,
+                        void* stream);
+
+/* (4) Combine -- moe_combine_normal_zb ReadBufferAndWeightedSum, section 2.6.
+ * For every token g and h: acc = 0.0f; for k = 0..K-1 in order:
+ *     acc = acc + (float(expert_out[row(g,k)][h]) * topk_weights[g][k])
+ * with each multiply and add rounded once (no FMA); out[g][h] = acc rounded
+ * to nearest even in the token dtype.  row(g,k) is the dispatch row.
+ *   expert_out   [expert_out_rows][H] bf16/fp16: the experts' outputs in the
+ *                same row positions as the dispatched rows, 16-byte aligned
+ *   topk_weights float [T][k] (read)
+ *   out          [T][H] bf16/fp16, 16-byte aligned
+ * A bad id or a row >= expert_out_rows contributes nothing and sets the
+ * matching status.  One launch. */
+moe_status moe_combine(const moe_shape* shape, const void* expert_out,
+                       int64_t expert_out_rows, const int32_t* topk_idx,
+                       const float* topk_weights, const int32_t* send_idx,
+                       const int32_t* put_offset,
+                       const int64_t* rank_recv_base, void* out,
+                       int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_EP_H */

@@ -46,6 +46,8 @@ def lib():
         L.oracle_dst_row.argtypes = [i, i, i, i, _i32p, _i32p, _i32p, _i64p,
                                      i64, i]
         L.oracle_dst_row.restype = i64
+        L.oracle_dst_rows.argtypes = [i, i, i, i, _i32p, _i32p, _i32p, _i64p,
+                                      _i64p]
         L.oracle_row_bytes.argtypes = [i, i]
         L.oracle_row_bytes.restype = i64
         L.oracle_quant_row.argtypes = [i, i, _u16p, _u8p]
@@ -162,12 +164,8 @@ def dst_rows(topk_idx, send_idx, put_offset, rank_recv_base, R, epr):
     T, k = idx.shape
     bs = T // R
     out = np.empty((T, k), np.int64)
-    L = lib()
-    for g in range(T):
-        for kk in range(k):
-            out[g, kk] = L.oracle_dst_row(R, bs, k, epr, _p(idx, _i32p),
-                                          _p(sidx, _i32p), _p(po, _i32p),
-                                          _p(base, _i64p), g, kk)
+    lib().oracle_dst_rows(R, bs, k, epr, _p(idx, _i32p), _p(sidx, _i32p),
+                          _p(po, _i32p), _p(base, _i64p), _p(out, _i64p))
     return out
 
 

@@ -175,6 +175,16 @@ int64_t oracle_dst_row(int R, int bs, int k, int epr, const int32_t* topk_idx,
          (int64_t)send_idx[p];
 }
 
+void oracle_dst_rows(int R, int bs, int k, int epr, const int32_t* topk_idx,
+                     const int32_t* send_idx, const int32_t* put_offset,
+                     const int64_t* rank_recv_base, int64_t* rows) {
+  const int64_t T = (int64_t)R * bs;
+  for (int64_t g = 0; g < T; ++g)
+    for (int kk = 0; kk < k; ++kk)
+      rows[g * k + kk] = oracle_dst_row(R, bs, k, epr, topk_idx, send_idx,
+                                        put_offset, rank_recv_base, g, kk);
+}
+
 int64_t oracle_row_bytes(int H, int quant) {
   if (quant) return (int64_t)((H + 31) / 32) * 32 + 32;
   return (int64_t)H * 2;

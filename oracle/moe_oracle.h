@@ -65,6 +65,11 @@ int64_t oracle_dst_row(int R, int bs, int k, int epr, const int32_t* topk_idx,
                        const int32_t* send_idx, const int32_t* put_offset,
                        const int64_t* rank_recv_base, int64_t g, int kk);
 
+/* oracle_dst_row for every pair: rows [T][k]. */
+void oracle_dst_rows(int R, int bs, int k, int epr, const int32_t* topk_idx,
+                     const int32_t* send_idx, const int32_t* put_offset,
+                     const int64_t* rank_recv_base, int64_t* rows);
+
 /* Bytes per receive row: quant -> align32(H) + 32, else H*2. */
 int64_t oracle_row_bytes(int H, int quant);
 
