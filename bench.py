@@ -485,6 +485,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--ref-tokens", type=int, default=32)
+    p.add_argument("--bs", type=int, default=None,
+                   help="override tokens per rank (small profiling cases)")
     return p.parse_args(argv)
 
 
@@ -493,6 +495,8 @@ def main(argv=None):
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     w = W.WORKLOADS[args.workload]
+    if args.bs is not None:
+        w = w.with_(bs=args.bs)
     world, rank, _ = dist_env()
     if world != args.gpus and not (world == 1 and args.gpus == 1):
         raise SystemExit("--gpus %d but WORLD_SIZE=%d; launch N>1 with torchrun"
