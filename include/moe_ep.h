@@ -109,6 +109,41 @@ moe_status moe_dispatch_layout(const moe_shape* shape, const int32_t* topk_idx,
                                int32_t* send_idx, void* workspace,
                                int32_t* dev_status, void* stream);
 
+/* Size of the scratch array behind moe_dispatch_layout_static (4 MiB). */
+#define MOE_EP_STATIC_LAYOUT_WS_BYTES (4u << 20)
+
+/* moe_dispatch_layout for callers that cannot allocate device memory.  (The
+ * paper has no counterpart: this is a convenience of this library.)
+ *
+ * Some callers have no way to call cudaMalloc: a plugin hosted by another
+ * runtime is handed only its input and output buffers and no allocator,
+ * and a serving loop whose device memory is reserved in full up front must
+ * not allocate on its hot path (cudaMalloc can synchronise the device and
+ * can fail under memory pressure).  This entry point takes the same
+ * arguments as moe_dispatch_layout minus the workspace and gives the same
+ * results.  The caller still passes (and owns) every input and output.
+ *
+ * Scratch: one file-scope device array of MOE_EP_STATIC_LAYOUT_WS_BYTES
+ * bytes inside the library, which every GPU that loads the library holds
+ * until the process exits.  A shape whose moe_layout_workspace_bytes()
+ * exceeds that size is rejected with MOE_ERR_INVALID_ARG and nothing is
+ * enqueued.  No call allocates or frees memory (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *
+ * The first call on each device does a one-time set-up with that device
+ * current: it looks up the array's device address (cudaGetSymbolAddress)
+ * and caches it; make that first call before any stream capture.  Every
+ * call then clears the part of the array it uses (cudaMemsetAsync on
+ * `stream`) and launches the layout kernel on it.  All calls share the one
+ * array, which keeps the last call's contents: calls that overlap on the
+ * GPU (different streams, or several host threads) race and must be
+ * serialised by the caller.  The current device must be the device of
+ * `stream`.  Returns MOE_ERR_CUDA if the set-up or the clear fails. */
+moe_status moe_dispatch_layout_static(const moe_shape* shape,
+                                      const int32_t* topk_idx, int32_t* count,
+                                      int32_t* rank_send, int32_t* send_idx,
+                                      int32_t* dev_status, void* stream);
+
 /* (2) Notify -- moe_notify_dispatch_zb, section 2.4.  The AllGather of every
  * rank's tokenPerExpert is the identity (count is already the whole R x E
  * matrix); then BuildTotalRecvCount / BuildMaxBs / BuildTotalRecvTokens /
