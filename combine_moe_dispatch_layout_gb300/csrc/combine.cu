@@ -4,13 +4,19 @@
 // Per token the page zeroes an fp32 accumulator, then for each of the k
 // experts in order reads the expert's output row from the destination rank
 // (shmem_ptr), casts it to fp32, multiplies by the gate weight (Muls) and
-// adds (Add), and finally casts back with round-to-nearest-even.  Here one
-// CTA owns one token; each thread owns 16-byte chunks of the hidden
-// dimension and issues the loads of up to 8 expert rows before doing any
-// arithmetic, so every thread keeps 8 x 16 bytes of the gather in flight.
-// The arithmetic is exactly the page's: acc = 0; acc = acc + (y * w) with
-// one rounding for the multiply and one for the add (__fmul_rn / __fadd_rn;
-// the translation unit is also compiled with -fmad=false); k in order.
+// adds (Add), and finally casts back with round-to-nearest-even.
+//
+// GB300 design: a persistent grid (as many CTAs as fit on the SMs) walks the
+// tokens.  The last warp of each CTA is a producer: while the compute warps
+// gather token g's k rows, it resolves token g+grid's rows (topk_idx ->
+// rank_recv_base / put_offset / send_idx, a chain of dependent loads) and
+// weights into the other half of a double-buffered shared table, so the
+// gather never waits on index arithmetic.  Each compute thread owns 16-byte
+// chunks of the hidden dimension and issues the loads of up to 8 expert
+// rows before doing any arithmetic.  The arithmetic is exactly the page's:
+// acc = 0; acc = acc + (y * w), one rounding for the multiply and one for
+// the add (__fmul_rn / __fadd_rn; the unit is also built with -fmad=false),
+// k in order; out = round-to-nearest-even in the token dtype.
 #include <algorithm>
 
 #include "moe_ep_internal.cuh"
@@ -18,77 +24,108 @@
 namespace moe_ep {
 namespace {
 
-constexpr int kBatch = 8;    // expert rows loaded before accumulating
-constexpr int kMaxCpt = 8;   // 16-byte chunks per thread (H <= 65536)
+constexpr int kBatch = 8;          // expert rows loaded before accumulating
+constexpr int kMaxThreads = 1024;
+
+// Resolve the rows and weights of token g into the shared tables (one warp).
+__device__ __forceinline__ void resolve_token(
+    int64_t g, const int32_t* __restrict__ topk_idx,
+    const float* __restrict__ weights, const int32_t* __restrict__ send_idx,
+    const int32_t* __restrict__ put_offset,
+    const int64_t* __restrict__ rank_recv_base, int R, int bs, int k, int epr,
+    int64_t y_rows, int64_t* rows, float* w, int32_t* dev_status, int lane) {
+  const int E = R * epr;
+  const int s = static_cast<int>(g / bs);
+  for (int kk = lane; kk < k; kk += 32) {
+    const int64_t pair = g * k + kk;
+    const int e = __ldg(topk_idx + pair);
+    const int32_t sidx = __ldg(send_idx + pair);
+    const float wt = __ldg(weights + pair);
+    int64_t row = -1;
+    if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+      set_status(dev_status, MOE_ERR_EXPERT_ID);
+    } else {
+      row = __ldg(rank_recv_base + e / epr) + __ldg(put_offset + int64_t(e) * R + s) + sidx;
+      if (row < 0 || row >= y_rows) {
+        set_status(dev_status, MOE_ERR_CAPACITY);
+        row = -1;
+      }
+    }
+    rows[kk] = row;
+    w[kk] = wt;
+  }
+}
 
 template <int DT>
-__global__ void __launch_bounds__(1024)
+__global__ void __launch_bounds__(kMaxThreads)
 combine_kernel(const uint4* __restrict__ y, int64_t y_rows,
                const int32_t* __restrict__ topk_idx,
                const float* __restrict__ weights,
                const int32_t* __restrict__ send_idx,
                const int32_t* __restrict__ put_offset,
                const int64_t* __restrict__ rank_recv_base, int R, int bs, int k,
-               int epr, int H, uint4* __restrict__ out, int32_t* dev_status) {
-  __shared__ int64_t s_rows[MOE_EP_MAX_TOPK];
-  __shared__ float s_w[MOE_EP_MAX_TOPK];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nthreads = blockDim.x;
-  const int64_t g = blockIdx.x;
-  const int s = static_cast<int>(g / bs);
+               int epr, int H, int64_t T, uint4* __restrict__ out,
+               int32_t* dev_status) {
+  __shared__ int64_t s_rows[2][MOE_EP_MAX_TOPK];
+  __shared__ float s_w[2][MOE_EP_MAX_TOPK];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int ncomp = blockDim.x - 32;            // compute threads
+  const bool producer = tid >= ncomp;           // the last warp
   const int nch = H / 8;
-  const int E = R * epr;
 
-  if (warp == 0) {
-    for (int kk = lane; kk < k; kk += 32) {
-      const int64_t pair = g * k + kk;
-      const int e = __ldg(topk_idx + pair);
-      int64_t row = -1;
-      if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
-        set_status(dev_status, MOE_ERR_EXPERT_ID);
-      } else {
-        row = __ldg(rank_recv_base + e / epr) +
-              __ldg(put_offset + int64_t(e) * R + s) + __ldg(send_idx + pair);
-        if (row < 0 || row >= y_rows) {
-          set_status(dev_status, MOE_ERR_CAPACITY);
-          row = -1;
-        }
-      }
-      s_rows[kk] = row;
-      s_w[kk] = __ldg(weights + pair);
-    }
-  }
+  int64_t g = blockIdx.x;
+  if (producer)
+    resolve_token(g, topk_idx, weights, send_idx, put_offset, rank_recv_base, R,
+                  bs, k, epr, y_rows, s_rows[0], s_w[0], dev_status, lane);
   __syncthreads();
 
+  for (int it = 0; g < T; ++it, g += gridDim.x) {
+    const int buf = it & 1;
+    if (producer) {
+      const int64_t gn = g + gridDim.x;
+      if (gn < T)
+        resolve_token(gn, topk_idx, weights, send_idx, put_offset, rank_recv_base,
+                      R, bs, k, epr, y_rows, s_rows[buf ^ 1], s_w[buf ^ 1],
+                      dev_status, lane);
+    } else {
+      const int64_t* rows = s_rows[buf];
+      const float* w = s_w[buf];
+      for (int c = tid; c < nch; c += ncomp) {
+        float acc[8];
 #pragma unroll
-  for (int i = 0; i < kMaxCpt; ++i) {
-    const int c = tid + i * nthreads;
-    if (c >= nch) break;
-    float acc[8];
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+        for (int k0 = 0; k0 < k; k0 += kBatch) {
+          uint4 v[kBatch];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
-    for (int k0 = 0; k0 < k; k0 += kBatch) {
-      uint4 v[kBatch];
+          for (int b = 0; b < kBatch; ++b) {
+            const int kk = k0 + b;
+            const int64_t row = kk < k ? rows[kk] : -1;
+            v[b] = row >= 0 ? ld_stream_16(y + row * nch + c) : make_uint4(0u, 0u, 0u, 0u);
+          }
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const int kk = k0 + b;
-        const int64_t row = kk < k ? s_rows[kk] : -1;
-        v[b] = row >= 0 ? ld_stream_16(y + row * nch + c) : make_uint4(0u, 0u, 0u, 0u);
-      }
+          for (int b = 0; b < kBatch; ++b) {
+            const int kk = k0 + b;
+            if (kk < k && rows[kk] >= 0) {
+              const float wk = w[kk];
+              float f[8];
+              unpack8<DT>(v[b], f);
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const int kk = k0 + b;
-        if (kk < k && s_rows[kk] >= 0) {
-          const float w = s_w[kk];
-          float f[8];
-          unpack8<DT>(v[b], f);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], __fmul_rn(f[j], w));
+              for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], __fmul_rn(f[j], wk));
+            }
+          }
         }
+        out[g * nch + c] = pack8<DT>(acc);
       }
     }
-    out[g * nch + c] = pack8<DT>(acc);
+    __syncthreads();   // this token's table is free, the next one is ready
   }
+}
+
+// Compute threads per CTA: about 4 chunks each, a multiple of 32, at most
+// 992 (plus the producer warp).
+int compute_threads(int nch) {
+  int t = ((nch + 3) / 4 + 31) / 32 * 32;
+  return std::max(32, std::min(kMaxThreads - 32, t));
 }
 
 template <int DT>
@@ -98,11 +135,17 @@ cudaError_t launch_t(const Shape& s, const void* y, int64_t y_rows,
                      const int64_t* rank_recv_base, void* out,
                      int32_t* dev_status, cudaStream_t st) {
   const int nch = s.H / 8;
-  int threads = std::max(32, std::min(1024, (nch + 31) / 32 * 32));
-  while ((nch + threads - 1) / threads > kMaxCpt) threads += 32;
-  combine_kernel<DT><<<static_cast<unsigned>(s.T()), threads, 0, st>>>(
+  const int threads = compute_threads(nch) + 32;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<DT>, threads, 0);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = std::min<int64_t>(s.T(), int64_t(std::max(1, per_sm)) * sms);
+  combine_kernel<DT><<<static_cast<unsigned>(grid), threads, 0, st>>>(
       static_cast<const uint4*>(y), y_rows, topk_idx, weights, send_idx,
-      put_offset, rank_recv_base, s.R, s.bs, s.k, s.epr, s.H,
+      put_offset, rank_recv_base, s.R, s.bs, s.k, s.epr, s.H, s.T(),
       static_cast<uint4*>(out), dev_status);
   return cudaGetLastError();
 }

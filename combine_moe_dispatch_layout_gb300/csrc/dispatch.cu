@@ -2,17 +2,28 @@
 // (UMDK/CAM deep analysis v2, section 2.5 moe_dispatch_normal_zb and
 // QuantProcess).
 //
-// The page moves each token row through the vector core's unified buffer
-// (MTE DMA in, vector quantise, DMA out to the peer's expandXOut).  Here one
-// CTA owns one token: its threads read the row once with 16-byte streaming
-// loads straight into registers, reduce max|x| with warp shuffles and one
-// shared-memory step, quantise in registers, and store the same image into
-// each of the token's k receive rows (k-fold write amplification is the
-// stage's inherent HBM cost; the read side is one pass over x).
+// The page moves each token row through the vector core's unified buffer:
+// MTE DMA in, vector quantise, DMA out to each destination's expandXOut.
+// The GB300 counterpart of that DMA engine is the TMA bulk-copy unit:
+//
+//   * a persistent grid walks the tokens; per CTA, x rows arrive in shared
+//     memory through cp.async.bulk loads issued one or two tokens ahead
+//     (double-buffered stages, mbarrier transaction counts);
+//   * INT8 path: compute warps reduce max|x| from shared memory (warp
+//     shuffles + one shared step), quantise into a staging row image (codes,
+//     zero pad, fp32 1/scale, zero pad), fence the async proxy, and one
+//     thread issues the k cp.async.bulk stores of that image to the token's
+//     k receive rows -- the k-fold write amplification costs the threads no
+//     store instructions;
+//   * verbatim path: one warp per CTA; the loaded x row is stored straight
+//     from shared memory to the k rows;
+//   * the last warp ("producer") resolves the receive rows of the next token
+//     (topk_idx -> rank_recv_base / put_offset / send_idx) while the current
+//     token is in flight.
 //
 // Quantisation, element by element: f = fp32(x) (exact); amax = max |f|;
-// scale = 127 / (amax + 1e-12f) with IEEE add and divide; q = round half to
-// even of (f * scale) (one fp32 multiply, then cvt.rni); |q| <= 127, so the
+// scale = 127 / (amax + 1e-12f), IEEE add and divide; q = round half to even
+// of (f * scale) (one fp32 multiply, then cvt.rni); |q| <= 127, so the
 // page's int32 -> int16 -> int8 casts are exact.  1/scale (IEEE divide) goes
 // to byte align32(H) of the row, every other byte after the codes is zero.
 #include <algorithm>
@@ -22,140 +33,312 @@
 namespace moe_ep {
 namespace {
 
-constexpr int kMaxCpt = 8;   // 16-byte chunks per thread (registers)
+constexpr int kMaxThreads = 1024;
+constexpr uint32_t kWaitLimit = 1u << 20;   // mbarrier polls before giving up
+constexpr int kSmemBudget = 200 * 1024;     // dynamic smem per CTA, upper bound
 
-// Destination row of pair (g, kk), -1 when the pair is skipped.
-__device__ __forceinline__ int64_t dst_row(
-    const int32_t* topk_idx, const int32_t* send_idx, const int32_t* put_offset,
-    const int64_t* rank_recv_base, int R, int epr, int s, int64_t pair,
-    int64_t capacity, int32_t* dev_status) {
+// Resolve the k receive rows of token g into rows[] (one warp).
+__device__ __forceinline__ void resolve_rows(
+    int64_t g, const int32_t* __restrict__ topk_idx,
+    const int32_t* __restrict__ send_idx, const int32_t* __restrict__ put_offset,
+    const int64_t* __restrict__ rank_recv_base, int R, int bs, int k, int epr,
+    int64_t capacity, int64_t* rows, int32_t* dev_status, int lane) {
   const int E = R * epr;
-  const int e = __ldg(topk_idx + pair);
-  if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
-    set_status(dev_status, MOE_ERR_EXPERT_ID);
-    return -1;
+  const int s = static_cast<int>(g / bs);
+  for (int kk = lane; kk < k; kk += 32) {
+    const int64_t pair = g * k + kk;
+    const int e = __ldg(topk_idx + pair);
+    const int32_t sidx = __ldg(send_idx + pair);
+    int64_t row = -1;
+    if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+      set_status(dev_status, MOE_ERR_EXPERT_ID);
+    } else {
+      row = __ldg(rank_recv_base + e / epr) + __ldg(put_offset + int64_t(e) * R + s) + sidx;
+      if (row < 0 || row >= capacity) {
+        set_status(dev_status, MOE_ERR_CAPACITY);
+        row = -1;
+      }
+    }
+    rows[kk] = row;
   }
-  const int64_t row = __ldg(rank_recv_base + e / epr) +
-                      __ldg(put_offset + int64_t(e) * R + s) +
-                      __ldg(send_idx + pair);
-  if (row < 0 || row >= capacity) {
-    set_status(dev_status, MOE_ERR_CAPACITY);
-    return -1;
-  }
-  return row;
 }
 
-template <int DT, bool QUANT>
-__global__ void __launch_bounds__(1024)
-dispatch_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ topk_idx,
-                const int32_t* __restrict__ send_idx,
-                const int32_t* __restrict__ put_offset,
-                const int64_t* __restrict__ rank_recv_base, int R, int bs, int k,
-                int epr, int H, unsigned char* __restrict__ recv,
-                int64_t row_bytes, int64_t capacity, int32_t* dev_status) {
-  __shared__ int64_t s_rows[MOE_EP_MAX_TOPK];
+struct SmemLayout {
+  int x_stride;    // bytes per x stage (16-byte multiple, 128-aligned)
+  int o_stride;    // bytes per staging row image
+  int bytes;       // total dynamic shared memory
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int H, int64_t row_bytes, int stages,
+                                                  bool quant) {
+  SmemLayout L;
+  L.x_stride = static_cast<int>(align_up(int64_t(H) * 2, 128));
+  L.o_stride = quant ? static_cast<int>(align_up(row_bytes, 128)) : 0;
+  L.bytes = stages * (L.x_stride + L.o_stride) + stages * 8;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// INT8 path
+// ---------------------------------------------------------------------------
+template <int DT, int S>
+__global__ void __launch_bounds__(kMaxThreads)
+dispatch_quant_kernel(const unsigned char* __restrict__ x,
+                      const int32_t* __restrict__ topk_idx,
+                      const int32_t* __restrict__ send_idx,
+                      const int32_t* __restrict__ put_offset,
+                      const int64_t* __restrict__ rank_recv_base, int R, int bs,
+                      int k, int epr, int H, int64_t T,
+                      unsigned char* __restrict__ recv, int64_t row_bytes,
+                      int64_t capacity, int32_t* dev_status) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int64_t s_rows[2][MOE_EP_MAX_TOPK];
   __shared__ float s_wmax[32];
+  __shared__ int s_abort;
+
+  const SmemLayout L = smem_layout(H, row_bytes, S, true);
+  unsigned char* xbuf = smem;
+  unsigned char* obuf = smem + S * L.x_stride;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + S * (L.x_stride + L.o_stride));
+
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nthreads = blockDim.x;
-  const int64_t g = blockIdx.x;
-  const int s = static_cast<int>(g / bs);
-  const int nch = H / 8;                        // 16-byte chunks per row
+  const int ncomp = blockDim.x - 32;
+  const int ncw = ncomp / 32;
+  const bool producer = tid >= ncomp;
+  const bool issuer = tid == ncomp;             // lane 0 of the producer warp
+  const int nch = H / 8;                        // 8-element chunks
+  const uint32_t xbytes = static_cast<uint32_t>(H) * 2u;
+  const int h_align = static_cast<int>(align_up(H, 32));
+  const int ntail = static_cast<int>((row_bytes - H) / 8);
+  const int inv_word = (h_align - H) / 8;
+  const int64_t grid = gridDim.x;
 
-  if (warp == 0) {
-    for (int kk = lane; kk < k; kk += 32)
-      s_rows[kk] = dst_row(topk_idx, send_idx, put_offset, rank_recv_base, R,
-                           epr, s, g * k + kk, capacity, dev_status);
+  int pend[2] = {-1, -1};   // issuer: parity of the load in flight per stage
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&mbar[s], 1);
+    fence_mbar_init();
+    s_abort = 0;
   }
-
-  uint4 v[kMaxCpt];
-  const uint4* xrow = x + g * nch;
-#pragma unroll
-  for (int i = 0; i < kMaxCpt; ++i) {
-    const int c = tid + i * nthreads;
-    v[i] = c < nch ? ld_stream_16(xrow + c) : make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  if (producer) {
+    if (issuer) {
+      for (int s = 0; s < S; ++s) {
+        const int64_t gs = blockIdx.x + s * grid;
+        if (gs < T) {
+          mbar_arrive_expect_tx(&mbar[s], xbytes);
+          bulk_load(xbuf + s * L.x_stride, x + gs * xbytes, xbytes, &mbar[s]);
+          pend[s] = 0;
+        }
+      }
+    }
+    resolve_rows(blockIdx.x, topk_idx, send_idx, put_offset, rank_recv_base, R, bs,
+                 k, epr, capacity, s_rows[0], dev_status, lane);
   }
+  __syncthreads();
 
-  if constexpr (QUANT) {
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kMaxCpt; ++i) {
-      if (tid + i * nthreads < nch) {
+  int it = 0;
+  for (int64_t g = blockIdx.x; g < T; ++it, g += grid) {
+    const int b = it % S;
+    const uint32_t parity = static_cast<uint32_t>(it / S) & 1u;
+    const unsigned char* xs = xbuf + b * L.x_stride;
+    unsigned char* os = obuf + b * L.o_stride;
+    if (producer) {
+      __syncwarp();   // the issuer is done reading the table refilled here
+      const int64_t gn = g + grid;
+      if (gn < T)
+        resolve_rows(gn, topk_idx, send_idx, put_offset, rank_recv_base, R, bs, k,
+                     epr, capacity, s_rows[(it + 1) & 1], dev_status, lane);
+      if (issuer) bulk_wait_read<S - 1>();   // staging image b is free again
+    } else {
+      if (!mbar_wait_bounded(&mbar[b], parity, kWaitLimit)) {
+        set_status(dev_status, MOE_ERR_TIMEOUT);
+        s_abort = 1;
+      }
+      float amax = 0.0f;
+      for (int c = tid; c < nch; c += ncomp) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xs + c * 16);
         float f[8];
-        unpack8<DT>(v[i], f);
+        unpack8<DT>(v, f);
 #pragma unroll
         for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
       }
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+      if (lane == 0) s_wmax[warp] = amax;
     }
+    __syncthreads();   // (A) maxima, abort flag and this token's rows visible
+    if (s_abort) break;
+    if (issuer) pend[b] = -1;   // consumed
+    if (!producer) {
+      float amax = s_wmax[0];
+      for (int w = 1; w < ncw; ++w) amax = fmaxf(amax, s_wmax[w]);
+      const float scale = __fdiv_rn(127.0f, __fadd_rn(amax, 1e-12f));
+      const float inv = __fdiv_rn(1.0f, scale);
+      for (int c = tid; c < nch; c += ncomp) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xs + c * 16);
+        float f[8];
+        unpack8<DT>(v, f);
+        uint32_t w2[2] = {0u, 0u};
 #pragma unroll
-    for (int d = 16; d > 0; d >>= 1)
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-    if (lane == 0) s_wmax[warp] = amax;
-    __syncthreads();
-    amax = s_wmax[0];
-    for (int w = 1; w < nthreads / 32; ++w) amax = fmaxf(amax, s_wmax[w]);
-    const float scale = __fdiv_rn(127.0f, __fadd_rn(amax, 1e-12f));
-    const float inv = __fdiv_rn(1.0f, scale);
-
-    uint2 q[kMaxCpt];
-#pragma unroll
-    for (int i = 0; i < kMaxCpt; ++i) {
-      float f[8];
-      unpack8<DT>(v[i], f);
-      uint32_t w[2] = {0u, 0u};
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int qi = __float2int_rn(__fmul_rn(f[j], scale));
-        w[j >> 2] |= (static_cast<uint32_t>(qi) & 0xffu) << (8 * (j & 3));
+        for (int j = 0; j < 8; ++j) {
+          const int q = __float2int_rn(__fmul_rn(f[j], scale));
+          w2[j >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (j & 3));
+        }
+        *reinterpret_cast<uint2*>(os + c * 8) = make_uint2(w2[0], w2[1]);
       }
-      q[i] = make_uint2(w[0], w[1]);
-    }
-    // tail: zero pad to align32(H), fp32 1/scale, zero pad to the row end
-    const int h_align = static_cast<int>(align_up(H, 32));
-    const int ntail = static_cast<int>((row_bytes - H) / 8);
-    const int inv_word = (h_align - H) / 8;
-    for (int kk = 0; kk < k; ++kk) {
-      const int64_t row = s_rows[kk];
-      if (row < 0) continue;
-      unsigned char* dst = recv + row * row_bytes;
-#pragma unroll
-      for (int i = 0; i < kMaxCpt; ++i) {
-        const int c = tid + i * nthreads;
-        if (c < nch) *reinterpret_cast<uint2*>(dst + int64_t(c) * 8) = q[i];
-      }
+      // zero pad to align32(H), fp32 1/scale, zero pad to the row end
       if (tid < ntail)
-        *reinterpret_cast<uint2*>(dst + H + 8 * tid) =
+        *reinterpret_cast<uint2*>(os + H + 8 * tid) =
             make_uint2(tid == inv_word ? __float_as_uint(inv) : 0u, 0u);
+      fence_proxy_async_smem();
     }
-  } else {
-    __syncthreads();   // s_rows
-    for (int kk = 0; kk < k; ++kk) {
-      const int64_t row = s_rows[kk];
-      if (row < 0) continue;
-      uint4* dst = reinterpret_cast<uint4*>(recv + row * row_bytes);
-#pragma unroll
-      for (int i = 0; i < kMaxCpt; ++i) {
-        const int c = tid + i * nthreads;
-        if (c < nch) dst[c] = v[i];
+    __syncthreads();   // (B) the image is complete; x stage b may be refilled
+    if (issuer) {
+      const int64_t* rows = s_rows[it & 1];
+      for (int kk = 0; kk < k; ++kk) {
+        const int64_t row = rows[kk];
+        if (row >= 0) bulk_store(recv + row * row_bytes, os, static_cast<uint32_t>(row_bytes));
+      }
+      bulk_commit();
+      const int64_t g2 = g + S * grid;
+      if (g2 < T) {
+        mbar_arrive_expect_tx(&mbar[b], xbytes);
+        bulk_load(xbuf + b * L.x_stride, x + g2 * xbytes, xbytes, &mbar[b]);
+        pend[b] = static_cast<int>(((it + S) / S) & 1);
       }
     }
   }
+
+  if (issuer) {
+    bulk_wait_all<0>();   // stores done before shared memory goes away
+    for (int s = 0; s < S; ++s)   // only after an abort: loads still in flight
+      if (pend[s] >= 0 && !mbar_wait_bounded(&mbar[s], pend[s], kWaitLimit))
+        set_status(dev_status, MOE_ERR_TIMEOUT);
+  }
 }
 
-template <int DT, bool QUANT>
-cudaError_t launch_t(const Shape& s, const void* x, const int32_t* topk_idx,
-                     const int32_t* send_idx, const int32_t* put_offset,
-                     const int64_t* rank_recv_base, void* recv,
-                     int64_t row_bytes, int64_t capacity, int32_t* dev_status,
-                     cudaStream_t st) {
+// ---------------------------------------------------------------------------
+// verbatim path: one warp per CTA, x rows copied to the k rows by TMA
+// ---------------------------------------------------------------------------
+template <int S>
+__global__ void __launch_bounds__(32)
+dispatch_copy_kernel(const unsigned char* __restrict__ x,
+                     const int32_t* __restrict__ topk_idx,
+                     const int32_t* __restrict__ send_idx,
+                     const int32_t* __restrict__ put_offset,
+                     const int64_t* __restrict__ rank_recv_base, int R, int bs,
+                     int k, int epr, int H, int64_t T,
+                     unsigned char* __restrict__ recv, int64_t row_bytes,
+                     int64_t capacity, int32_t* dev_status) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int64_t s_rows[MOE_EP_MAX_TOPK];
+  const SmemLayout L = smem_layout(H, row_bytes, S, false);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + S * L.x_stride);
+  const int lane = threadIdx.x;
+  const uint32_t xbytes = static_cast<uint32_t>(H) * 2u;
+  const int64_t grid = gridDim.x;
+  int pend[2] = {-1, -1};
+
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&mbar[s], 1);
+    fence_mbar_init();
+    for (int s = 0; s < S; ++s) {
+      const int64_t gs = blockIdx.x + s * grid;
+      if (gs < T) {
+        mbar_arrive_expect_tx(&mbar[s], xbytes);
+        bulk_load(smem + s * L.x_stride, x + gs * xbytes, xbytes, &mbar[s]);
+        pend[s] = 0;
+      }
+    }
+  }
+  __syncwarp();
+  int it = 0;
+  for (int64_t g = blockIdx.x; g < T; ++it, g += grid) {
+    const int b = it % S;
+    resolve_rows(g, topk_idx, send_idx, put_offset, rank_recv_base, R, bs, k, epr,
+                 capacity, s_rows, dev_status, lane);
+    __syncwarp();
+    int abort = 0;
+    if (lane == 0) {
+      if (!mbar_wait_bounded(&mbar[b], static_cast<uint32_t>(it / S) & 1u, kWaitLimit)) {
+        set_status(dev_status, MOE_ERR_TIMEOUT);
+        abort = 1;
+      } else {
+        pend[b] = -1;
+        for (int kk = 0; kk < k; ++kk)
+          if (s_rows[kk] >= 0)
+            bulk_store(recv + s_rows[kk] * row_bytes, smem + b * L.x_stride, xbytes);
+        bulk_commit();
+        bulk_wait_read<0>();   // stage b is read out; refill it
+        const int64_t g2 = g + S * grid;
+        if (g2 < T) {
+          mbar_arrive_expect_tx(&mbar[b], xbytes);
+          bulk_load(smem + b * L.x_stride, x + g2 * xbytes, xbytes, &mbar[b]);
+          pend[b] = static_cast<int>(((it + S) / S) & 1);
+        }
+      }
+    }
+    if (__shfl_sync(0xffffffffu, abort, 0)) break;
+    __syncwarp();   // s_rows is rewritten by the next iteration
+  }
+  if (lane == 0) {
+    bulk_wait_all<0>();
+    for (int s = 0; s < S; ++s)
+      if (pend[s] >= 0 && !mbar_wait_bounded(&mbar[s], pend[s], kWaitLimit))
+        set_status(dev_status, MOE_ERR_TIMEOUT);
+  }
+}
+
+// ---------------------------------------------------------------------------
+
+template <typename Kernel>
+cudaError_t launch_persistent(Kernel kernel, int threads, int smem, int64_t T,
+                              int* grid_out) {
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  *grid_out = static_cast<int>(std::min<int64_t>(T, int64_t(std::max(1, per_sm)) * sms));
+  return cudaSuccess;
+}
+
+template <int DT, int S>
+cudaError_t launch_quant(const Shape& s, const void* x, const int32_t* topk_idx,
+                         const int32_t* send_idx, const int32_t* put_offset,
+                         const int64_t* rank_recv_base, void* recv, int64_t row_bytes,
+                         int64_t capacity, int32_t* dev_status, cudaStream_t st) {
   const int nch = s.H / 8;
-  // about 2 chunks per thread: enough bytes in flight per SM without
-  // starving the amax reduction of threads
-  int threads = ((nch + 1) / 2 + 31) / 32 * 32;
-  threads = std::max(32, std::min(1024, threads));
-  while ((nch + threads - 1) / threads > kMaxCpt) threads += 32;   // H large
-  dispatch_kernel<DT, QUANT><<<static_cast<unsigned>(s.T()), threads, 0, st>>>(
-      static_cast<const uint4*>(x), topk_idx, send_idx, put_offset,
-      rank_recv_base, s.R, s.bs, s.k, s.epr, s.H,
+  const int ncomp = std::max(32, std::min(kMaxThreads - 32, ((nch + 3) / 4 + 31) / 32 * 32));
+  const int threads = ncomp + 32;
+  const int smem = smem_layout(s.H, row_bytes, S, true).bytes;
+  int grid = 0;
+  cudaError_t e = launch_persistent(dispatch_quant_kernel<DT, S>, threads, smem, s.T(), &grid);
+  if (e != cudaSuccess) return e;
+  dispatch_quant_kernel<DT, S><<<grid, threads, smem, st>>>(
+      static_cast<const unsigned char*>(x), topk_idx, send_idx, put_offset,
+      rank_recv_base, s.R, s.bs, s.k, s.epr, s.H, s.T(),
+      static_cast<unsigned char*>(recv), row_bytes, capacity, dev_status);
+  return cudaGetLastError();
+}
+
+template <int S>
+cudaError_t launch_copy(const Shape& s, const void* x, const int32_t* topk_idx,
+                        const int32_t* send_idx, const int32_t* put_offset,
+                        const int64_t* rank_recv_base, void* recv, int64_t row_bytes,
+                        int64_t capacity, int32_t* dev_status, cudaStream_t st) {
+  const int smem = smem_layout(s.H, row_bytes, S, false).bytes;
+  int grid = 0;
+  cudaError_t e = launch_persistent(dispatch_copy_kernel<S>, 32, smem, s.T(), &grid);
+  if (e != cudaSuccess) return e;
+  dispatch_copy_kernel<S><<<grid, 32, smem, st>>>(
+      static_cast<const unsigned char*>(x), topk_idx, send_idx, put_offset,
+      rank_recv_base, s.R, s.bs, s.k, s.epr, s.H, s.T(),
       static_cast<unsigned char*>(recv), row_bytes, capacity, dev_status);
   return cudaGetLastError();
 }
@@ -170,19 +353,26 @@ cudaError_t launch_dispatch(const Shape& s, const void* x,
                             int64_t capacity_rows, int32_t* dev_status,
                             cudaStream_t st) {
   if (s.T() == 0) return cudaSuccess;
+  // two stages (prefetch one token ahead) unless the rows are too wide
+  const bool two = smem_layout(s.H, row_bytes, 2, quant).bytes <= kSmemBudget;
+  if (!quant)
+    return two ? launch_copy<2>(s, x, topk_idx, send_idx, put_offset, rank_recv_base,
+                                recv, row_bytes, capacity_rows, dev_status, st)
+               : launch_copy<1>(s, x, topk_idx, send_idx, put_offset, rank_recv_base,
+                                recv, row_bytes, capacity_rows, dev_status, st);
   if (s.dtype == MOE_BF16)
-    return quant ? launch_t<MOE_BF16, true>(s, x, topk_idx, send_idx, put_offset,
-                                            rank_recv_base, recv, row_bytes,
-                                            capacity_rows, dev_status, st)
-                 : launch_t<MOE_BF16, false>(s, x, topk_idx, send_idx, put_offset,
-                                             rank_recv_base, recv, row_bytes,
-                                             capacity_rows, dev_status, st);
-  return quant ? launch_t<MOE_FP16, true>(s, x, topk_idx, send_idx, put_offset,
-                                          rank_recv_base, recv, row_bytes,
-                                          capacity_rows, dev_status, st)
-               : launch_t<MOE_FP16, false>(s, x, topk_idx, send_idx, put_offset,
+    return two ? launch_quant<MOE_BF16, 2>(s, x, topk_idx, send_idx, put_offset,
+                                           rank_recv_base, recv, row_bytes,
+                                           capacity_rows, dev_status, st)
+               : launch_quant<MOE_BF16, 1>(s, x, topk_idx, send_idx, put_offset,
                                            rank_recv_base, recv, row_bytes,
                                            capacity_rows, dev_status, st);
+  return two ? launch_quant<MOE_FP16, 2>(s, x, topk_idx, send_idx, put_offset,
+                                         rank_recv_base, recv, row_bytes, capacity_rows,
+                                         dev_status, st)
+             : launch_quant<MOE_FP16, 1>(s, x, topk_idx, send_idx, put_offset,
+                                         rank_recv_base, recv, row_bytes, capacity_rows,
+                                         dev_status, st);
 }
 
 }  // namespace moe_ep
