@@ -326,8 +326,9 @@ def run_gpu(args, w):
                 "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": e2e_max_ms, "steps": e2e["steps"],
-                "note": "x, topk_idx, topk_weights copied from pinned host memory "
-                        "and out copied back inside the timed region; expert "
+                "note": "every step copies x, topk_idx, topk_weights from pinned "
+                        "host memory and out back inside the timed region; copies "
+                        "of neighbouring steps overlap compute (3 streams); expert "
                         "outputs y stay on the device (they are produced there)"},
         "gpu_launches": 4 * args.steps,
         "clocks": clk,
@@ -338,43 +339,68 @@ def run_gpu(args, w):
 
 
 def run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush):
+    """Throughput through the public API with the inputs in pinned host
+    memory: every step copies x, topk_idx and topk_weights to the device,
+    runs the four stages and copies the output back.  Copies of neighbouring
+    steps overlap with compute (an H2D stream, the compute stream and a D2H
+    stream; inputs and outputs double-buffered), as a caller streaming
+    batches would run it."""
     x_p = x_h.pin_memory()
     idx_p = idx_h.pin_memory()
     wt_p = wt_h.pin_memory()
-    out_p = torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory()
-    x_d = torch.empty_like(x_p, device=dev)
-    idx_d = torch.empty_like(idx_p, device=dev)
-    wt_d = torch.empty_like(wt_p, device=dev)
+    outs_p = [torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory()
+              for _ in range(2)]
+    x_d = [torch.empty_like(x_p, device=dev) for _ in range(2)]
+    idx_d = [torch.empty_like(idx_p, device=dev) for _ in range(2)]
+    wt_d = [torch.empty_like(wt_p, device=dev) for _ in range(2)]
+    out_d = [b.out, torch.empty_like(b.out)]
+    s_h2d = torch.cuda.Stream(dev)
+    s_d2h = torch.cuda.Stream(dev)
     steps = max(3, min(args.steps, args.e2e_steps))
+    n_warm = max(3, args.warmup)
+    # per buffer slot: inputs consumed by compute / output drained by D2H
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
 
-    def one(e0=None, e1=None):
-        if e0 is not None:
-            e0.record(stream)
-        x_d.copy_(x_p, non_blocking=True)
-        idx_d.copy_(idx_p, non_blocking=True)
-        wt_d.copy_(wt_p, non_blocking=True)
-        pl.run_pipeline(b, x_d, idx_d, wt_d, y, stream)
-        out_p.copy_(b.out, non_blocking=True)
-        if e1 is not None:
-            e1.record(stream)
+    def one(i):
+        j = i % 2
+        with torch.cuda.stream(s_h2d):
+            if i >= 2:
+                s_h2d.wait_event(consumed[j])
+            x_d[j].copy_(x_p, non_blocking=True)
+            idx_d[j].copy_(idx_p, non_blocking=True)
+            wt_d[j].copy_(wt_p, non_blocking=True)
+            loaded = torch.cuda.Event()
+            loaded.record(s_h2d)
+        stream.wait_event(loaded)
+        if i >= 2:
+            stream.wait_event(drained[j])
+        b.out = out_d[j]
+        pl.run_pipeline(b, x_d[j], idx_d[j], wt_d[j], y, stream)
+        consumed[j].record(stream)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(consumed[j])
+            outs_p[j].copy_(out_d[j], non_blocking=True)
+            drained[j].record(s_d2h)
 
-    for i in range(max(3, args.warmup)):
-        one()
+    for i in range(n_warm):
+        one(i)
     torch.cuda.synchronize()
-    ms = []
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(s_h2d)
     for i in range(steps):
-        flush.fill_(i & 0xff)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        one(e0, e1)
-        e1.synchronize()
-        ms.append(e0.elapsed_time(e1))
+        one(n_warm + i)
+    s_d2h.wait_event(consumed[(n_warm + steps - 1) % 2])
+    e1.record(s_d2h)
+    torch.cuda.synchronize()
+    b.out = out_d[0]
     if b.status() != 0:
         raise RuntimeError("device status %d in e2e" % b.status())
     h2d = (x_p.numel() * x_p.element_size() + idx_p.numel() * 4
            + wt_p.numel() * 4)
-    d2h = out_p.numel() * out_p.element_size()
-    return {"ms_per_step": float(np.mean(ms)), "h2d": h2d, "d2h": d2h,
+    d2h = outs_p[0].numel() * outs_p[0].element_size()
+    return {"ms_per_step": e0.elapsed_time(e1) / steps, "h2d": h2d, "d2h": d2h,
             "steps": steps}
 
 
@@ -487,6 +513,9 @@ def parse_args(argv=None):
     p.add_argument("--ref-tokens", type=int, default=32)
     p.add_argument("--bs", type=int, default=None,
                    help="override tokens per rank (small profiling cases)")
+    p.add_argument("--hidden", type=int, default=None,
+                   help="override the hidden size (profiling the index stages "
+                        "at full pair count with small rows)")
     return p.parse_args(argv)
 
 
@@ -497,6 +526,8 @@ def main(argv=None):
     w = W.WORKLOADS[args.workload]
     if args.bs is not None:
         w = w.with_(bs=args.bs)
+    if args.hidden is not None:
+        w = w.with_(H=args.hidden)
     world, rank, _ = dist_env()
     if world != args.gpus and not (world == 1 and args.gpus == 1):
         raise SystemExit("--gpus %d but WORLD_SIZE=%d; launch N>1 with torchrun"

@@ -6,22 +6,28 @@
 // Here one launch does both, deterministically, without order-dependent
 // atomics:
 //
-//   * the pairs of each source rank are cut into tiles of TILE pairs; a CTA
-//     takes the next tile from an atomic ticket, so a tile only ever waits
-//     for tiles that started before it (forward progress without assuming
-//     co-residency);
-//   * inside a tile each warp walks its contiguous 256-pair segment 32 pairs
-//     at a time; __match_any_sync groups the lanes holding the same expert,
-//     so a lane's rank inside the warp segment is a shared-memory counter
-//     plus the popcount of its lower group-mates (stable order);
-//   * a column scan over the 16 warp counters gives each warp's offset and
-//     the tile histogram;
+//   * the pairs of each source rank are cut into tiles whose size follows the
+//     shape (one warp x 32 rounds of 32 pairs when a rank has at most 1024
+//     pairs, else eight warps x 16 rounds); a CTA takes the next tile from an
+//     atomic ticket, so a tile only ever waits for tiles that started before
+//     it (forward progress without assuming co-residency);
+//   * inside a tile each warp walks its contiguous segment 32 pairs at a
+//     time, all index loads issued up front; __match_any_sync groups the
+//     lanes holding the same expert, so a lane's rank inside the warp
+//     segment is a shared-memory counter plus the popcount of its lower
+//     group-mates (stable order);
+//   * a column scan over the warp counters gives each warp's offset and the
+//     tile histogram;
 //   * decoupled look-back across the tiles of the same source rank turns the
 //     tile histograms into exclusive prefixes (vector-valued: one entry per
-//     expert).  Status words carry a per-launch epoch (the page's "magic"
-//     counter, section 2.2.2) so the workspace never needs clearing between
-//     calls; the last CTA to finish advances the epoch and resets the
-//     ticket.
+//     expert).  One warp polls the status words of up to 32 predecessors at
+//     once; the nearest one that has published its inclusive prefix ends the
+//     walk, and every thread then adds the vectors in between in one pass.
+//     Status words carry a per-launch epoch (the page's "magic" counter,
+//     section 2.2.2) so the workspace never needs clearing between calls; the
+//     last CTA to finish advances the epoch and resets the ticket.  When a
+//     rank's pairs fit in one tile there is nothing to look back on and the
+//     workspace is not touched at all.
 //
 // send_idx[p] = tile prefix[e] + warp offset[e] + rank in warp; the last tile
 // of each rank also writes count[s][:] and rank_send[s][:].
@@ -29,12 +35,6 @@
 
 namespace moe_ep {
 namespace {
-
-constexpr int kWarps = 16;
-constexpr int kThreads = kWarps * 32;
-constexpr int kRounds = 8;                       // 32-pair rounds per warp
-constexpr int kSegment = kRounds * 32;           // pairs per warp
-constexpr int kTile = kWarps * kSegment;         // pairs per tile (4096)
 
 constexpr uint32_t kStateAgg = 1;   // tile aggregate published
 constexpr uint32_t kStateInc = 2;   // inclusive prefix published
@@ -84,15 +84,20 @@ __device__ __forceinline__ void finish_launch(WsHeader* hdr, int num_tiles) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
+template <int W, int ROUNDS>   // warps per CTA, 32-pair rounds per warp
+__global__ void __launch_bounds__(W * 32)
 layout_kernel(const int32_t* __restrict__ topk_idx, int R, int epr,
               int64_t pairs_per_rank, int tiles_per_rank, int num_tiles,
               int32_t* __restrict__ count, int32_t* __restrict__ rank_send,
               int32_t* __restrict__ send_idx, void* workspace,
               int32_t* dev_status) {
+  constexpr int kWarps = W;
+  constexpr int kThreads = W * 32;
+  constexpr int kSegment = ROUNDS * 32;     // pairs per warp
+  constexpr int kTile = W * kSegment;       // pairs per tile
   extern __shared__ __align__(16) unsigned char smem[];
   const int E = R * epr;
-  uint16_t* wcnt = reinterpret_cast<uint16_t*>(smem);            // [16][E]
+  uint16_t* wcnt = reinterpret_cast<uint16_t*>(smem);            // [W][E]
   int32_t* excl = reinterpret_cast<int32_t*>(smem + align_up(2 * kWarps * E, 16));
   int32_t* tagg = excl + E;                                      // [E]
   __shared__ uint32_t s_tile, s_epoch, s_state;
@@ -100,9 +105,15 @@ layout_kernel(const int32_t* __restrict__ topk_idx, int R, int epr,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   WsView ws = ws_view(workspace, num_tiles, E);
 
+  const bool chained = tiles_per_rank > 1;   // look-back needed
   if (tid == 0) {
-    s_tile = atomicAdd(&ws.hdr->ticket, 1u);
-    s_epoch = __ldcg(&ws.hdr->magic) % 0x3fffffffu + 1u;
+    if (chained) {
+      s_tile = atomicAdd(&ws.hdr->ticket, 1u);
+      s_epoch = __ldcg(&ws.hdr->magic) % 0x3fffffffu + 1u;
+    } else {
+      s_tile = blockIdx.x;   // independent tiles: no ordering needed
+      s_epoch = 0u;
+    }
   }
   for (int i = tid; i < kWarps * E / 2; i += kThreads)
     reinterpret_cast<uint32_t*>(wcnt)[i] = 0u;
@@ -128,27 +139,34 @@ layout_kernel(const int32_t* __restrict__ topk_idx, int R, int epr,
   const int64_t seg0 = p0 + int64_t(warp) * kSegment;
 
   // ---- per-warp stable ranks ------------------------------------------------
-  int ev[kRounds];
+  int ev[ROUNDS];
 #pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
+  for (int r = 0; r < ROUNDS; ++r) {
     const int64_t p = seg0 + r * 32 + lane;
     ev[r] = (p < p_end) ? __ldg(idx_rank + p) : -1;
   }
-  int rk[kRounds];
+  // lane groups of equal experts, all rounds first (independent of each other)
+  unsigned grp[ROUNDS];
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    const int64_t p = seg0 + r * 32 + lane;
+    const bool valid = static_cast<unsigned>(ev[r]) < static_cast<unsigned>(E);
+    if (p < p_end && !valid) set_status(dev_status, MOE_ERR_EXPERT_ID);
+    if (!valid) ev[r] = -1 - lane;   // invalid lanes never group
+    grp[r] = __match_any_sync(0xffffffffu, ev[r]);
+  }
+  // then the running per-warp counters, round by round
+  int rk[ROUNDS];
   const unsigned lt = lanemask_lt();
   uint16_t* my_cnt = wcnt + warp * E;
 #pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
-    const int64_t p = seg0 + r * 32 + lane;
+  for (int r = 0; r < ROUNDS; ++r) {
     const int e = ev[r];
-    const bool valid = static_cast<unsigned>(e) < static_cast<unsigned>(E);
-    if (p < p_end && !valid) set_status(dev_status, MOE_ERR_EXPERT_ID);
-    const int key = valid ? e : -1 - lane;   // invalid lanes never group
-    const unsigned grp = __match_any_sync(0xffffffffu, key);
-    const int lrank = __popc(grp & lt);
+    const bool valid = e >= 0;
+    const int lrank = __popc(grp[r] & lt);
     const int base = valid ? my_cnt[e] : 0;
     __syncwarp();
-    if (valid && lrank == 0) my_cnt[e] = static_cast<uint16_t>(base + __popc(grp));
+    if (valid && lrank == 0) my_cnt[e] = static_cast<uint16_t>(base + __popc(grp[r]));
     __syncwarp();
     rk[r] = valid ? base + lrank : -1;
   }
@@ -156,12 +174,14 @@ layout_kernel(const int32_t* __restrict__ topk_idx, int R, int epr,
 
   // ---- warp offsets and tile histogram ---------------------------------------
   for (int e = tid; e < E; e += kThreads) {
+    int v[kWarps];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) v[w] = wcnt[w * E + e];
     int run = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const int v = wcnt[w * E + e];
-      wcnt[w * E + e] = static_cast<uint16_t>(run);
-      run += v;
+      if (kWarps > 1) wcnt[w * E + e] = static_cast<uint16_t>(run);
+      run += v[w];
     }
     tagg[e] = run;
     excl[e] = 0;
@@ -169,7 +189,7 @@ layout_kernel(const int32_t* __restrict__ topk_idx, int R, int epr,
   __syncthreads();
 
   // ---- decoupled look-back over the tiles of this source rank ---------------
-  if (tiles_per_rank > 1) {
+  if (chained) {
     int32_t* my_vec = (c == 0 ? ws.inc : ws.agg) + int64_t(tile) * E;
     for (int e = tid; e < E; e += kThreads) my_vec[e] = tagg[e];
     __threadfence();
@@ -178,30 +198,72 @@ layout_kernel(const int32_t* __restrict__ topk_idx, int R, int epr,
       st_release_gpu(ws.status + tile, make_status(epoch, c == 0 ? kStateInc : kStateAgg));
 
     if (c > 0) {
-      int pred = tile - 1;
+      const int first = tile - c;    // tile 0 of this rank (always publishes INC)
+      int hi = tile - 1;             // newest predecessor not yet added
       while (true) {
-        if (tid == 0) {
-          uint32_t st = 0, spins = 0;
-          while (true) {
-            const uint32_t v = ld_acquire_gpu(ws.status + pred);
-            if ((v >> 2) == epoch && (v & 3u) != 0) { st = v & 3u; break; }
-            if (++spins >= kSpinLimit) break;
+        // warp 0: lane j watches tile hi - j until it has published something
+        if (warp == 0) {
+          const int t = hi - lane;
+          const bool mine = t >= first;
+          uint32_t st = 0;
+          bool ok = true;
+          for (uint32_t spins = 0;; ++spins) {
+            if (mine && st == 0) {
+              const uint32_t v = ld_acquire_gpu(ws.status + t);
+              if ((v >> 2) == epoch && (v & 3u) != 0) st = v & 3u;
+            }
+            if (__all_sync(0xffffffffu, !mine || st != 0)) break;
+            if (spins >= kSpinLimit) { ok = false; break; }
             __nanosleep(64);
           }
-          if (st == 0) set_status(dev_status, MOE_ERR_TIMEOUT);
-          s_state = st;
+          const unsigned inc = __ballot_sync(0xffffffffu, mine && st == kStateInc);
+          const int nvalid = min(32, hi - first + 1);
+          if (lane == 0) {   // ok is warp-uniform: the loop exits together
+            if (!ok) {
+              set_status(dev_status, MOE_ERR_TIMEOUT);
+              s_state = 0x40000000u;                        // give up
+            } else {
+              // the nearest inclusive prefix ends the walk; otherwise all 32
+              s_state = inc ? static_cast<uint32_t>(__ffs(inc) - 1) | 0x80000000u
+                            : static_cast<uint32_t>(nvalid - 1);
+            }
+          }
         }
         __syncthreads();
-        const uint32_t st = s_state;
-        if (st != 0) {
-          const int32_t* src = (st == kStateInc ? ws.inc : ws.agg) + int64_t(pred) * E;
-          for (int e = tid; e < E; e += kThreads) excl[e] += __ldcg(src + e);
+        const uint32_t sv = s_state;
+        if (sv & 0x40000000u) break;                      // timed out
+        const int last = static_cast<int>(sv & 0x3fffffffu);   // lanes 0..last
+        const bool found = (sv & 0x80000000u) != 0;
+        // add vectors hi .. hi-last; this thread's (vector, expert) loads are
+        // flattened and issued eight at a time so they overlap in flight
+        const int slots = (E + kThreads - 1) / kThreads;   // experts per thread
+        const int nload = (last + 1) * slots;
+        for (int q0 = 0; q0 < nload; q0 += 8) {
+          int v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int q = q0 + u;
+            const int j = q / slots, e = tid + (q - j * slots) * kThreads;
+            v[u] = 0;
+            if (q < nload && e < E) {
+              const int32_t* src = (found && j == last ? ws.inc : ws.agg) + int64_t(hi - j) * E;
+              v[u] = __ldcg(src + e);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int q = q0 + u;
+            const int j = q / slots, e = tid + (q - j * slots) * kThreads;
+            if (q < nload && e < E) excl[e] += v[u];
+          }
         }
-        __syncthreads();   // s_state is rewritten by the next iteration
-        if (st != kStateAgg) break;      // inclusive prefix found, or timeout
-        --pred;   // pred's own tile index in the rank is > 0 here, so pred-1 is still in rank s
+        __syncthreads();   // s_state is rewritten by the next window
+        if (found) break;
+        hi -= 32;
       }
-      if (c < tiles_per_rank - 1) {
+      // successors whose 32-tile window reaches tile 0 never need this
+      // tile's inclusive prefix
+      if (c < tiles_per_rank - 1 && tiles_per_rank > 33) {
         int32_t* inc = ws.inc + int64_t(tile) * E;
         for (int e = tid; e < E; e += kThreads) inc[e] = excl[e] + tagg[e];
         __threadfence();
@@ -213,11 +275,11 @@ layout_kernel(const int32_t* __restrict__ topk_idx, int R, int epr,
 
   // ---- send indices -----------------------------------------------------------
 #pragma unroll
-  for (int r = 0; r < kRounds; ++r) {
+  for (int r = 0; r < ROUNDS; ++r) {
     const int64_t p = seg0 + r * 32 + lane;
     if (p < p_end) {
       const int e = ev[r];
-      out_rank[p] = rk[r] < 0 ? -1 : excl[e] + my_cnt[e] + rk[r];
+      out_rank[p] = rk[r] < 0 ? -1 : excl[e] + (kWarps > 1 ? my_cnt[e] : 0) + rk[r];
     }
   }
 
@@ -237,16 +299,52 @@ layout_kernel(const int32_t* __restrict__ topk_idx, int R, int epr,
   }
 
   // ---- the last CTA out advances the epoch and resets the ticket -------------
-  __syncthreads();
-  if (tid == 0) finish_launch(ws.hdr, num_tiles);
+  if (chained) {
+    __syncthreads();
+    if (tid == 0) finish_launch(ws.hdr, num_tiles);
+  }
+}
+
+// Tile geometry from the pairs per rank: (warps, rounds) with tile =
+// warps * rounds * 32 pairs.
+struct Geometry {
+  int warps, rounds;
+  int tile() const { return warps * rounds * 32; }
+};
+
+Geometry geometry_of(const Shape& s) {
+  const int64_t per_rank = int64_t(s.bs) * s.k;
+  if (per_rank <= 256) return {1, 8};
+  if (per_rank <= 1024) return {1, 32};
+  return {8, 16};
 }
 
 int tiles_per_rank_of(const Shape& s) {
-  return static_cast<int>((int64_t(s.bs) * s.k + kTile - 1) / kTile);
+  const int64_t tile = geometry_of(s).tile();
+  return static_cast<int>((int64_t(s.bs) * s.k + tile - 1) / tile);
 }
 
-size_t smem_bytes(int E) {
-  return static_cast<size_t>(align_up(2 * kWarps * E, 16) + 8 * int64_t(E));
+size_t smem_bytes(int warps, int E) {
+  return static_cast<size_t>(align_up(2 * int64_t(warps) * E, 16) + 8 * int64_t(E));
+}
+
+template <int W, int ROUNDS>
+cudaError_t launch_t(const Shape& s, const int32_t* topk_idx, int32_t* count,
+                     int32_t* rank_send, int32_t* send_idx, void* workspace,
+                     int32_t* dev_status, cudaStream_t st) {
+  const int tpr = tiles_per_rank_of(s);
+  const int num_tiles = s.R * tpr;
+  const size_t smem = smem_bytes(W, s.E());
+  if (smem > 48 * 1024) {   // opt in to more than 48 KB (large E only)
+    cudaError_t e = cudaFuncSetAttribute(layout_kernel<W, ROUNDS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  layout_kernel<W, ROUNDS><<<num_tiles, W * 32, smem, st>>>(
+      topk_idx, s.R, s.epr, int64_t(s.bs) * s.k, tpr, num_tiles, count,
+      rank_send, send_idx, workspace, dev_status);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -262,19 +360,12 @@ cudaError_t launch_layout(const Shape& s, const int32_t* topk_idx,
                           int32_t* count, int32_t* rank_send,
                           int32_t* send_idx, void* workspace,
                           int32_t* dev_status, cudaStream_t st) {
-  const int tpr = tiles_per_rank_of(s);
-  const int num_tiles = s.R * tpr;
-  const size_t smem = smem_bytes(s.E());
-  if (smem > 48 * 1024) {   // opt in to more than 48 KB (large E only)
-    cudaError_t e = cudaFuncSetAttribute(
-        layout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
-  layout_kernel<<<num_tiles, kThreads, smem, st>>>(
-      topk_idx, s.R, s.epr, int64_t(s.bs) * s.k, tpr, num_tiles, count,
-      rank_send, send_idx, workspace, dev_status);
-  return cudaGetLastError();
+  const Geometry g = geometry_of(s);
+  if (g.warps == 1 && g.rounds == 8)
+    return launch_t<1, 8>(s, topk_idx, count, rank_send, send_idx, workspace, dev_status, st);
+  if (g.warps == 1)
+    return launch_t<1, 32>(s, topk_idx, count, rank_send, send_idx, workspace, dev_status, st);
+  return launch_t<8, 16>(s, topk_idx, count, rank_send, send_idx, workspace, dev_status, st);
 }
 
 }  // namespace moe_ep

@@ -160,7 +160,9 @@ moe_status moe_dispatch_layout_static(const moe_shape* shape,
  *                                 when every id is valid)
  *   recv_per_expert int32 [E]     rows expert e receives
  *   max_bs          int32 [1]     tokens per rank (bs)
- * One launch (a cluster of 8 CTAs). */
+ * One launch when R <= 64; otherwise two: a per-destination-rank scan (one
+ * warp per rank, spread over many SMs), then a one-CTA scan of the rank
+ * totals. */
 moe_status moe_notify_dispatch(const moe_shape* shape, const int32_t* count,
                                int32_t* put_offset, int32_t* total_recv,
                                int64_t* rank_recv_base,
