@@ -1,0 +1,86 @@
+"""bench.py's multi-rank host logic on CPU with gloo, world size 2.
+
+With N GPUs the benchmark runs N independent replicas of the pipeline (one
+per rank, no data-path collective); ranks only meet in a barrier and a
+max-reduction of the step time, and rank 0 reports the whole-job
+throughput.  These tests run that host logic with two gloo ranks, and the
+reference arm (the CPU oracle) under torchrun with two ranks.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port),
+                      RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch
+    import bench
+    w, r, _ = bench.dist_env()
+    bench.init_dist(w, "gloo")
+    bench.barrier(w)
+    step_ms = [1.5, 2.5][rank]            # rank 1 is the slow one
+    mx = bench.reduce_max(step_ms, w)
+    tps = bench.aggregate_tokens_per_s(32768, w, mx / 1e3)
+    out.put((rank, mx, tps))
+    torch.distributed.destroy_process_group()
+
+
+def test_reduce_max_and_aggregate_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [2.5, 2.5]          # both see the max
+    # whole job: 2 replicas x 32768 tokens over the slowest rank's 2.5 ms
+    assert res[0][2] == pytest.approx(2 * 32768 / 2.5e-3)
+
+
+def test_single_rank_helpers():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.reduce_max(3.0, 1) == 3.0
+    assert bench.aggregate_tokens_per_s(100, 1, 0.5) == 200.0
+    b = bench.alg_bytes(__import__("workloads").WORKLOADS["dsv3"])
+    assert b["combine"] == 4231004160          # P*H*2 + P*12 + T*H*2
+    assert b["dispatch"] == (32768 * 7168 * 2 + 262144 * 7200 + 262144 * 8
+                             + 256 * 8 * 4 + 9 * 8)
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           "--nproc-per-node=2", "--master-addr=127.0.0.1",
+           "--master-port=%d" % port, os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--workload", "tiny",
+           "--steps", "3", "--warmup", "3"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300,
+                       cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1                     # rank 0 alone prints
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2
+    assert rec["value"] > 0 and rec["e2e"]["h2d_bytes_per_step"] == 0
+    assert rec["cpu_baseline"]["kind"] == "oracle"

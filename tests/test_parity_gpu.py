@@ -273,3 +273,33 @@ def test_combine_ulp_bar_documented(oracle_mod, pl):
     b, ref = _check_full(oracle_mod, pl, w)
     got = b.out.view(torch.int16).cpu().numpy().view(np.uint16)
     assert _ulp_diff_bf16(got, ref["out"]).max() <= 1
+
+
+def test_unzeroed_workspace_is_reported_and_recovers(oracle_mod, ep, pl):
+    """Failure detection without a fault: a layout workspace whose ticket
+    counter is not zero (the caller broke the zero-fill contract) makes tile
+    0 never run.  Its successors' waits for tile 0 run out (bounded), the
+    CTA that draws the out-of-range ticket reports MOE_ERR_WORKSPACE and
+    touches nothing, and every CTA still reaches the end-of-launch
+    bookkeeping, which resets the workspace: the next call is correct."""
+    import time
+    w = W.Workload("ws_bad", R=2, epr=8, bs=4096, k=4, H=64)   # 4 tiles/rank
+    idx, _ = W.routing(w)
+    shape = ep.make_shape(w.R, w.bs, w.k, w.epr, w.H)
+    b = pl.PipelineBuffers(w.R, w.bs, w.k, w.epr, w.H, w.dtype, w.quant)
+    b.workspace[0:4] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8)  # ticket = 1
+    t0 = time.time()
+    ep.moe_dispatch_layout(shape, idx.cuda(), b.count, b.rank_send, b.send_idx,
+                           b.workspace, b.dev_status)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 30
+    assert b.status() in (ep.MOE_ERR_WORKSPACE, ep.MOE_ERR_TIMEOUT)
+    # recovery: same workspace, fresh status
+    b.dev_status.zero_()
+    ep.moe_dispatch_layout(shape, idx.cuda(), b.count, b.rank_send, b.send_idx,
+                           b.workspace, b.dev_status)
+    torch.cuda.synchronize()
+    assert b.status() == 0
+    L = oracle_mod.layout(idx.numpy(), w.R, w.epr)
+    _eq("send_idx", b.send_idx, L["send_idx"])
+    _eq("count", b.count, L["count"])
