@@ -38,7 +38,7 @@ namespace {
 
 constexpr uint32_t kStateAgg = 1;   // tile aggregate published
 constexpr uint32_t kStateInc = 2;   // inclusive prefix published
-constexpr uint32_t kSpinLimit = 1u << 22;   // ~0.3 s of 64 ns sleeps
+constexpr uint32_t kSpinLimit = 1u << 20;   // polls (an L2 round trip each): ~1 s
 
 struct WsHeader {
   uint32_t ticket;   // next tile id

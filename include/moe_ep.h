@@ -99,7 +99,7 @@ size_t moe_layout_workspace_bytes(const moe_shape* shape);
  *                               (source rank, expert), in (token, k) order
  *   workspace moe_layout_workspace_bytes() bytes, 16-byte aligned
  * An id outside [0,E) is not counted, gets send_idx -1, and sets
- * MOE_ERR_EXPERT_ID.  A layout wait that exceeds its bound (~0.3 s)
+ * MOE_ERR_EXPERT_ID.  A layout wait that exceeds its bound (about 1 s)
  * sets MOE_ERR_TIMEOUT; a workspace in an unexpected state sets
  * MOE_ERR_WORKSPACE (the CTA that notices skips its tile).  One kernel
  * launch (none when T*k == 0: count and rank_send are then zeroed with
