@@ -62,10 +62,11 @@ def alg_bytes(w):
     dispatch = (w.T * w.H * es + w.P * row_bytes(w) + w.P * 8
                 + w.E * w.R * 4 + (w.R + 1) * 8)
     combine = w.P * w.H * es + w.P * 12 + w.T * w.H * es
+    combine_quant = w.P * row_bytes(w.with_(quant=True)) + w.P * 12 + w.T * w.H * es
     layout = w.P * 8 + w.R * w.E * 4 + w.R * w.R * 4
     notify = 2 * w.R * w.E * 4 + w.E * 4 + w.R * 4 + (w.R + 1) * 8
     return dict(layout=layout, notify=notify, dispatch=dispatch,
-                combine=combine)
+                combine=combine, combine_quant=combine_quant)
 
 
 def workload_desc(w):
@@ -268,6 +269,32 @@ def run_gpu(args, w):
     peak, peak_kind = measured_peaks()
     gbs = {n: ab[n] / (stage_mean[j] * 1e-3) / 1e9 for j, n in enumerate(names)}
 
+    # ---- combine over INT8 expert outputs (moe_combine_quant) -------------
+    cq = None
+    if w.quant:
+        yq = W.expert_outputs_int8(w).to(dev)
+        for i in range(3):
+            pl.run_combine_quant(b, yq, idx, wt, stream)
+        cq_ms = []
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            pl.run_combine_quant(b, yq, idx, wt, stream)
+            c1.record(stream)
+            cq_ms.append((c0, c1))
+        torch.cuda.synchronize()
+        if b.status() != 0:
+            raise RuntimeError("device status %d in combine_quant" % b.status())
+        cq_us = float(np.mean([a.elapsed_time(c) for a, c in cq_ms])) * 1e3
+        cq_bytes = alg_bytes(w)["combine_quant"]
+        cq = {"us": cq_us, "achieved_gbs": cq_bytes / (cq_us * 1e-6) / 1e9,
+              "algorithmic_bytes": cq_bytes,
+              "frac": cq_bytes / (cq_us * 1e-6) / 1e9 / peak,
+              "tokens_per_s": w.T / (cq_us * 1e-6)}
+        del yq
+
     # ---- end to end through the public API with host buffers --------------
     e2e = run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush)
     e2e_max_ms = reduce_max(e2e["ms_per_step"], world, dev)
@@ -319,6 +346,7 @@ def run_gpu(args, w):
             "algorithmic_bytes": ab["dispatch"],
             "avg_launch_ms": float(stage_mean[2]),
         },
+        "combine_quant": cq,
         "stages_us": {n: float(stage_mean[j] * 1e3) for j, n in enumerate(names)},
         "stages_gbs": gbs,
         "dispatch_combine_tokens_per_s": w.T / ((stage_mean[2] + stage_mean[3]) * 1e-3),

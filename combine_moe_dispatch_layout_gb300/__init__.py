@@ -64,8 +64,9 @@ def _load():
     L.moe_dispatch.argtypes = [sp, vp, vp, vp, vp, vp, ctypes.c_int, vp, i64,
                                vp, vp]
     L.moe_combine.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_combine_quant.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     for name in ("moe_dispatch_layout", "moe_notify_dispatch", "moe_dispatch",
-                 "moe_combine"):
+                 "moe_combine", "moe_combine_quant"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -200,3 +201,27 @@ def moe_combine(shape, expert_out, expert_out_rows, topk_idx, topk_weights,
         _ptr(out, (torch.bfloat16, torch.float16), T * shape.H, "out"),
         _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
     return _check(st, "moe_combine")
+
+
+def moe_combine_quant(shape, expert_out_q, expert_out_rows, topk_idx,
+                      topk_weights, send_idx, put_offset, rank_recv_base, out,
+                      dev_status, stream=None):
+    """Stage 4 over INT8 expert outputs (row images with 1/scale):
+    dequantise, then the same weighted sum as moe_combine."""
+    R, E = shape.R, shape.R * shape.experts_per_rank
+    T, P = shape.R * shape.bs, shape.R * shape.bs * shape.k
+    rb = recv_row_bytes(shape, True)
+    if expert_out_q is not None and \
+            expert_out_q.numel() * expert_out_q.element_size() < rb * int(expert_out_rows):
+        raise ValueError("expert_out_q is smaller than expert_out_rows rows")
+    st = _lib.moe_combine_quant(
+        ctypes.byref(shape), _ptr(expert_out_q, None, None, "expert_out_q"),
+        int(expert_out_rows),
+        _ptr(topk_idx, torch.int32, P, "topk_idx"),
+        _ptr(topk_weights, torch.float32, P, "topk_weights"),
+        _ptr(send_idx, torch.int32, P, "send_idx"),
+        _ptr(put_offset, torch.int32, E * R, "put_offset"),
+        _ptr(rank_recv_base, torch.int64, R + 1, "rank_recv_base"),
+        _ptr(out, (torch.bfloat16, torch.float16), T * shape.H, "out"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_combine_quant")

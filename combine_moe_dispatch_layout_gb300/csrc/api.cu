@@ -149,4 +149,27 @@ moe_status moe_combine(const moe_shape* shape, const void* expert_out,
                                           dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_combine_quant(const moe_shape* shape, const void* expert_out_q,
+                             int64_t expert_out_rows, const int32_t* topk_idx,
+                             const float* topk_weights, const int32_t* send_idx,
+                             const int32_t* put_offset,
+                             const int64_t* rank_recv_base, void* out,
+                             int32_t* dev_status, void* stream) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return MOE_ERR_INVALID_ARG;
+  if (expert_out_rows < 0 || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (s.T() == 0) return MOE_OK;
+  if ((!expert_out_q && expert_out_rows > 0) || !topk_idx || !topk_weights ||
+      !send_idx || !put_offset || !rank_recv_base || !out)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(expert_out_q, 16) || !aligned(out, 16) || !aligned(topk_idx, 4) ||
+      !aligned(topk_weights, 4) || !aligned(send_idx, 4) ||
+      !aligned(put_offset, 4) || !aligned(rank_recv_base, 8) ||
+      !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_combine_quant(
+      s, expert_out_q, expert_out_rows, topk_idx, topk_weights, send_idx, put_offset,
+      rank_recv_base, out, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -202,6 +202,12 @@ cudaError_t launch_dispatch(const Shape& s, const void* x,
                             int64_t capacity_rows, int32_t* dev_status,
                             cudaStream_t st);
 
+cudaError_t launch_combine_quant(const Shape& s, const void* yq, int64_t y_rows,
+                                 const int32_t* topk_idx, const float* weights,
+                                 const int32_t* send_idx, const int32_t* put_offset,
+                                 const int64_t* rank_recv_base, void* out,
+                                 int32_t* dev_status, cudaStream_t st);
+
 cudaError_t launch_combine(const Shape& s, const void* y, int64_t y_rows,
                            const int32_t* topk_idx, const float* weights,
                            const int32_t* send_idx, const int32_t* put_offset,

@@ -9,8 +9,9 @@ synchronisation is needed between the stages.
 """
 import torch
 
-from . import (make_shape, layout_workspace_bytes, moe_combine, moe_dispatch,
-               moe_dispatch_layout, moe_notify_dispatch, recv_row_bytes)
+from . import (make_shape, layout_workspace_bytes, moe_combine,
+               moe_combine_quant, moe_dispatch, moe_dispatch_layout,
+               moe_notify_dispatch, recv_row_bytes)
 
 
 class PipelineBuffers:
@@ -62,6 +63,13 @@ def run_dispatch(b, x, topk_idx, stream=None):
 def run_combine(b, y, topk_idx, topk_weights, stream=None):
     moe_combine(b.shape, y, y.shape[0], topk_idx, topk_weights, b.send_idx,
                 b.put_offset, b.rank_recv_base, b.out, b.dev_status, stream)
+
+
+def run_combine_quant(b, yq, topk_idx, topk_weights, stream=None):
+    """Combine over INT8 expert outputs (row images, 1/scale per row)."""
+    moe_combine_quant(b.shape, yq, yq.shape[0], topk_idx, topk_weights,
+                      b.send_idx, b.put_offset, b.rank_recv_base, b.out,
+                      b.dev_status, stream)
 
 
 def run_pipeline(b, x, topk_idx, topk_weights, y, stream=None):

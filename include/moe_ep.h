@@ -208,6 +208,24 @@ moe_status moe_combine(const moe_shape* shape, const void* expert_out,
                        const int64_t* rank_recv_base, void* out,
                        int32_t* dev_status, void* stream);
 
+/* (4') Combine over INT8 expert outputs -- the "+ dequant" of the pipeline
+ * diagram (section 2.1, stage 4: shmem read + weighted sum + dequant).
+ * Same gather and arithmetic as moe_combine, except that each expert-output
+ * row is an INT8 row image in the layout moe_dispatch writes
+ * (moe_recv_row_bytes(shape, 1) bytes: H int8 codes, fp32 1/scale at byte
+ * align32(H)), dequantised element by element as float(q) * (1/scale) (one
+ * fp32 rounding) before acc = acc + (y * w).  The page prints no dequant
+ * code; that order is the reading taken.
+ *   expert_out_q  [expert_out_rows][moe_recv_row_bytes(shape, 1)] bytes,
+ *                 16-byte aligned
+ *   other arguments as moe_combine.  One launch. */
+moe_status moe_combine_quant(const moe_shape* shape, const void* expert_out_q,
+                             int64_t expert_out_rows, const int32_t* topk_idx,
+                             const float* topk_weights, const int32_t* send_idx,
+                             const int32_t* put_offset,
+                             const int64_t* rank_recv_base, void* out,
+                             int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -59,6 +59,9 @@ def lib():
         L.oracle_combine_tokens.argtypes = [i, i, i, i, i, i, _u16p, i64,
                                             _i32p, _f32p, _i32p, _i32p,
                                             _i64p, _i64p, i64, _u16p]
+        L.oracle_combine_quant_tokens.argtypes = [i, i, i, i, i, i, _u8p, i64,
+                                                  _i32p, _f32p, _i32p, _i32p,
+                                                  _i64p, _i64p, i64, _u16p]
         _lib = L
     return _lib
 
@@ -239,6 +242,31 @@ def combine(y_bits, topk_idx, topk_weights, send_idx, put_offset,
     out = np.zeros((n, H), np.uint16)
     st = lib().oracle_combine_tokens(
         R, bs, k, epr, H, dtype, _p(y, _u16p), y.shape[0], _p(idx, _i32p),
+        _p(w, _f32p), _p(_c(send_idx, np.int32), _i32p),
+        _p(_c(put_offset, np.int32), _i32p),
+        _p(_c(rank_recv_base, np.int64), _i64p),
+        None if toks is None else _p(toks, _i64p), n, _p(out, _u16p))
+    return out, st
+
+
+def combine_quant(yq, topk_idx, topk_weights, send_idx, put_offset,
+                  rank_recv_base, R, epr, dtype, H, tokens=None):
+    """Combine over INT8 expert outputs (uint8 [rows, align32(H)+32] row
+    images).  Returns (out uint16 [n, H], status)."""
+    yq = _c(yq, np.uint8)
+    idx = _c(topk_idx, np.int32)
+    w = _c(topk_weights, np.float32)
+    T, k = idx.shape
+    bs = T // R
+    assert yq.ndim == 2 and yq.shape[1] == row_bytes(H, 1)
+    if tokens is None:
+        toks, n = None, T
+    else:
+        toks = _c(tokens, np.int64)
+        n = toks.size
+    out = np.zeros((n, H), np.uint16)
+    st = lib().oracle_combine_quant_tokens(
+        R, bs, k, epr, H, dtype, _p(yq, _u8p), yq.shape[0], _p(idx, _i32p),
         _p(w, _f32p), _p(_c(send_idx, np.int32), _i32p),
         _p(_c(put_offset, np.int32), _i32p),
         _p(_c(rank_recv_base, np.int64), _i64p),

@@ -342,3 +342,51 @@ int oracle_combine_tokens(int R, int bs, int k, int epr, int H, int dtype,
   free(acc);
   return status;
 }
+
+/* ---- combine over INT8 expert outputs (section 2.1 "+ dequant") ---------- */
+
+int oracle_combine_quant_tokens(int R, int bs, int k, int epr, int H, int dtype,
+                                const uint8_t* yq, int64_t y_rows,
+                                const int32_t* topk_idx,
+                                const float* topk_weights,
+                                const int32_t* send_idx,
+                                const int32_t* put_offset,
+                                const int64_t* rank_recv_base,
+                                const int64_t* tokens, int64_t ntok,
+                                uint16_t* out) {
+  const int64_t T = (int64_t)R * bs;
+  const int64_t S = oracle_row_bytes(H, 1);
+  const int64_t h_align = (int64_t)((H + 31) / 32) * 32;
+  if (!tokens) ntok = T;
+  float* acc = (float*)malloc(sizeof(float) * (size_t)(H > 0 ? H : 1));
+  if (!acc) return ST_INVALID;
+  int status = ST_OK;
+  for (int64_t i = 0; i < ntok; ++i) {
+    const int64_t g = tokens ? tokens[i] : i;
+    for (int h = 0; h < H; ++h) acc[h] = 0.0f;
+    for (int kk = 0; kk < k; ++kk) {
+      const int64_t row = oracle_dst_row(R, bs, k, epr, topk_idx, send_idx,
+                                         put_offset, rank_recv_base, g, kk);
+      if (row < 0) {
+        if (!status) status = ST_EXPERT_ID;
+        continue;
+      }
+      if (row >= y_rows) {
+        if (!status) status = ST_CAPACITY;
+        continue;
+      }
+      const uint8_t* img = yq + row * S;
+      float inv;
+      memcpy(&inv, img + h_align, 4);
+      const float w = topk_weights[g * k + kk];
+      for (int h = 0; h < H; ++h) {
+        const float t = (float)(int8_t)img[h] * inv;   /* dequantise */
+        const float prod = t * w;                      /* Muls */
+        acc[h] = acc[h] + prod;                        /* Add */
+      }
+    }
+    for (int h = 0; h < H; ++h) out[i * (int64_t)H + h] = from_f32(dtype, acc[h]);
+  }
+  free(acc);
+  return status;
+}

@@ -108,6 +108,21 @@ int oracle_combine_tokens(int R, int bs, int k, int epr, int H, int dtype,
                           const int64_t* rank_recv_base,
                           const int64_t* tokens, int64_t ntok, uint16_t* out);
 
+/* Combine over INT8 expert outputs (the "+ dequant" of the pipeline diagram,
+ * section 2.1).  yq holds y_rows rows of oracle_row_bytes(H, 1) bytes laid
+ * out like a dispatched INT8 row (H codes, fp32 1/scale at align32(H)).
+ * Per element: t = float(q) * inv (one rounding), then the combine of
+ * section 2.6: acc = acc + (t * w), RNE to the token dtype. */
+int oracle_combine_quant_tokens(int R, int bs, int k, int epr, int H, int dtype,
+                                const uint8_t* yq, int64_t y_rows,
+                                const int32_t* topk_idx,
+                                const float* topk_weights,
+                                const int32_t* send_idx,
+                                const int32_t* put_offset,
+                                const int64_t* rank_recv_base,
+                                const int64_t* tokens, int64_t ntok,
+                                uint16_t* out);
+
 #ifdef __cplusplus
 }
 #endif

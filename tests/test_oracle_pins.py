@@ -403,12 +403,57 @@ def check_dispatch_capacity(oracle):
     np.testing.assert_array_equal(recv, full[:cap])
 
 
+def _int8_images(codes, inv, H):
+    """Row images: codes int8 [n, H], inv float32 [n]."""
+    ha = (H + 31) // 32 * 32
+    n = codes.shape[0]
+    img = np.zeros((n, ha + 32), np.uint8)
+    img[:, :H] = codes.astype(np.int8).view(np.uint8)
+    img[:, ha:ha + 4] = np.asarray(inv, np.float32).reshape(n, 1).view(np.uint8)
+    return img
+
+
+def check_combine_quant(oracle, seed=8):
+    rng = np.random.default_rng(seed)
+    for H in (40, 96):       # H % 32 != 0 checks where 1/scale is read from
+        wl = W.Workload("pinq", R=3, epr=2, bs=12, H=H, k=3, seed=5)
+        idx, wt = W.routing(wl)
+        idx, wt = idx.numpy(), wt.numpy()
+        L = oracle.layout(idx, wl.R, wl.epr)
+        N = oracle.notify(L["count"], wl.R, wl.bs, wl.epr)
+        args = (idx, wt, L["send_idx"], N["put_offset"], N["rank_recv_base"],
+                wl.R, wl.epr, 0)
+        codes = rng.integers(-127, 128, size=(wl.P, H))
+        # 1/scale = 1 or an exact power of two: float(q) * inv is exact, so
+        # the result is the (pinned) combine of the exactly dequantised rows
+        for inv in (1.0, 2.0 ** -7, 2.0 ** 5):
+            img = _int8_images(codes, np.full(wl.P, inv), H)
+            got, st = oracle.combine_quant(img, *args, H=H)
+            assert st == 0
+            y = _bf16_bits((codes * inv).astype(np.float32))
+            ref, _ = oracle.combine(y, *args)
+            np.testing.assert_array_equal(got, ref)
+        # general 1/scale: error bound against the fp64 value
+        inv = rng.uniform(1e-3, 3e-2, size=wl.P).astype(np.float32)
+        img = _int8_images(codes, inv, H)
+        got, _ = oracle.combine_quant(img, *args, H=H)
+        rows = rows_by_sort(idx)
+        terms = (codes[rows] * inv[rows][..., None].astype(np.float64)
+                 * wt[..., None].astype(np.float64))
+        ref = terms.sum(axis=1)
+        g = oracle.to_f32(got, 0).astype(np.float64)
+        tol = 2.0 ** -8 * np.abs(ref) + (wl.k + 2) * 2.0 ** -23 * \
+            np.abs(terms).sum(axis=1) + 1e-30
+        assert (np.abs(g - ref) <= tol).all()
+
+
 ALL_CHECKS = [
     check_handworked_layout_notify, check_layout_brute_force,
     check_layout_invariants, check_notify_closed_form, check_rows_closed_form,
     check_invalid_ids, check_handworked_quant, check_quant_properties,
     check_quant_zero_row, check_conversions, check_combine_special_cases,
     check_combine_one_hot_and_bound, check_combine_k1, check_dispatch_capacity,
+    check_combine_quant,
 ]
 
 
@@ -426,11 +471,11 @@ MUTANTS = {
     "no_epsilon": ("amax + 1e-12f", "amax + 0.0f"),
     "stores_scale": ("1.0f / scale", "scale"),
     "fused_multiply_add": ("acc[h] = acc[h] + prod;",
-                           "acc[h] = fmaf(to_f32(dtype, yrow[h]), w, acc[h]);"),
+                           "acc[h] = fmaf(to_f32(dtype, yrow[h]), w, acc[h]);", 0),
     "combine_reverse_k": ("for (int kk = 0; kk < k; ++kk) {\n"
                           "      const int64_t row",
                           "for (int kk = k - 1; kk >= 0; --kk) {\n"
-                          "      const int64_t row"),
+                          "      const int64_t row", 0),
     "send_idx_inclusive": ("send_idx[p] = cnt[e];\n        cnt[e] += 1;",
                            "cnt[e] += 1;\n        send_idx[p] = cnt[e];"),
     "put_offset_source_major": ("for (int j = 0; j < epr; ++j) {\n"
@@ -447,6 +492,10 @@ MUTANTS = {
     "row_uses_dst_rank_index": ("put_offset[(int64_t)e * R + s] +",
                                 "put_offset[(int64_t)e * R + dst] +"),
     "amax_signed": ("fabsf(to_f32(dtype, xrow[h]))", "(to_f32(dtype, xrow[h]))"),
+    "dequant_ignores_scale": ("const float t = (float)(int8_t)img[h] * inv;",
+                              "const float t = (float)(int8_t)img[h] + 0.0f * inv;"),
+    "dequant_scale_after_codes": ("memcpy(&inv, img + h_align, 4);",
+                                  "memcpy(&inv, img + H, 4);"),
 }
 
 
@@ -456,8 +505,15 @@ def test_mutants_are_caught(oracle_mod, name):
         pytest.skip("gcc not available")
     here = os.path.dirname(os.path.abspath(oracle_mod.__file__))
     src = open(os.path.join(here, "moe_oracle.c")).read()
-    old, new = MUTANTS[name]
-    assert src.count(old) == 1, "mutation anchor not found: " + name
+    old, new = MUTANTS[name][:2]
+    occurrence = MUTANTS[name][2] if len(MUTANTS[name]) > 2 else None
+    if occurrence is None:
+        assert src.count(old) == 1, "mutation anchor not unique: " + name
+    else:   # replace only the given occurrence of a repeated anchor
+        parts = src.split(old)
+        assert len(parts) > occurrence + 1, "mutation anchor not found: " + name
+        src = old.join(parts[:occurrence + 1]) + "\x00" + old.join(parts[occurrence + 1:])
+        old = "\x00"
     tmp = tempfile.mkdtemp()
     try:
         shutil.copy(os.path.join(here, "moe_oracle.h"), tmp)

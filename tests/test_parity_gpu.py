@@ -303,3 +303,53 @@ def test_unzeroed_workspace_is_reported_and_recovers(oracle_mod, ep, pl):
     L = oracle_mod.layout(idx.numpy(), w.R, w.epr)
     _eq("send_idx", b.send_idx, L["send_idx"])
     _eq("count", b.count, L["count"])
+
+
+# ---------------------------------------------------------------------------
+# combine over INT8 expert outputs (moe_combine_quant)
+# ---------------------------------------------------------------------------
+
+def _check_combine_quant(oracle, pl, w, idx=None, rows=None, expect_status=0):
+    idx_t, wt_t = W.routing(w)
+    if idx is not None:
+        idx_t = torch.from_numpy(idx)
+    yq = W.expert_outputs_int8(w)
+    if rows is not None:
+        yq = yq[:rows].contiguous()
+    L = oracle.layout(idx_t.numpy(), w.R, w.epr)
+    N = oracle.notify(L["count"], w.R, w.bs, w.epr)
+    ref, st = oracle.combine_quant(yq.numpy(), idx_t.numpy(), wt_t.numpy(),
+                                   L["send_idx"], N["put_offset"],
+                                   N["rank_recv_base"], w.R, w.epr, w.dtype, w.H)
+    b = pl.PipelineBuffers(w.R, w.bs, w.k, w.epr, w.H, w.dtype, True)
+    idx_d, wt_d = idx_t.cuda(), wt_t.cuda()
+    pl.run_layout_notify(b, idx_d)
+    pl.run_combine_quant(b, yq.cuda(), idx_d, wt_d)
+    torch.cuda.synchronize()
+    assert b.status() == expect_status == st, (b.status(), st)
+    _eq("out(quant combine)",
+        b.out.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+
+@pytest.mark.parametrize("name", ["dsv3", "maxrank", "skew"])
+def test_combine_quant_full_size(oracle_mod, pl, name):
+    _check_combine_quant(oracle_mod, pl, W.WORKLOADS[name])
+
+
+@pytest.mark.parametrize("case", [
+    dict(R=3, epr=5, bs=700, k=7, H=1000),                 # H % 16 == 8
+    dict(R=5, epr=3, bs=400, k=4, H=136, dtype=W.FP16),    # fp16 out, half chunk
+    dict(R=4, epr=2, bs=300, k=1, H=64),                   # k = 1
+    dict(R=2, epr=4, bs=50, k=8, H=65536),                 # widest rows
+], ids=lambda c: "-".join("%s%s" % kv for kv in c.items()))
+def test_combine_quant_mid(oracle_mod, pl, case):
+    _check_combine_quant(oracle_mod, pl, W.Workload("cq", **case))
+
+
+def test_combine_quant_bad_ids_and_short_rows(oracle_mod, pl):
+    w = W.Workload("cqbad", R=3, epr=2, bs=40, k=3, H=64)
+    idx, _ = W.routing(w)
+    idx = idx.numpy().copy()
+    idx[7, 2] = -3
+    _check_combine_quant(oracle_mod, pl, w, idx=idx, expect_status=2)
+    _check_combine_quant(oracle_mod, pl, w, rows=w.P - 11, expect_status=3)

@@ -154,6 +154,23 @@ def expert_outputs(w: Workload, rows: Optional[int] = None) -> torch.Tensor:
     return _rows(n, w.H, w.dtype, "normal", 1.0, _gen(w.seed, _S_Y))
 
 
+def expert_outputs_int8(w: Workload, rows: Optional[int] = None) -> torch.Tensor:
+    """Synthetic INT8 expert outputs: rows laid out like a dispatched INT8
+    row (H int8 codes, zeros to align32(H), fp32 1/scale, zeros to
+    align32(H) + 32 bytes).  Codes are uniform in [-127, 127]; 1/scale is
+    amax/127 with amax = 0.1 + 3|N(0,1)|.  uint8 tensor [rows, row_bytes]."""
+    n = w.P if rows is None else rows
+    g = _gen(w.seed, _S_Y)
+    h_align = (w.H + 31) // 32 * 32
+    img = torch.zeros((n, h_align + 32), dtype=torch.uint8)
+    codes = torch.randint(-127, 128, (n, w.H), generator=g, dtype=torch.int16)
+    img[:, :w.H] = codes.to(torch.int8).view(torch.uint8)
+    amax = 0.1 + 3.0 * torch.randn((n,), generator=g).abs()
+    inv = (amax / 127.0).to(torch.float32)
+    img[:, h_align:h_align + 4] = inv.view(torch.uint8).view(n, 4)
+    return img
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """uint16 bit patterns of a bf16/fp16 CPU tensor (no copy)."""
     assert t.dtype in (torch.bfloat16, torch.float16)
