@@ -295,6 +295,26 @@ def run_gpu(args, w):
               "tokens_per_s": w.T / (cq_us * 1e-6)}
         del yq
 
+    # ---- token-level layout (moe_token_layout) ------------------------------
+    tpr = torch.empty((w.R, w.R), dtype=torch.int32, device=dev)
+    inr = torch.empty((w.T, w.R), dtype=torch.uint8, device=dev)
+    for i in range(3):
+        ep.moe_token_layout(b.shape, idx, tpr, inr, b.dev_status, stream)
+    tl_ev = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        t0e = torch.cuda.Event(enable_timing=True)
+        t1e = torch.cuda.Event(enable_timing=True)
+        t0e.record(stream)
+        ep.moe_token_layout(b.shape, idx, tpr, inr, b.dev_status, stream)
+        t1e.record(stream)
+        tl_ev.append((t0e, t1e))
+    torch.cuda.synchronize()
+    if b.status() != 0:
+        raise RuntimeError("device status %d in token_layout" % b.status())
+    tl_us = float(np.mean([a.elapsed_time(c) for a, c in tl_ev])) * 1e3
+    del tpr, inr
+
     # ---- end to end through the public API with host buffers --------------
     e2e = run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush)
     e2e_max_ms = reduce_max(e2e["ms_per_step"], world, dev)
@@ -347,6 +367,7 @@ def run_gpu(args, w):
             "avg_launch_ms": float(stage_mean[2]),
         },
         "combine_quant": cq,
+        "token_layout_us": tl_us,
         "stages_us": {n: float(stage_mean[j] * 1e3) for j, n in enumerate(names)},
         "stages_gbs": gbs,
         "dispatch_combine_tokens_per_s": w.T / ((stage_mean[2] + stage_mean[3]) * 1e-3),

@@ -65,8 +65,9 @@ def _load():
                                vp, vp]
     L.moe_combine.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_combine_quant.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_token_layout.argtypes = [sp, vp, vp, vp, vp, vp]
     for name in ("moe_dispatch_layout", "moe_notify_dispatch", "moe_dispatch",
-                 "moe_combine", "moe_combine_quant"):
+                 "moe_combine", "moe_combine_quant", "moe_token_layout"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -225,3 +226,17 @@ def moe_combine_quant(shape, expert_out_q, expert_out_rows, topk_idx,
         _ptr(out, (torch.bfloat16, torch.float16), T * shape.H, "out"),
         _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
     return _check(st, "moe_combine_quant")
+
+
+def moe_token_layout(shape, topk_idx, tokens_per_rank, in_rank, dev_status,
+                     stream=None):
+    """Distinct tokens per (source rank, destination rank) and the token x
+    rank membership map (uint8 [T, R])."""
+    R, T = shape.R, shape.R * shape.bs
+    P = T * shape.k
+    st = _lib.moe_token_layout(
+        ctypes.byref(shape), _ptr(topk_idx, torch.int32, P, "topk_idx"),
+        _ptr(tokens_per_rank, torch.int32, R * R, "tokens_per_rank"),
+        _ptr(in_rank, torch.uint8, T * R, "in_rank"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_token_layout")

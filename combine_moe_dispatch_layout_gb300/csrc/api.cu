@@ -83,6 +83,20 @@ moe_status moe_dispatch_layout(const moe_shape* shape, const int32_t* topk_idx,
                                          workspace, dev_status, st));
 }
 
+moe_status moe_token_layout(const moe_shape* shape, const int32_t* topk_idx,
+                            int32_t* tokens_per_rank, uint8_t* in_rank,
+                            int32_t* dev_status, void* stream) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return MOE_ERR_INVALID_ARG;
+  if (!tokens_per_rank || !dev_status || !aligned(tokens_per_rank, 4) ||
+      !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (s.T() > 0 && (!topk_idx || !in_rank || !aligned(topk_idx, 4) || !aligned(in_rank, 4)))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_token_layout(s, topk_idx, tokens_per_rank, in_rank,
+                                               dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_notify_dispatch(const moe_shape* shape, const int32_t* count,
                                int32_t* put_offset, int32_t* total_recv,
                                int64_t* rank_recv_base,

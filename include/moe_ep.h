@@ -144,6 +144,19 @@ moe_status moe_dispatch_layout_static(const moe_shape* shape,
                                       int32_t* rank_send, int32_t* send_idx,
                                       int32_t* dev_status, void* stream);
 
+/* (1') Token-level layout -- section 2.3's "how many tokens each rank must
+ * receive" counted in distinct tokens: a token that routes several of its k
+ * pairs to experts of the same rank counts once for that rank.
+ *   topk_idx        int32 [R][bs][k] (read)
+ *   tokens_per_rank int32 [R][R]  tokens of source rank s reaching rank r
+ *   in_rank         uint8 [T][R]  1 if token g reaches rank r, else 0;
+ *                                 4-byte aligned
+ * Ids outside [0,E) are ignored and set MOE_ERR_EXPERT_ID.  A
+ * cudaMemsetAsync of tokens_per_rank, then one launch. */
+moe_status moe_token_layout(const moe_shape* shape, const int32_t* topk_idx,
+                            int32_t* tokens_per_rank, uint8_t* in_rank,
+                            int32_t* dev_status, void* stream);
+
 /* (2) Notify -- moe_notify_dispatch_zb, section 2.4.  The AllGather of every
  * rank's tokenPerExpert is the identity (count is already the whole R x E
  * matrix); then BuildTotalRecvCount / BuildMaxBs / BuildTotalRecvTokens /

@@ -59,6 +59,7 @@ def lib():
         L.oracle_combine_tokens.argtypes = [i, i, i, i, i, i, _u16p, i64,
                                             _i32p, _f32p, _i32p, _i32p,
                                             _i64p, _i64p, i64, _u16p]
+        L.oracle_token_layout.argtypes = [i, i, i, i, _i32p, _i32p, _u8p]
         L.oracle_combine_quant_tokens.argtypes = [i, i, i, i, i, i, _u8p, i64,
                                                   _i32p, _f32p, _i32p, _i32p,
                                                   _i64p, _i64p, i64, _u16p]
@@ -272,3 +273,17 @@ def combine_quant(yq, topk_idx, topk_weights, send_idx, put_offset,
         _p(_c(rank_recv_base, np.int64), _i64p),
         None if toks is None else _p(toks, _i64p), n, _p(out, _u16p))
     return out, st
+
+
+def token_layout(topk_idx, R, epr):
+    """Distinct tokens per (source rank, destination rank) and the token x
+    rank membership map.  Returns dict(tokens_per_rank [R,R] int32,
+    in_rank [T,R] uint8, status)."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    bs = T // R
+    tpr = np.zeros((R, R), np.int32)
+    inr = np.zeros((T, R), np.uint8)
+    st = lib().oracle_token_layout(R, bs, k, epr, _p(idx, _i32p), _p(tpr, _i32p),
+                                   _p(inr, _u8p))
+    return dict(tokens_per_rank=tpr, in_rank=inr, status=st)

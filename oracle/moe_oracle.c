@@ -390,3 +390,30 @@ int oracle_combine_quant_tokens(int R, int bs, int k, int epr, int H, int dtype,
   free(acc);
   return status;
 }
+
+/* ---- token-level layout (distinct tokens per destination rank) ----------- */
+
+int oracle_token_layout(int R, int bs, int k, int epr, const int32_t* topk_idx,
+                        int32_t* tokens_per_rank, uint8_t* in_rank) {
+  if (R < 1 || bs < 0 || k < 1 || epr < 1) return ST_INVALID;
+  const int E = R * epr;
+  int status = ST_OK;
+  for (int64_t i = 0; i < (int64_t)R * R; ++i) tokens_per_rank[i] = 0;
+  for (int s = 0; s < R; ++s) {
+    for (int t = 0; t < bs; ++t) {
+      const int64_t g = (int64_t)s * bs + t;
+      uint8_t* row = in_rank + g * R;
+      for (int r = 0; r < R; ++r) row[r] = 0;
+      for (int kk = 0; kk < k; ++kk) {
+        const int32_t e = topk_idx[g * k + kk];
+        if (e < 0 || e >= E) {
+          status = ST_EXPERT_ID;
+          continue;
+        }
+        row[e / epr] = 1;
+      }
+      for (int r = 0; r < R; ++r) tokens_per_rank[(int64_t)s * R + r] += row[r];
+    }
+  }
+  return status;
+}

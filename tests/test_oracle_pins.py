@@ -447,13 +447,40 @@ def check_combine_quant(oracle, seed=8):
         assert (np.abs(g - ref) <= tol).all()
 
 
+def check_token_layout(oracle, seed=9):
+    rng = np.random.default_rng(seed)
+    for c in range(6):
+        R = int(rng.integers(1, 6))
+        epr = int(rng.integers(1, 4))
+        bs = int(rng.integers(0, 30))
+        E = R * epr
+        k = int(rng.integers(1, E + 1))
+        idx = _random_routing(rng, R, epr, bs, k, distinct=(c % 2 == 0))
+        TL = oracle.token_layout(idx, R, epr)
+        L = oracle.layout(idx, R, epr)
+        assert TL["status"] == 0
+        # brute force: a Python set of destination ranks per token
+        exp_in = np.zeros((R * bs, R), np.uint8)
+        for g in range(R * bs):
+            for r in {int(e) // epr for e in idx[g]}:
+                exp_in[g, r] = 1
+        np.testing.assert_array_equal(TL["in_rank"], exp_in)
+        np.testing.assert_array_equal(
+            TL["tokens_per_rank"], exp_in.reshape(R, bs, R).sum(axis=1))
+        # never more tokens than pairs; equal when a rank owns one expert and
+        # experts are distinct per token
+        assert (TL["tokens_per_rank"] <= L["rank_send"]).all()
+        if epr == 1 and c % 2 == 0:
+            np.testing.assert_array_equal(TL["tokens_per_rank"], L["rank_send"])
+
+
 ALL_CHECKS = [
     check_handworked_layout_notify, check_layout_brute_force,
     check_layout_invariants, check_notify_closed_form, check_rows_closed_form,
     check_invalid_ids, check_handworked_quant, check_quant_properties,
     check_quant_zero_row, check_conversions, check_combine_special_cases,
     check_combine_one_hot_and_bound, check_combine_k1, check_dispatch_capacity,
-    check_combine_quant,
+    check_combine_quant, check_token_layout,
 ]
 
 
@@ -496,6 +523,7 @@ MUTANTS = {
                               "const float t = (float)(int8_t)img[h] + 0.0f * inv;"),
     "dequant_scale_after_codes": ("memcpy(&inv, img + h_align, 4);",
                                   "memcpy(&inv, img + H, 4);"),
+    "token_layout_counts_pairs": ("row[e / epr] = 1;", "row[e / epr] += 1;"),
 }
 
 

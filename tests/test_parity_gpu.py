@@ -353,3 +353,37 @@ def test_combine_quant_bad_ids_and_short_rows(oracle_mod, pl):
     idx[7, 2] = -3
     _check_combine_quant(oracle_mod, pl, w, idx=idx, expect_status=2)
     _check_combine_quant(oracle_mod, pl, w, rows=w.P - 11, expect_status=3)
+
+
+# ---------------------------------------------------------------------------
+# token-level layout (moe_token_layout)
+# ---------------------------------------------------------------------------
+
+def _check_token_layout(oracle, ep, w, idx=None, expect_status=0):
+    idx_t = W.routing(w)[0] if idx is None else torch.from_numpy(idx)
+    ref = oracle.token_layout(idx_t.numpy(), w.R, w.epr)
+    shape = ep.make_shape(w.R, w.bs, w.k, w.epr, w.H)
+    tpr = torch.full((w.R, w.R), -5, dtype=torch.int32, device="cuda")
+    inr = torch.full((w.T, w.R), 7, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.moe_token_layout(shape, idx_t.cuda(), tpr, inr, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == expect_status == ref["status"]
+    _eq("tokens_per_rank", tpr, ref["tokens_per_rank"])
+    _eq("in_rank", inr, ref["in_rank"])
+
+
+@pytest.mark.parametrize("name", W.ORDER)
+def test_token_layout_workloads(oracle_mod, ep, name):
+    _check_token_layout(oracle_mod, ep, W.WORKLOADS[name])
+
+
+def test_token_layout_edges(oracle_mod, ep):
+    rng = np.random.default_rng(3)
+    w = W.Workload("tl", R=5, epr=3, bs=300, k=9, H=64)          # R % 4 != 0
+    idx = rng.integers(0, w.E, size=(w.T, w.k)).astype(np.int32)   # duplicates
+    _check_token_layout(oracle_mod, ep, w, idx=idx)
+    idx[4, 2] = w.E + 3
+    _check_token_layout(oracle_mod, ep, w, idx=idx, expect_status=2)
+    _check_token_layout(oracle_mod, ep, W.Workload("tl0", R=3, epr=2, bs=0, k=2, H=64))
+    _check_token_layout(oracle_mod, ep, W.Workload("tlk", R=64, epr=1, bs=40, k=64, H=64))
