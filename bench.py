@@ -295,6 +295,26 @@ def run_gpu(args, w):
               "tokens_per_s": w.T / (cq_us * 1e-6)}
         del yq
 
+    # ---- one-launch low-latency dispatch vs the three separate launches ------
+    def timed(fn, n):
+        evs = []
+        for i in range(n):
+            flush.fill_(i & 0xff)
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            fn()
+            a1.record(stream)
+            evs.append((a0, a1))
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(c) for a, c in evs])) * 1e3
+    for i in range(3):
+        pl.run_dispatch_fused(b, x, idx, stream)
+    fused_us = timed(lambda: pl.run_dispatch_fused(b, x, idx, stream), args.steps)
+    if b.status() != 0:
+        raise RuntimeError("device status %d in fused dispatch" % b.status())
+    separate_us = float(stage_mean[0] + stage_mean[1] + stage_mean[2]) * 1e3
+
     # ---- token-level layout (moe_token_layout) ------------------------------
     tpr = torch.empty((w.R, w.R), dtype=torch.int32, device=dev)
     inr = torch.empty((w.T, w.R), dtype=torch.uint8, device=dev)
@@ -368,6 +388,9 @@ def run_gpu(args, w):
         },
         "combine_quant": cq,
         "token_layout_us": tl_us,
+        "dispatch_fused": {"us": fused_us, "separate_us": separate_us,
+                           "note": "layout+notify+dispatch in one cooperative "
+                                   "launch vs three launches"},
         "stages_us": {n: float(stage_mean[j] * 1e3) for j, n in enumerate(names)},
         "stages_gbs": gbs,
         "dispatch_combine_tokens_per_s": w.T / ((stage_mean[2] + stage_mean[3]) * 1e-3),

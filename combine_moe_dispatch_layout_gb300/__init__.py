@@ -66,8 +66,12 @@ def _load():
     L.moe_combine.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_combine_quant.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_token_layout.argtypes = [sp, vp, vp, vp, vp, vp]
+    L.moe_fused_workspace_bytes.argtypes = [sp]
+    L.moe_fused_workspace_bytes.restype = ctypes.c_size_t
+    L.moe_dispatch_fused.argtypes = [sp, vp, vp, ctypes.c_int] + [vp] * 9 + [i64, vp, vp, vp]
     for name in ("moe_dispatch_layout", "moe_notify_dispatch", "moe_dispatch",
-                 "moe_combine", "moe_combine_quant", "moe_token_layout"):
+                 "moe_combine", "moe_combine_quant", "moe_token_layout",
+                 "moe_dispatch_fused"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -240,3 +244,37 @@ def moe_token_layout(shape, topk_idx, tokens_per_rank, in_rank, dev_status,
         _ptr(in_rank, torch.uint8, T * R, "in_rank"),
         _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
     return _check(st, "moe_token_layout")
+
+
+def fused_workspace_bytes(shape):
+    return int(_lib.moe_fused_workspace_bytes(ctypes.byref(shape)))
+
+
+def moe_dispatch_fused(shape, x, topk_idx, quant, count, rank_send, send_idx,
+                       put_offset, total_recv, rank_recv_base, recv_per_expert,
+                       max_bs, recv, recv_capacity_rows, workspace, dev_status,
+                       stream=None):
+    """Low-latency dispatch: layout + notify + dispatch in one launch, same
+    results as the three separate calls."""
+    R, E = shape.R, shape.R * shape.experts_per_rank
+    T, P = shape.R * shape.bs, shape.R * shape.bs * shape.k
+    rb = recv_row_bytes(shape, quant)
+    if recv is not None and recv.numel() * recv.element_size() < \
+            rb * int(recv_capacity_rows):
+        raise ValueError("recv is smaller than recv_capacity_rows rows")
+    st = _lib.moe_dispatch_fused(
+        ctypes.byref(shape),
+        _ptr(x, (torch.bfloat16, torch.float16), T * shape.H, "x"),
+        _ptr(topk_idx, torch.int32, P, "topk_idx"), int(bool(quant)),
+        _ptr(count, torch.int32, R * E, "count"),
+        _ptr(rank_send, torch.int32, R * R, "rank_send"),
+        _ptr(send_idx, torch.int32, P, "send_idx"),
+        _ptr(put_offset, torch.int32, E * R, "put_offset"),
+        _ptr(total_recv, torch.int32, R, "total_recv"),
+        _ptr(rank_recv_base, torch.int64, R + 1, "rank_recv_base"),
+        _ptr(recv_per_expert, torch.int32, E, "recv_per_expert"),
+        _ptr(max_bs, torch.int32, 1, "max_bs"),
+        _ptr(recv, None, None, "recv"), int(recv_capacity_rows),
+        _ptr(workspace, None, None, "workspace"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_dispatch_fused")

@@ -163,6 +163,40 @@ moe_status moe_combine(const moe_shape* shape, const void* expert_out,
                                           dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_fused_workspace_bytes(const moe_shape* shape) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return 0;
+  return moe_ep::fused_workspace_bytes(s);
+}
+
+moe_status moe_dispatch_fused(const moe_shape* shape, const void* x,
+                              const int32_t* topk_idx, int quant, int32_t* count,
+                              int32_t* rank_send, int32_t* send_idx,
+                              int32_t* put_offset, int32_t* total_recv,
+                              int64_t* rank_recv_base, int32_t* recv_per_expert,
+                              int32_t* max_bs, void* recv,
+                              int64_t recv_capacity_rows, void* workspace,
+                              int32_t* dev_status, void* stream) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return MOE_ERR_INVALID_ARG;
+  if (recv_capacity_rows < 0 || !count || !rank_send || !put_offset || !total_recv ||
+      !rank_recv_base || !recv_per_expert || !max_bs || !workspace || !dev_status)
+    return MOE_ERR_INVALID_ARG;
+  if (s.T() > 0 && (!x || !topk_idx || !send_idx || (!recv && recv_capacity_rows > 0)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(recv, 16) || !aligned(workspace, 16) ||
+      !aligned(topk_idx, 4) || !aligned(count, 4) || !aligned(rank_send, 4) ||
+      !aligned(send_idx, 4) || !aligned(put_offset, 4) || !aligned(total_recv, 4) ||
+      !aligned(rank_recv_base, 8) || !aligned(recv_per_expert, 4) ||
+      !aligned(max_bs, 4) || !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  const int64_t row_bytes = quant ? moe_ep::align_up(s.H, 32) + 32 : int64_t(s.H) * 2;
+  return from_cuda(moe_ep::launch_fused_dispatch(
+      s, x, topk_idx, quant != 0, count, rank_send, send_idx, put_offset, total_recv,
+      rank_recv_base, recv_per_expert, max_bs, recv, row_bytes, recv_capacity_rows,
+      workspace, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_combine_quant(const moe_shape* shape, const void* expert_out_q,
                              int64_t expert_out_rows, const int32_t* topk_idx,
                              const float* topk_weights, const int32_t* send_idx,

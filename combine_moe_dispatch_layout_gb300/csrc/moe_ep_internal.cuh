@@ -193,6 +193,15 @@ cudaError_t launch_token_layout(const Shape& s, const int32_t* topk_idx,
                                 int32_t* tokens_per_rank, uint8_t* in_rank,
                                 int32_t* dev_status, cudaStream_t st);
 
+size_t fused_workspace_bytes(const Shape& s);
+cudaError_t launch_fused_dispatch(const Shape& s, const void* x, const int32_t* topk_idx,
+                                  bool quant, int32_t* count, int32_t* rank_send,
+                                  int32_t* send_idx, int32_t* put_offset,
+                                  int32_t* total_recv, int64_t* rank_recv_base,
+                                  int32_t* recv_per_expert, int32_t* max_bs, void* recv,
+                                  int64_t row_bytes, int64_t capacity, void* workspace,
+                                  int32_t* dev_status, cudaStream_t st);
+
 cudaError_t launch_notify(const Shape& s, const int32_t* count,
                           int32_t* put_offset, int32_t* total_recv,
                           int64_t* rank_recv_base, int32_t* recv_per_expert,

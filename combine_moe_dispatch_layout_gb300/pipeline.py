@@ -9,9 +9,10 @@ synchronisation is needed between the stages.
 """
 import torch
 
-from . import (make_shape, layout_workspace_bytes, moe_combine,
-               moe_combine_quant, moe_dispatch, moe_dispatch_layout,
-               moe_notify_dispatch, recv_row_bytes)
+from . import (fused_workspace_bytes, make_shape, layout_workspace_bytes,
+               moe_combine, moe_combine_quant, moe_dispatch,
+               moe_dispatch_fused, moe_dispatch_layout, moe_notify_dispatch,
+               recv_row_bytes)
 
 
 class PipelineBuffers:
@@ -40,6 +41,18 @@ class PipelineBuffers:
         self.recv = torch.empty((P, self.row_bytes), dtype=torch.uint8,
                                 device=device)
         self.out = torch.empty((T, H), dtype=self.torch_dtype, device=device)
+        self.device = device
+        self._fused_ws = None
+
+    @property
+    def fused_workspace(self):
+        """Workspace of the one-launch dispatch (allocated zeroed on first
+        use)."""
+        if self._fused_ws is None:
+            self._fused_ws = torch.zeros(
+                max(16, fused_workspace_bytes(self.shape)), dtype=torch.uint8,
+                device=self.device)
+        return self._fused_ws
 
     def status(self):
         """First device-side error code of the calls so far (syncs)."""
@@ -63,6 +76,14 @@ def run_dispatch(b, x, topk_idx, stream=None):
 def run_combine(b, y, topk_idx, topk_weights, stream=None):
     moe_combine(b.shape, y, y.shape[0], topk_idx, topk_weights, b.send_idx,
                 b.put_offset, b.rank_recv_base, b.out, b.dev_status, stream)
+
+
+def run_dispatch_fused(b, x, topk_idx, stream=None):
+    """Layout + notify + dispatch in one launch (the low-latency path)."""
+    moe_dispatch_fused(b.shape, x, topk_idx, b.quant, b.count, b.rank_send,
+                       b.send_idx, b.put_offset, b.total_recv,
+                       b.rank_recv_base, b.recv_per_expert, b.max_bs, b.recv,
+                       b.capacity, b.fused_workspace, b.dev_status, stream)
 
 
 def run_combine_quant(b, yq, topk_idx, topk_weights, stream=None):

@@ -221,6 +221,28 @@ moe_status moe_combine(const moe_shape* shape, const void* expert_out,
                        const int64_t* rank_recv_base, void* out,
                        int32_t* dev_status, void* stream);
 
+/* Low-latency dispatch: stages (1), (2) and (3) in ONE launch, the way the
+ * page's moe_dispatch_lowlatency_zb runs layout, count notify, prefix and
+ * token output inside one kernel (section 3.2).  Same arguments and results
+ * as moe_dispatch_layout + moe_notify_dispatch + moe_dispatch (bit for
+ * bit), for small batches where three launches cost more than the work.
+ * One cooperative launch of persistent CTAs with grid barriers between the
+ * phases; for large batches the separate calls are faster.
+ *   workspace  moe_fused_workspace_bytes() bytes, 16-byte aligned,
+ *              zero-filled once before first use (each call leaves it ready;
+ *              after MOE_ERR_TIMEOUT zero it again)
+ * Calls sharing a workspace must not overlap on the GPU.  A grid-barrier
+ * wait that exceeds about a second sets MOE_ERR_TIMEOUT. */
+size_t moe_fused_workspace_bytes(const moe_shape* shape);
+moe_status moe_dispatch_fused(const moe_shape* shape, const void* x,
+                              const int32_t* topk_idx, int quant, int32_t* count,
+                              int32_t* rank_send, int32_t* send_idx,
+                              int32_t* put_offset, int32_t* total_recv,
+                              int64_t* rank_recv_base, int32_t* recv_per_expert,
+                              int32_t* max_bs, void* recv,
+                              int64_t recv_capacity_rows, void* workspace,
+                              int32_t* dev_status, void* stream);
+
 /* (4') Combine over INT8 expert outputs -- the "+ dequant" of the pipeline
  * diagram (section 2.1, stage 4: shmem read + weighted sum + dequant).
  * Same gather and arithmetic as moe_combine, except that each expert-output

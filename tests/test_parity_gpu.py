@@ -387,3 +387,62 @@ def test_token_layout_edges(oracle_mod, ep):
     _check_token_layout(oracle_mod, ep, w, idx=idx, expect_status=2)
     _check_token_layout(oracle_mod, ep, W.Workload("tl0", R=3, epr=2, bs=0, k=2, H=64))
     _check_token_layout(oracle_mod, ep, W.Workload("tlk", R=64, epr=1, bs=40, k=64, H=64))
+
+
+# ---------------------------------------------------------------------------
+# one-launch low-latency dispatch (moe_dispatch_fused)
+# ---------------------------------------------------------------------------
+
+def _check_fused(oracle, pl, w, idx=None, capacity=None, expect_status=0, b=None,
+                 x=None):
+    idx_t = W.routing(w)[0] if idx is None else torch.from_numpy(idx)
+    x_t = W.tokens(w) if x is None else x
+    L = oracle.layout(idx_t.numpy(), w.R, w.epr)
+    N = oracle.notify(L["count"], w.R, w.bs, w.epr)
+    cap = w.P if capacity is None else capacity
+    recv_ref, st = oracle.dispatch(W.bits(x_t), idx_t.numpy(), L["send_idx"],
+                                   N["put_offset"], N["rank_recv_base"], w.R,
+                                   w.epr, w.dtype, w.quant, capacity_rows=cap)
+    assert st == expect_status
+    if b is None:
+        b = pl.PipelineBuffers(w.R, w.bs, w.k, w.epr, w.H, w.dtype, w.quant)
+    b.capacity = cap
+    b.recv.fill_(0xAB)
+    b.dev_status.zero_()
+    pl.run_dispatch_fused(b, x_t.cuda(), idx_t.cuda())
+    torch.cuda.synchronize()
+    assert b.status() == expect_status, b.status()
+    _check_layout_notify(b, dict(L=L, N=N))
+    rows = oracle.dst_rows(idx_t.numpy(), L["send_idx"], N["put_offset"],
+                           N["rank_recv_base"], w.R, w.epr)
+    ok = rows[(rows >= 0) & (rows < cap)]
+    _eq("recv(fused)", b.recv[:cap].cpu().numpy()[ok], recv_ref[ok])
+    return b
+
+
+@pytest.mark.parametrize("name", W.ORDER)
+def test_fused_dispatch_workloads(oracle_mod, pl, name):
+    _check_fused(oracle_mod, pl, W.WORKLOADS[name])
+
+
+def test_fused_dispatch_edges_and_reuse(oracle_mod, pl):
+    w = W.Workload("fz", R=3, epr=5, bs=1500, k=7, H=1000)     # 6 tiles/rank
+    b = _check_fused(oracle_mod, pl, w)
+    _check_fused(oracle_mod, pl, w.with_(seed=77), b=b)          # same workspace
+    idx, _ = W.routing(w)
+    idx = idx.numpy().copy()
+    idx[9, 3] = -1
+    _check_fused(oracle_mod, pl, w, idx=idx, expect_status=2, b=b)
+    _check_fused(oracle_mod, pl, w, capacity=w.P - 50, expect_status=3, b=b)
+    _check_fused(oracle_mod, pl, W.Workload("fzv", R=4, epr=2, bs=300, k=3, H=136,
+                                            dtype=W.FP16, quant=False))
+    _check_fused(oracle_mod, pl, W.Workload("fz1", R=1, epr=16, bs=20000, k=8, H=64))
+    w0 = W.Workload("fz0", R=4, epr=2, bs=0, k=2, H=64)
+    b0 = pl.PipelineBuffers(w0.R, w0.bs, w0.k, w0.epr, w0.H, w0.dtype, w0.quant)
+    b0.count.fill_(9)
+    e = torch.empty((0, w0.k), dtype=torch.int32, device="cuda")
+    pl.run_dispatch_fused(b0, torch.empty((0, w0.H), dtype=torch.bfloat16,
+                                          device="cuda"), e)
+    torch.cuda.synchronize()
+    assert b0.status() == 0 and int(b0.count.abs().sum()) == 0
+    assert b0.rank_recv_base.cpu().tolist() == [0] * (w0.R + 1)
