@@ -34,6 +34,7 @@ if ROOT not in sys.path:
 import workloads as W  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20          # > 129 MB of L2
+SWIGLU_INTERMEDIATE = 2048          # expert intermediate size (DeepSeek-V3)
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = {                  # kernel -> source file (traffic staleness)
     "combine": "combine_moe_dispatch_layout_gb300/csrc/combine.cu",
@@ -315,6 +316,25 @@ def run_gpu(args, w):
         raise RuntimeError("device status %d in fused dispatch" % b.status())
     separate_us = float(stage_mean[0] + stage_mean[1] + stage_mean[2]) * 1e3
 
+    # ---- GMM1 epilogue (moe_swiglu_quant): one row per dispatched pair, I=2048
+    sw = None
+    if w.quant:
+        I = SWIGLU_INTERMEDIATE
+        acc_h, ws_h, ts_h = W.gmm1_accumulators(w.P, I)
+        acc_d, ws_d, ts_d = acc_h.to(dev), ws_h.to(dev), ts_h.to(dev)
+        del acc_h
+        sw_out = torch.empty((w.P, (I + 31) // 32 * 32 + 32), dtype=torch.uint8,
+                             device=dev)
+        for i in range(3):
+            ep.moe_swiglu_quant(acc_d, ws_d, ts_d, sw_out, b.dev_status, stream)
+        sw_us = timed(lambda: ep.moe_swiglu_quant(acc_d, ws_d, ts_d, sw_out,
+                                                  b.dev_status, stream), args.steps)
+        sw_bytes = w.P * (8 * I + (I + 31) // 32 * 32 + 32 + 4) + 8 * I
+        sw = {"us": sw_us, "rows": w.P, "I": I, "algorithmic_bytes": sw_bytes,
+              "achieved_gbs": sw_bytes / (sw_us * 1e-6) / 1e9,
+              "frac": sw_bytes / (sw_us * 1e-6) / 1e9 / peak}
+        del acc_d, sw_out
+
     # ---- token-level layout (moe_token_layout) ------------------------------
     tpr = torch.empty((w.R, w.R), dtype=torch.int32, device=dev)
     inr = torch.empty((w.T, w.R), dtype=torch.uint8, device=dev)
@@ -388,6 +408,7 @@ def run_gpu(args, w):
         },
         "combine_quant": cq,
         "token_layout_us": tl_us,
+        "swiglu_quant": sw,
         "dispatch_fused": {"us": fused_us, "separate_us": separate_us,
                            "note": "layout+notify+dispatch in one cooperative "
                                    "launch vs three launches"},

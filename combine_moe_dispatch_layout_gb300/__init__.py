@@ -66,12 +66,13 @@ def _load():
     L.moe_combine.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_combine_quant.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_token_layout.argtypes = [sp, vp, vp, vp, vp, vp]
+    L.moe_swiglu_quant.argtypes = [vp, i64, ctypes.c_int32, vp, vp, vp, vp, vp]
     L.moe_fused_workspace_bytes.argtypes = [sp]
     L.moe_fused_workspace_bytes.restype = ctypes.c_size_t
     L.moe_dispatch_fused.argtypes = [sp, vp, vp, ctypes.c_int] + [vp] * 9 + [i64, vp, vp, vp]
     for name in ("moe_dispatch_layout", "moe_notify_dispatch", "moe_dispatch",
                  "moe_combine", "moe_combine_quant", "moe_token_layout",
-                 "moe_dispatch_fused"):
+                 "moe_dispatch_fused", "moe_swiglu_quant"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -278,3 +279,22 @@ def moe_dispatch_fused(shape, x, topk_idx, quant, count, rank_send, send_idx,
         _ptr(workspace, None, None, "workspace"),
         _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
     return _check(st, "moe_dispatch_fused")
+
+
+def moe_swiglu_quant(acc, weight_scale, token_scale, out, dev_status,
+                     stream=None):
+    """GMM1 epilogue: int32 acc [M, 2I] -> INT8 row images out
+    [M, align32(I) + 32] (dequant, SwiGLU, dynamic requant)."""
+    if acc.dim() != 2 or acc.shape[1] % 2:
+        raise ValueError("acc must be [M, 2I]")
+    M, I = acc.shape[0], acc.shape[1] // 2
+    rb = (I + 31) // 32 * 32 + 32
+    if out.numel() * out.element_size() < M * rb:
+        raise ValueError("out is smaller than M rows")
+    st = _lib.moe_swiglu_quant(
+        _ptr(acc, torch.int32, M * 2 * I, "acc"), int(M), int(I),
+        _ptr(weight_scale, torch.float32, 2 * I, "weight_scale"),
+        _ptr(token_scale, torch.float32, M, "token_scale"),
+        _ptr(out, None, None, "out"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_swiglu_quant")

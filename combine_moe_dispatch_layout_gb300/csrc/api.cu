@@ -163,6 +163,19 @@ moe_status moe_combine(const moe_shape* shape, const void* expert_out,
                                           dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_swiglu_quant(const int32_t* acc, int64_t M, int32_t I,
+                            const float* weight_scale, const float* token_scale,
+                            void* out, int32_t* dev_status, void* stream) {
+  if (M < 0 || I < 8 || I > 16384 || I % 8 != 0 || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  if (!acc || !weight_scale || !token_scale || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(acc, 16) || !aligned(weight_scale, 16) || !aligned(token_scale, 4) ||
+      !aligned(out, 16) || !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_swiglu_quant(acc, M, I, weight_scale, token_scale, out,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_fused_workspace_bytes(const moe_shape* shape) {
   Shape s;
   if (!valid_shape(shape, &s)) return 0;

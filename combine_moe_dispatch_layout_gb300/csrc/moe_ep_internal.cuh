@@ -202,6 +202,10 @@ cudaError_t launch_fused_dispatch(const Shape& s, const void* x, const int32_t* 
                                   int64_t row_bytes, int64_t capacity, void* workspace,
                                   int32_t* dev_status, cudaStream_t st);
 
+cudaError_t launch_swiglu_quant(const int32_t* acc, int64_t M, int I,
+                                const float* weight_scale, const float* token_scale,
+                                void* out, cudaStream_t st);
+
 cudaError_t launch_notify(const Shape& s, const int32_t* count,
                           int32_t* put_offset, int32_t* total_recv,
                           int64_t* rank_recv_base, int32_t* recv_per_expert,

@@ -1,0 +1,153 @@
+// swiglu.cu -- GMM1 epilogue of the fused deep MoE, standalone (UMDK/CAM deep
+// analysis v2, section 4.8.1 PerTokenDequantSwiGLU and section 8.7
+// "INT32 -> [Cast + Dequant + SwiGLU + Quant] -> INT8").
+//
+// Row m of the grouped GEMM's int32 accumulator acc [M][2I] becomes one INT8
+// row image, in one pass over HBM:
+//   v    = fp32(acc) (round to nearest) * weight_scale[col] * token_scale[m]
+//   gate = v[j], up = v[I + j]        (left half / right half)
+//   h[j] = (gate / (1 + exp(-gate))) * up   (the page's Muls(-1), Exp,
+//          Adds(1), Div on the left half; the right half passes through)
+//   then the dispatch's dynamic quantisation of h: scale = 127/(amax +
+//   1e-12f), q = round-half-even(h * scale), 1/scale at byte align32(I).
+// Every step is one fp32 operation rounded to nearest even (explicit _rn
+// intrinsics; the unit is built with -fmad=false).  exp is computed by Cody
+// and Waite's two-constant range reduction, x = n*ln2 + r with |r| <= ln2/2,
+// and the degree-7 Taylor polynomial of e^r in Horner form, scaled by 2^n
+// (input clamped to [-87, 88]); the CPU oracle evaluates the same textbook
+// method in the same order, so results match bit for bit.
+//
+// Persistent CTAs walk the rows; each thread owns 8-output chunks (two
+// 32-byte loads of the accumulator per chunk), max|h| is reduced with warp
+// shuffles and one shared step, and the row image is written with 8-byte
+// stores.  HBM-bound: 8I bytes read and align32(I) + 32 written per row.
+#include <algorithm>
+
+#include "moe_ep_internal.cuh"
+
+namespace moe_ep {
+namespace {
+
+constexpr int kMaxThreads = 512;   // with kCpt: I <= 16384
+constexpr int kCpt = 4;            // 8-output chunks per thread, at most
+
+__device__ __forceinline__ float exp_cody_waite(float x) {
+  if (x > 88.0f) x = 88.0f;
+  if (x < -87.0f) x = -87.0f;
+  const float t = __fmul_rn(x, 1.44269504f);                 // x / ln 2
+  const float n = rintf(t);                                  // ties to even
+  float r = __fsub_rn(x, __fmul_rn(n, 0.693359375f));       // ln 2, high part
+  r = __fsub_rn(r, __fmul_rn(n, -2.12194440e-4f));          // ln 2, low part
+  float p = 1.98412698e-4f;                                  // 1/7!
+  p = __fadd_rn(__fmul_rn(p, r), 1.38888889e-3f);           // 1/6!
+  p = __fadd_rn(__fmul_rn(p, r), 8.33333333e-3f);           // 1/5!
+  p = __fadd_rn(__fmul_rn(p, r), 4.16666667e-2f);           // 1/4!
+  p = __fadd_rn(__fmul_rn(p, r), 1.66666667e-1f);           // 1/3!
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);                     // 1/2!
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);                     // 1/1!
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);                     // 1/0!
+  const int ni = static_cast<int>(n);                        // -126 .. 127
+  return __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(ni + 127) << 23));
+}
+
+__global__ void __launch_bounds__(kMaxThreads)
+swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I,
+                    const float* __restrict__ weight_scale,
+                    const float* __restrict__ token_scale,
+                    unsigned char* __restrict__ out, int64_t row_bytes) {
+  __shared__ float s_wmax[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, nwarps = nthreads / 32;
+  const int nch = I / 8;
+  const int i_align = static_cast<int>(align_up(I, 32));
+  const int ntail = static_cast<int>((row_bytes - I) / 8);
+  const int inv_word = (i_align - I) / 8;
+
+  for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+    const int32_t* row = acc + m * 2 * int64_t(I);
+    const float ts = __ldg(token_scale + m);
+    float h[kCpt][8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kCpt; ++i) {
+      const int c = tid + i * nthreads;
+      if (c < nch) {
+        const uint4 g0 = ld_stream_16(row + 8 * c), g1 = ld_stream_16(row + 8 * c + 4);
+        const uint4 u0 = ld_stream_16(row + I + 8 * c), u1 = ld_stream_16(row + I + 8 * c + 4);
+        const int32_t gi[8] = {int32_t(g0.x), int32_t(g0.y), int32_t(g0.z), int32_t(g0.w),
+                               int32_t(g1.x), int32_t(g1.y), int32_t(g1.z), int32_t(g1.w)};
+        const int32_t ui[8] = {int32_t(u0.x), int32_t(u0.y), int32_t(u0.z), int32_t(u0.w),
+                               int32_t(u1.x), int32_t(u1.y), int32_t(u1.z), int32_t(u1.w)};
+        const float4 wg0 = __ldg(reinterpret_cast<const float4*>(weight_scale + 8 * c));
+        const float4 wg1 = __ldg(reinterpret_cast<const float4*>(weight_scale + 8 * c + 4));
+        const float4 wu0 = __ldg(reinterpret_cast<const float4*>(weight_scale + I + 8 * c));
+        const float4 wu1 = __ldg(reinterpret_cast<const float4*>(weight_scale + I + 8 * c + 4));
+        const float wg[8] = {wg0.x, wg0.y, wg0.z, wg0.w, wg1.x, wg1.y, wg1.z, wg1.w};
+        const float wu[8] = {wu0.x, wu0.y, wu0.z, wu0.w, wu1.x, wu1.y, wu1.z, wu1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float gate = __int2float_rn(gi[j]);
+          gate = __fmul_rn(gate, wg[j]);
+          gate = __fmul_rn(gate, ts);
+          float up = __int2float_rn(ui[j]);
+          up = __fmul_rn(up, wu[j]);
+          up = __fmul_rn(up, ts);
+          const float e = exp_cody_waite(-gate);
+          const float d = __fadd_rn(e, 1.0f);
+          const float sg = __fdiv_rn(gate, d);
+          h[i][j] = __fmul_rn(sg, up);
+          amax = fmaxf(amax, fabsf(h[i][j]));
+        }
+      }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    if (lane == 0) s_wmax[warp] = amax;
+    __syncthreads();
+    amax = s_wmax[0];
+    for (int w = 1; w < nwarps; ++w) amax = fmaxf(amax, s_wmax[w]);
+    const float scale = __fdiv_rn(127.0f, __fadd_rn(amax, 1e-12f));
+    const float inv = __fdiv_rn(1.0f, scale);
+    unsigned char* dst = out + m * row_bytes;
+#pragma unroll
+    for (int i = 0; i < kCpt; ++i) {
+      const int c = tid + i * nthreads;
+      if (c < nch) {
+        uint32_t w2[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int q = __float2int_rn(__fmul_rn(h[i][j], scale));
+          w2[j >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (j & 3));
+        }
+        *reinterpret_cast<uint2*>(dst + 8 * c) = make_uint2(w2[0], w2[1]);
+      }
+    }
+    if (tid < ntail)
+      *reinterpret_cast<uint2*>(dst + I + 8 * tid) =
+          make_uint2(tid == inv_word ? __float_as_uint(inv) : 0u, 0u);
+    __syncthreads();   // s_wmax is rewritten for the next row
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_swiglu_quant(const int32_t* acc, int64_t M, int I,
+                                const float* weight_scale, const float* token_scale,
+                                void* out, cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  const int nch = I / 8;
+  const int threads = std::max(32, std::min(kMaxThreads, ((nch + kCpt - 1) / kCpt + 31) / 32 * 32));
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, swiglu_quant_kernel, threads, 0);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = std::min<int64_t>(M, int64_t(std::max(1, per_sm)) * sms);
+  swiglu_quant_kernel<<<static_cast<unsigned>(grid), threads, 0, st>>>(
+      acc, M, I, weight_scale, token_scale, static_cast<unsigned char*>(out),
+      align_up(I, 32) + 32);
+  return cudaGetLastError();
+}
+
+}  // namespace moe_ep

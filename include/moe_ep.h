@@ -243,6 +243,24 @@ moe_status moe_dispatch_fused(const moe_shape* shape, const void* x,
                               int64_t recv_capacity_rows, void* workspace,
                               int32_t* dev_status, void* stream);
 
+/* GMM1 epilogue of the fused deep MoE, as a standalone pass over the grouped
+ * GEMM's int32 output (section 4.8.1 PerTokenDequantSwiGLU; section 8.7
+ * "INT32 -> [Cast + Dequant + SwiGLU + Quant] -> INT8").  Per row m:
+ *   v = fp32(acc[m][c]) * weight_scale[c] * token_scale[m]   (c < 2I)
+ *   h[j] = (v[j] / (1 + exp(-v[j]))) * v[I + j]                (j < I)
+ * then h is quantised like moe_dispatch's INT8 rows (scale = 127/(max|h| +
+ * 1e-12f), round half to even, 1/scale at byte align32(I)).  Each step is
+ * one fp32 round-to-nearest operation; exp is Cody-Waite reduction plus a
+ * degree-7 Taylor polynomial (deterministic, within 2 ulp of exp).
+ *   acc           int32 [M][2I], 16-byte aligned (gate half, then up half)
+ *   weight_scale  fp32 [2I] per column, 16-byte aligned
+ *   token_scale   fp32 [M] per row (e.g. the dispatched rows' 1/scale)
+ *   out           [M][align32(I) + 32] bytes, 16-byte aligned
+ * Valid when M >= 0 and 8 <= I <= 16384 with I % 8 == 0.  One launch. */
+moe_status moe_swiglu_quant(const int32_t* acc, int64_t M, int32_t I,
+                            const float* weight_scale, const float* token_scale,
+                            void* out, int32_t* dev_status, void* stream);
+
 /* (4') Combine over INT8 expert outputs -- the "+ dequant" of the pipeline
  * diagram (section 2.1, stage 4: shmem read + weighted sum + dequant).
  * Same gather and arithmetic as moe_combine, except that each expert-output

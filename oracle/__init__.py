@@ -60,6 +60,9 @@ def lib():
                                             _i32p, _f32p, _i32p, _i32p,
                                             _i64p, _i64p, i64, _u16p]
         L.oracle_token_layout.argtypes = [i, i, i, i, _i32p, _i32p, _u8p]
+        L.oracle_exp_f32.argtypes = [_f32p, _f32p, i64]
+        L.oracle_swiglu_quant_rows.argtypes = [i64, i, _i32p, _f32p, _f32p, _i64p,
+                                               i64, _u8p]
         L.oracle_combine_quant_tokens.argtypes = [i, i, i, i, i, i, _u8p, i64,
                                                   _i32p, _f32p, _i32p, _i32p,
                                                   _i64p, _i64p, i64, _u16p]
@@ -287,3 +290,32 @@ def token_layout(topk_idx, R, epr):
     st = lib().oracle_token_layout(R, bs, k, epr, _p(idx, _i32p), _p(tpr, _i32p),
                                    _p(inr, _u8p))
     return dict(tokens_per_rank=tpr, in_rank=inr, status=st)
+
+
+def exp_f32(x):
+    """The oracle's fp32 exp (Cody-Waite reduction + Taylor polynomial)."""
+    x = _c(x, np.float32)
+    out = np.empty_like(x)
+    lib().oracle_exp_f32(_p(x, _f32p), _p(out, _f32p), x.size)
+    return out
+
+
+def swiglu_quant(acc, weight_scale, token_scale, rows=None):
+    """GMM1 epilogue: acc int32 [M, 2I] -> INT8 row images uint8
+    [n, align32(I) + 32] (n = M, or len(rows))."""
+    acc = _c(acc, np.int32)
+    M, N = acc.shape
+    I = N // 2
+    ws = _c(weight_scale, np.float32)
+    ts = _c(token_scale, np.float32)
+    assert ws.size == N and ts.size == M
+    if rows is None:
+        rr, n = None, M
+    else:
+        rr = _c(rows, np.int64)
+        n = rr.size
+    out = np.zeros((n, row_bytes(I, 1)), np.uint8)
+    lib().oracle_swiglu_quant_rows(M, I, _p(acc, _i32p), _p(ws, _f32p), _p(ts, _f32p),
+                                   None if rr is None else _p(rr, _i64p), n,
+                                   _p(out, _u8p))
+    return out

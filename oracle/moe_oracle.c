@@ -417,3 +417,77 @@ int oracle_token_layout(int R, int bs, int k, int epr, const int32_t* topk_idx,
   }
   return status;
 }
+
+/* ---- exp by Cody-Waite reduction + Taylor polynomial (fp32) -------------- */
+
+static float exp_cw(float x) {
+  if (x > 88.0f) x = 88.0f;
+  if (x < -87.0f) x = -87.0f;
+  const float t = x * 1.44269504f;           /* x / ln 2 */
+  const float n = nearbyintf(t);             /* nearest integer, ties even */
+  float r = x - n * 0.693359375f;            /* ln 2, high part (exact product) */
+  r = r - n * -2.12194440e-4f;               /* ln 2, low part */
+  float p = 1.98412698e-4f;                  /* 1/7! */
+  p = p * r + 1.38888889e-3f;                /* 1/6! */
+  p = p * r + 8.33333333e-3f;                /* 1/5! */
+  p = p * r + 4.16666667e-2f;                /* 1/4! */
+  p = p * r + 1.66666667e-1f;                /* 1/3! */
+  p = p * r + 0.5f;                          /* 1/2! */
+  p = p * r + 1.0f;                          /* 1/1! */
+  p = p * r + 1.0f;                          /* 1/0! */
+  const int ni = (int)n;                     /* -126 .. 127 after the clamp */
+  const uint32_t bits = (uint32_t)(ni + 127) << 23;
+  float two_n;
+  memcpy(&two_n, &bits, 4);
+  return p * two_n;
+}
+
+void oracle_exp_f32(const float* in, float* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = exp_cw(in[i]);
+}
+
+/* ---- GMM1 epilogue: dequant, SwiGLU, requant (sections 4.8.1, 8.7) ------- */
+
+void oracle_swiglu_quant_rows(int64_t M, int I, const int32_t* acc,
+                              const float* weight_scale,
+                              const float* token_scale, const int64_t* rows,
+                              int64_t nrows, uint8_t* out) {
+  const int64_t S = oracle_row_bytes(I, 1);
+  const int64_t i_align = (int64_t)((I + 31) / 32) * 32;
+  float* h = (float*)malloc(sizeof(float) * (size_t)(I > 0 ? I : 1));
+  if (!h) return;
+  if (!rows) nrows = M;
+  for (int64_t i = 0; i < nrows; ++i) {
+    const int64_t m = rows ? rows[i] : i;
+    const int32_t* a_row = acc + m * 2 * (int64_t)I;
+    const float ts = token_scale[m];
+    float amax = 0.0f;
+    for (int j = 0; j < I; ++j) {
+      /* 1. Cast (RINT)  2. x weight_scale (column)  3. x per-token scale */
+      float gate = (float)a_row[j];
+      gate = gate * weight_scale[j];
+      gate = gate * ts;
+      float up = (float)a_row[I + j];
+      up = up * weight_scale[I + j];
+      up = up * ts;
+      /* 4. SwiGLU: Muls(-1), Exp, Adds(1), Div on the left half */
+      const float e = exp_cw(-gate);
+      const float d = e + 1.0f;
+      const float sg = gate / d;
+      h[j] = sg * up;
+      const float ah = fabsf(h[j]);
+      if (ah > amax) amax = ah;
+    }
+    /* 5. dynamic INT8 quantisation, as the dispatch's QuantProcess */
+    uint8_t* img = out + i * S;
+    memset(img, 0, (size_t)S);
+    const float scale = 127.0f / (amax + 1e-12f);
+    for (int j = 0; j < I; ++j) {
+      const float v = h[j] * scale;
+      img[j] = (uint8_t)(int8_t)(int)nearbyintf(v);
+    }
+    const float inv = 1.0f / scale;
+    memcpy(img + i_align, &inv, 4);
+  }
+  free(h);
+}

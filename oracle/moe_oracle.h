@@ -116,6 +116,27 @@ int oracle_combine_tokens(int R, int bs, int k, int epr, int H, int dtype,
 int oracle_token_layout(int R, int bs, int k, int epr, const int32_t* topk_idx,
                         int32_t* tokens_per_rank, uint8_t* in_rank);
 
+/* exp in fp32 by Cody and Waite's two-constant range reduction
+ * (x = n*ln2 + r, |r| <= ln2/2) and the degree-7 Taylor polynomial of e^r
+ * in Horner form, scaled by 2^n; input clamped to [-87, 88].  Every step is
+ * one fp32 operation rounded to nearest even.  Exported for pinning. */
+void oracle_exp_f32(const float* in, float* out, int64_t n);
+
+/* GMM1 epilogue of the fused deep MoE (section 4.8.1 PerTokenDequantSwiGLU,
+ * section 8.7 "Cast + Dequant + SwiGLU + Quant"): for row m of the int32
+ * accumulator acc [M][2I]:
+ *   v = fp32(acc) (round to nearest) * weight_scale[col] * token_scale[m]
+ *   a = v / (1 + exp(-v)) on the left half (columns j < I), right half b = v
+ *   h[j] = a[j] * b[j + I]
+ *   then the dispatch's dynamic INT8 quantisation of h: row image of
+ *   align32(I) + 32 bytes (codes, zeros, fp32 1/scale at align32(I), zeros).
+ * rows = NULL: all M rows, image i at out + i*row_bytes; else the listed
+ * rows, image i for rows[i]. */
+void oracle_swiglu_quant_rows(int64_t M, int I, const int32_t* acc,
+                              const float* weight_scale,
+                              const float* token_scale, const int64_t* rows,
+                              int64_t nrows, uint8_t* out);
+
 /* Combine over INT8 expert outputs (the "+ dequant" of the pipeline diagram,
  * section 2.1).  yq holds y_rows rows of oracle_row_bytes(H, 1) bytes laid
  * out like a dispatched INT8 row (H codes, fp32 1/scale at align32(H)).

@@ -38,6 +38,7 @@ def test_header_declares_the_four_stages():
     for n in ("moe_dispatch_layout", "moe_notify_dispatch", "moe_dispatch",
               "moe_combine", "moe_combine_quant", "moe_token_layout",
               "moe_dispatch_fused", "moe_fused_workspace_bytes",
+              "moe_swiglu_quant",
               "moe_status_string",
               "moe_recv_row_bytes", "moe_layout_workspace_bytes"):
         assert n in names

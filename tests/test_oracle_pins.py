@@ -474,13 +474,72 @@ def check_token_layout(oracle, seed=9):
             np.testing.assert_array_equal(TL["tokens_per_rank"], L["rank_send"])
 
 
+def check_exp(oracle):
+    x = np.linspace(-87.0, 88.0, 400001, dtype=np.float32)
+    y = oracle.exp_f32(x).astype(np.float64)
+    ref = np.exp(x.astype(np.float64))
+    ulp = np.abs(y - ref) / np.spacing(ref.astype(np.float32)).astype(np.float64)
+    assert ulp.max() <= 2.0                    # textbook method, fp32 Horner
+    assert float(oracle.exp_f32(np.array([0.0], np.float32))[0]) == 1.0
+    assert (np.diff(y) >= 0).all()             # monotone on the sweep
+
+
+def _swiglu_inputs(rng, M, I, big=False):
+    acc = np.round(rng.standard_normal((M, 2 * I)) * 2.0 ** 17).astype(np.int64)
+    if big:                                    # beyond 2^24: the cast rounds
+        acc[:, ::37] = acc[:, ::37] * 64 + 1
+    acc = acc.astype(np.int32)
+    ws = (rng.uniform(0.5, 1.5, 2 * I) * 4e-4).astype(np.float32)
+    ts = rng.uniform(0.005, 0.03, M).astype(np.float32)
+    return acc, ws, ts
+
+
+def check_swiglu_quant(oracle, seed=10):
+    rng = np.random.default_rng(seed)
+    for I, big in ((40, False), (256, True)):
+        M = 24
+        acc, ws, ts = _swiglu_inputs(rng, M, I, big)
+        img = oracle.swiglu_quant(acc, ws, ts)
+        ia = (I + 31) // 32 * 32
+        assert img.shape == (M, ia + 32)
+        q = img[:, :I].view(np.int8).astype(np.int64)
+        inv = img[:, ia:ia + 4].copy().view(np.float32)[:, 0].astype(np.float64)
+        assert not img[:, I:ia].any() and not img[:, ia + 4:].any()
+        # fp64 restatement of dequant -> SwiGLU (independent arithmetic)
+        v = acc.astype(np.float64) * ws.astype(np.float64) * ts.astype(np.float64)[:, None]
+        gate, up = v[:, :I], v[:, I:]
+        h = gate / (1.0 + np.exp(-gate)) * up
+        amax = np.abs(h).max(axis=1)
+        np.testing.assert_allclose(inv, (amax + 1e-12) / 127, rtol=1e-5)
+        # dequantised values within the quantisation step (+ fp32 slack)
+        err = np.abs(q * inv[:, None] - h)
+        assert (err <= (amax[:, None] + 1e-12) / 254 * (1 + 2.0 ** -10)
+                + 1e-6 * np.abs(h)).all()
+        # codes equal round-half-even of the fp64 value away from ties
+        t = h * (127.0 / (amax + 1e-12))[:, None]
+        margin = np.abs(np.abs(t - np.floor(t)) - 0.5)
+        ok = margin > 1e-3
+        np.testing.assert_array_equal(q[ok], np.rint(t)[ok].astype(np.int64))
+        # a listed-rows call gives the same images
+        rows = np.array([3, 0, M - 1], np.int64)
+        np.testing.assert_array_equal(oracle.swiglu_quant(acc, ws, ts, rows=rows),
+                                      img[rows])
+    # gate = 0 everywhere: silu(0) = 0, the row is all zero codes
+    acc = np.zeros((2, 64), np.int32)
+    acc[:, 32:] = 12345
+    img = oracle.swiglu_quant(acc, np.ones(64, np.float32), np.ones(2, np.float32))
+    assert not img[:, :32].any()
+    assert abs(float(img[0, 32:36].copy().view(np.float32)[0]) /
+               (float(np.float32(1e-12)) / 127) - 1) < 1e-6
+
+
 ALL_CHECKS = [
     check_handworked_layout_notify, check_layout_brute_force,
     check_layout_invariants, check_notify_closed_form, check_rows_closed_form,
     check_invalid_ids, check_handworked_quant, check_quant_properties,
     check_quant_zero_row, check_conversions, check_combine_special_cases,
     check_combine_one_hot_and_bound, check_combine_k1, check_dispatch_capacity,
-    check_combine_quant, check_token_layout,
+    check_combine_quant, check_token_layout, check_exp, check_swiglu_quant,
 ]
 
 
@@ -494,9 +553,11 @@ def test_oracle_pin(oracle_mod, check):
 # ---------------------------------------------------------------------------
 
 MUTANTS = {
-    "rint_truncates": ("(int)nearbyintf(v)", "(int)truncf(v)"),
-    "no_epsilon": ("amax + 1e-12f", "amax + 0.0f"),
-    "stores_scale": ("1.0f / scale", "scale"),
+    "rint_truncates": ("(int)nearbyintf(v)", "(int)truncf(v)", 0),
+    "requant_rint_truncates": ("(int)nearbyintf(v)", "(int)truncf(v)", 1),
+    "no_epsilon": ("amax + 1e-12f", "amax + 0.0f", 0),
+    "requant_no_epsilon": ("amax + 1e-12f", "amax + 0.0f", 1),
+    "stores_scale": ("1.0f / scale", "scale", 0),
     "fused_multiply_add": ("acc[h] = acc[h] + prod;",
                            "acc[h] = fmaf(to_f32(dtype, yrow[h]), w, acc[h]);", 0),
     "combine_reverse_k": ("for (int kk = 0; kk < k; ++kk) {\n"
@@ -524,6 +585,11 @@ MUTANTS = {
     "dequant_scale_after_codes": ("memcpy(&inv, img + h_align, 4);",
                                   "memcpy(&inv, img + H, 4);"),
     "token_layout_counts_pairs": ("row[e / epr] = 1;", "row[e / epr] += 1;"),
+    "swiglu_halves_swapped": ("float gate = (float)a_row[j];", "float gate = (float)a_row[I + j];"),
+    "swiglu_no_token_scale": ("      gate = gate * ts;\n", "      gate = gate * 1.0f;\n"),
+    "swiglu_sigmoid_not_silu": ("const float sg = gate / d;", "const float sg = 1.0f / d;"),
+    "exp_sign_error": ("const float e = exp_cw(-gate);", "const float e = exp_cw(gate);"),
+    "exp_low_part_dropped": ("r = r - n * -2.12194440e-4f;", "r = r - n * 0.0f;"),
 }
 
 

@@ -446,3 +446,44 @@ def test_fused_dispatch_edges_and_reuse(oracle_mod, pl):
     torch.cuda.synchronize()
     assert b0.status() == 0 and int(b0.count.abs().sum()) == 0
     assert b0.rank_recv_base.cpu().tolist() == [0] * (w0.R + 1)
+
+
+# ---------------------------------------------------------------------------
+# GMM1 epilogue (moe_swiglu_quant)
+# ---------------------------------------------------------------------------
+
+def _check_swiglu(oracle, ep, M, I, sample=None):
+    acc, ws, ts = W.gmm1_accumulators(M, I, seed=M + I)
+    rb = (I + 31) // 32 * 32 + 32
+    out = torch.full((max(M, 1), rb), 0xAB, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.moe_swiglu_quant(acc.cuda(), ws.cuda(), ts.cuda(), out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    if M == 0:
+        return
+    if sample is None:
+        ref = oracle.swiglu_quant(acc.numpy(), ws.numpy(), ts.numpy())
+        _eq("swiglu rows", out[:M].cpu().numpy(), ref)
+    else:
+        rng = np.random.default_rng(5)
+        rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, sample)]))
+        ref = oracle.swiglu_quant(acc.numpy(), ws.numpy(), ts.numpy(), rows=rows)
+        got = out[torch.from_numpy(rows).cuda()].cpu().numpy()
+        _eq("swiglu rows (sampled)", got, ref)
+        # whole buffer: every row written (tail pad is zero), codes reach 127
+        ia = (I + 31) // 32 * 32
+        assert int((out[:M, -1] != 0).sum().item()) == 0
+        q = out[:M, :I].view(torch.int8)
+        assert int((q.abs().amax(dim=1) != 127).sum().item()) == 0
+
+
+@pytest.mark.parametrize("M,I", [(3000, 2048), (500, 40), (257, 16384), (0, 64),
+                                 (1, 8)])
+def test_swiglu_quant_full(oracle_mod, ep, M, I):
+    _check_swiglu(oracle_mod, ep, M, I)
+
+
+def test_swiglu_quant_dsv3_size(oracle_mod, ep):
+    """DeepSeek-V3 shape: one row per dispatched pair (262,144), I = 2048."""
+    _check_swiglu(oracle_mod, ep, 262144, 2048, sample=1500)

@@ -171,6 +171,25 @@ def expert_outputs_int8(w: Workload, rows: Optional[int] = None) -> torch.Tensor
     return img
 
 
+def gmm1_accumulators(M: int, I: int, seed: int = 99):
+    """Synthetic grouped-GEMM outputs for the GMM1 epilogue: int32 acc
+    [M, 2I] ~ round(N(0,1) * 2^17) with every 37th column x64 + 1 (beyond
+    2^24, so the int-to-float cast rounds), per-column weight scales
+    U(0.5, 1.5) * 4e-4 and per-row token scales U(0.005, 0.03)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed * 16 + 7)
+    acc = torch.empty((M, 2 * I), dtype=torch.int32)
+    rows_per_chunk = max(1, (1 << 24) // max(1, 2 * I))
+    for r0 in range(0, M, rows_per_chunk):
+        r1 = min(M, r0 + rows_per_chunk)
+        v = torch.round(torch.randn((r1 - r0, 2 * I), generator=g) * 2.0 ** 17)
+        v[:, ::37] = v[:, ::37] * 64 + 1
+        acc[r0:r1] = v.to(torch.int32)
+    ws = (torch.rand((2 * I,), generator=g) + 0.5) * 4e-4
+    ts = torch.rand((M,), generator=g) * 0.025 + 0.005
+    return acc, ws.to(torch.float32), ts.to(torch.float32)
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """uint16 bit patterns of a bf16/fp16 CPU tensor (no copy)."""
     assert t.dtype in (torch.bfloat16, torch.float16)
