@@ -35,10 +35,13 @@ import workloads as W  # noqa: E402
 
 L2_FLUSH_BYTES = 256 << 20          # > 129 MB of L2
 SWIGLU_INTERMEDIATE = 2048          # expert intermediate size (DeepSeek-V3)
+EXTRA_STEPS = 50                    # timed iterations of the extra kernels
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = {                  # kernel -> source file (traffic staleness)
     "combine": "combine_moe_dispatch_layout_gb300/csrc/combine.cu",
     "dispatch": "combine_moe_dispatch_layout_gb300/csrc/dispatch.cu",
+    "combine_quant": "combine_moe_dispatch_layout_gb300/csrc/combine_quant.cu",
+    "swiglu_quant": "combine_moe_dispatch_layout_gb300/csrc/swiglu.cu",
 }
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
                "clocks_event_reasons.active,"
@@ -277,7 +280,7 @@ def run_gpu(args, w):
         for i in range(3):
             pl.run_combine_quant(b, yq, idx, wt, stream)
         cq_ms = []
-        for i in range(args.steps):
+        for i in range(min(args.steps, EXTRA_STEPS)):
             flush.fill_(i & 0xff)
             c0 = torch.cuda.Event(enable_timing=True)
             c1 = torch.cuda.Event(enable_timing=True)
@@ -292,6 +295,7 @@ def run_gpu(args, w):
         cq_bytes = alg_bytes(w)["combine_quant"]
         cq = {"us": cq_us, "achieved_gbs": cq_bytes / (cq_us * 1e-6) / 1e9,
               "algorithmic_bytes": cq_bytes,
+              "traffic": recorded_traffic("combine_quant", w.name),
               "frac": cq_bytes / (cq_us * 1e-6) / 1e9 / peak,
               "tokens_per_s": w.T / (cq_us * 1e-6)}
         del yq
@@ -311,7 +315,8 @@ def run_gpu(args, w):
         return float(np.mean([a.elapsed_time(c) for a, c in evs])) * 1e3
     for i in range(3):
         pl.run_dispatch_fused(b, x, idx, stream)
-    fused_us = timed(lambda: pl.run_dispatch_fused(b, x, idx, stream), args.steps)
+    fused_us = timed(lambda: pl.run_dispatch_fused(b, x, idx, stream),
+                     min(args.steps, EXTRA_STEPS))
     if b.status() != 0:
         raise RuntimeError("device status %d in fused dispatch" % b.status())
     separate_us = float(stage_mean[0] + stage_mean[1] + stage_mean[2]) * 1e3
@@ -328,9 +333,11 @@ def run_gpu(args, w):
         for i in range(3):
             ep.moe_swiglu_quant(acc_d, ws_d, ts_d, sw_out, b.dev_status, stream)
         sw_us = timed(lambda: ep.moe_swiglu_quant(acc_d, ws_d, ts_d, sw_out,
-                                                  b.dev_status, stream), args.steps)
+                                                  b.dev_status, stream),
+                      min(args.steps, EXTRA_STEPS))
         sw_bytes = w.P * (8 * I + (I + 31) // 32 * 32 + 32 + 4) + 8 * I
         sw = {"us": sw_us, "rows": w.P, "I": I, "algorithmic_bytes": sw_bytes,
+              "traffic": recorded_traffic("swiglu_quant", w.name),
               "achieved_gbs": sw_bytes / (sw_us * 1e-6) / 1e9,
               "frac": sw_bytes / (sw_us * 1e-6) / 1e9 / peak}
         del acc_d, sw_out
@@ -341,7 +348,7 @@ def run_gpu(args, w):
     for i in range(3):
         ep.moe_token_layout(b.shape, idx, tpr, inr, b.dev_status, stream)
     tl_ev = []
-    for i in range(args.steps):
+    for i in range(min(args.steps, EXTRA_STEPS)):
         flush.fill_(i & 0xff)
         t0e = torch.cuda.Event(enable_timing=True)
         t1e = torch.cuda.Event(enable_timing=True)

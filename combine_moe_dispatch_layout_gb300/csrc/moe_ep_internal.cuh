@@ -174,6 +174,37 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Combine: resolve the receive rows and gate weights of token g into the
+// shared tables rows[k], w[k] (one warp; lane kk handles pair kk).  A bad
+// expert id or a row outside [0, y_rows) gives row -1 and a status code.
+__device__ __forceinline__ void resolve_token(
+    int64_t g, const int32_t* __restrict__ topk_idx,
+    const float* __restrict__ weights, const int32_t* __restrict__ send_idx,
+    const int32_t* __restrict__ put_offset,
+    const int64_t* __restrict__ rank_recv_base, int R, int bs, int k, int epr,
+    int64_t y_rows, int64_t* rows, float* w, int32_t* dev_status, int lane) {
+  const int E = R * epr;
+  const int s = static_cast<int>(g / bs);
+  for (int kk = lane; kk < k; kk += 32) {
+    const int64_t pair = g * k + kk;
+    const int e = __ldg(topk_idx + pair);
+    const int32_t sidx = __ldg(send_idx + pair);
+    const float wt = __ldg(weights + pair);
+    int64_t row = -1;
+    if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+      set_status(dev_status, MOE_ERR_EXPERT_ID);
+    } else {
+      row = __ldg(rank_recv_base + e / epr) + __ldg(put_offset + int64_t(e) * R + s) + sidx;
+      if (row < 0 || row >= y_rows) {
+        set_status(dev_status, MOE_ERR_CAPACITY);
+        row = -1;
+      }
+    }
+    rows[kk] = row;
+    w[kk] = wt;
+  }
+}
+
 // ---- launchers (one per translation unit) ----------------------------------
 
 struct Shape {
