@@ -218,24 +218,25 @@ def run_gpu(args, w):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(evs=None):
+    def step(evs=None, st=None):
+        st = stream if st is None else st
         if evs:
-            evs[0].record(stream)
+            evs[0].record(st)
         pl.moe_dispatch_layout(b.shape, idx, b.count, b.rank_send, b.send_idx,
-                               b.workspace, b.dev_status, stream)
+                               b.workspace, b.dev_status, st)
         if evs:
-            evs[1].record(stream)
+            evs[1].record(st)
         pl.moe_notify_dispatch(b.shape, b.count, b.put_offset, b.total_recv,
                                b.rank_recv_base, b.recv_per_expert, b.max_bs,
-                               b.dev_status, stream)
+                               b.dev_status, st)
         if evs:
-            evs[2].record(stream)
-        pl.run_dispatch(b, x, idx, stream)
+            evs[2].record(st)
+        pl.run_dispatch(b, x, idx, st)
         if evs:
-            evs[3].record(stream)
-        pl.run_combine(b, y, idx, wt, stream)
+            evs[3].record(st)
+        pl.run_combine(b, y, idx, wt, st)
         if evs:
-            evs[4].record(stream)
+            evs[4].record(st)
 
     for i in range(args.warmup):
         flush.fill_(i & 0xff)
@@ -299,6 +300,29 @@ def run_gpu(args, w):
               "frac": cq_bytes / (cq_us * 1e-6) / 1e9 / peak,
               "tokens_per_s": w.T / (cq_us * 1e-6)}
         del yq
+
+    # ---- the same step replayed as a CUDA graph (no host enqueue cost) ------
+    gs = torch.cuda.Stream(dev)
+    gs.wait_stream(stream)
+    with torch.cuda.stream(gs):
+        step_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(step_graph, stream=gs):
+            step(st=gs)
+    stream.wait_stream(gs)
+    graph_ev = []
+    for i in range(min(args.steps, EXTRA_STEPS)):
+        flush.fill_(i & 0xff)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        step_graph.replay()
+        g1.record(stream)
+        graph_ev.append((g0, g1))
+    torch.cuda.synchronize()
+    if b.status() != 0:
+        raise RuntimeError("device status %d in graph replay" % b.status())
+    graph_us = float(np.mean([a.elapsed_time(c) for a, c in graph_ev])) * 1e3
+    del step_graph
 
     # ---- one-launch low-latency dispatch vs the three separate launches ------
     def timed(fn, n):
@@ -415,6 +439,7 @@ def run_gpu(args, w):
         },
         "combine_quant": cq,
         "token_layout_us": tl_us,
+        "graph_step_us": graph_us,
         "swiglu_quant": sw,
         "dispatch_fused": {"us": fused_us, "separate_us": separate_us,
                            "note": "layout+notify+dispatch in one cooperative "

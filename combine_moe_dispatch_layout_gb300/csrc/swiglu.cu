@@ -14,8 +14,9 @@
 // intrinsics; the unit is built with -fmad=false).  exp is computed by Cody
 // and Waite's two-constant range reduction, x = n*ln2 + r with |r| <= ln2/2,
 // and the degree-7 Taylor polynomial of e^r in Horner form, scaled by 2^n
-// (input clamped to [-87, 88]); the CPU oracle evaluates the same textbook
-// method in the same order, so results match bit for bit.
+// (input clamped to [-87, 88]); the reduction and Horner steps are fused
+// multiply-adds.  The CPU oracle evaluates the same textbook method in the
+// same order, so results match bit for bit.
 //
 // Persistent CTAs walk the rows; each thread owns 8-output chunks (two
 // 32-byte loads of the accumulator per chunk), max|h| is reduced with warp
@@ -28,28 +29,36 @@
 namespace moe_ep {
 namespace {
 
-constexpr int kMaxThreads = 512;   // with kCpt: I <= 16384
-constexpr int kCpt = 4;            // 8-output chunks per thread, at most
+constexpr int kMaxThreads = 512;
+// 8-output chunks per thread: 2 while that fits 512 threads (I <= 8192; more
+// warps per SM, measured fastest at I = 2048), else 4 (I <= 16384).
+
+// 1.5 * 2^23: adding it to a float of magnitude below 2^22 rounds that float
+// to an integer (ties to even), which then sits in the low mantissa bits.
+constexpr float kRoundMagic = 12582912.0f;
 
 __device__ __forceinline__ float exp_cody_waite(float x) {
   if (x > 88.0f) x = 88.0f;
   if (x < -87.0f) x = -87.0f;
   const float t = __fmul_rn(x, 1.44269504f);                 // x / ln 2
-  const float n = rintf(t);                                  // ties to even
-  float r = __fsub_rn(x, __fmul_rn(n, 0.693359375f));       // ln 2, high part
-  r = __fsub_rn(r, __fmul_rn(n, -2.12194440e-4f));          // ln 2, low part
+  const float s = __fadd_rn(t, kRoundMagic);                 // rint(t) in the low bits
+  const float n = __fsub_rn(s, kRoundMagic);                 // rint(t), exactly
+  float r = __fmaf_rn(-n, 0.693359375f, x);                  // x - n*C1 (ln 2, high part)
+  r = __fmaf_rn(-n, -2.12194440e-4f, r);                     // - n*C2 (ln 2, low part)
   float p = 1.98412698e-4f;                                  // 1/7!
-  p = __fadd_rn(__fmul_rn(p, r), 1.38888889e-3f);           // 1/6!
-  p = __fadd_rn(__fmul_rn(p, r), 8.33333333e-3f);           // 1/5!
-  p = __fadd_rn(__fmul_rn(p, r), 4.16666667e-2f);           // 1/4!
-  p = __fadd_rn(__fmul_rn(p, r), 1.66666667e-1f);           // 1/3!
-  p = __fadd_rn(__fmul_rn(p, r), 0.5f);                     // 1/2!
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);                     // 1/1!
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);                     // 1/0!
-  const int ni = static_cast<int>(n);                        // -126 .. 127
-  return __fmul_rn(p, __uint_as_float(static_cast<uint32_t>(ni + 127) << 23));
+  p = __fmaf_rn(p, r, 1.38888889e-3f);                       // 1/6!
+  p = __fmaf_rn(p, r, 8.33333333e-3f);                       // 1/5!
+  p = __fmaf_rn(p, r, 4.16666667e-2f);                       // 1/4!
+  p = __fmaf_rn(p, r, 1.66666667e-1f);                       // 1/3!
+  p = __fmaf_rn(p, r, 0.5f);                                 // 1/2!
+  p = __fmaf_rn(p, r, 1.0f);                                 // 1/1!
+  p = __fmaf_rn(p, r, 1.0f);                                 // 1/0!
+  // n is in -126 .. 127: the low 9 bits of s hold n (two's complement), so
+  // (s + 127) << 23 is the bit pattern of 2^n.
+  return __fmul_rn(p, __uint_as_float((__float_as_uint(s) + 127u) << 23));
 }
 
+template <int kCpt>
 __global__ void __launch_bounds__(kMaxThreads)
 swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I,
                     const float* __restrict__ weight_scale,
@@ -113,13 +122,17 @@ swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I,
     for (int i = 0; i < kCpt; ++i) {
       const int c = tid + i * nthreads;
       if (c < nch) {
-        uint32_t w2[2] = {0u, 0u};
+        // q = rint(h * scale) in [-127, 127]; after adding kRoundMagic the
+        // low byte of the float's bits is q as an int8.
+        uint32_t b[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int q = __float2int_rn(__fmul_rn(h[i][j], scale));
-          w2[j >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (j & 3));
-        }
-        *reinterpret_cast<uint2*>(dst + 8 * c) = make_uint2(w2[0], w2[1]);
+        for (int j = 0; j < 8; ++j)
+          b[j] = __float_as_uint(__fadd_rn(__fmul_rn(h[i][j], scale), kRoundMagic));
+        const uint32_t w0 = __byte_perm(__byte_perm(b[0], b[1], 0x0040),
+                                        __byte_perm(b[2], b[3], 0x0040), 0x5410);
+        const uint32_t w1 = __byte_perm(__byte_perm(b[4], b[5], 0x0040),
+                                        __byte_perm(b[6], b[7], 0x0040), 0x5410);
+        *reinterpret_cast<uint2*>(dst + 8 * c) = make_uint2(w0, w1);
       }
     }
     if (tid < ntail)
@@ -129,6 +142,24 @@ swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I,
   }
 }
 
+template <int kCpt>
+cudaError_t launch_t(const int32_t* acc, int64_t M, int I, const float* weight_scale,
+                     const float* token_scale, void* out, cudaStream_t st) {
+  const int nch = I / 8;
+  const int threads = std::max(32, std::min(kMaxThreads, ((nch + kCpt - 1) / kCpt + 31) / 32 * 32));
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, swiglu_quant_kernel<kCpt>, threads, 0);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = std::min<int64_t>(M, int64_t(std::max(1, per_sm)) * sms);
+  swiglu_quant_kernel<kCpt><<<static_cast<unsigned>(grid), threads, 0, st>>>(
+      acc, M, I, weight_scale, token_scale, static_cast<unsigned char*>(out),
+      align_up(I, 32) + 32);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_swiglu_quant(const int32_t* acc, int64_t M, int I,
@@ -136,18 +167,9 @@ cudaError_t launch_swiglu_quant(const int32_t* acc, int64_t M, int I,
                                 void* out, cudaStream_t st) {
   if (M == 0) return cudaSuccess;
   const int nch = I / 8;
-  const int threads = std::max(32, std::min(kMaxThreads, ((nch + kCpt - 1) / kCpt + 31) / 32 * 32));
-  int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, swiglu_quant_kernel, threads, 0);
-  if (e != cudaSuccess) return e;
-  const int64_t grid = std::min<int64_t>(M, int64_t(std::max(1, per_sm)) * sms);
-  swiglu_quant_kernel<<<static_cast<unsigned>(grid), threads, 0, st>>>(
-      acc, M, I, weight_scale, token_scale, static_cast<unsigned char*>(out),
-      align_up(I, 32) + 32);
-  return cudaGetLastError();
+  return nch <= 2 * kMaxThreads
+             ? launch_t<2>(acc, M, I, weight_scale, token_scale, out, st)
+             : launch_t<4>(acc, M, I, weight_scale, token_scale, out, st);
 }
 
 }  // namespace moe_ep

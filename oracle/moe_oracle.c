@@ -419,22 +419,27 @@ int oracle_token_layout(int R, int bs, int k, int epr, const int32_t* topk_idx,
 }
 
 /* ---- exp by Cody-Waite reduction + Taylor polynomial (fp32) -------------- */
+/* e^x = 2^n * e^r with n = nearest integer to x / ln 2 and r = x - n ln 2,
+ * |r| <= ln 2 / 2.  ln 2 is split into C1 = 0.693359375 (a few bits, so n*C1
+ * is exact) and C2 = ln 2 - C1 (Cody and Waite).  e^r is the degree-7 Taylor
+ * polynomial in Horner form.  Each reduction step and each Horner step is one
+ * fused multiply-add (fmaf: a*b+c rounded once). */
 
 static float exp_cw(float x) {
   if (x > 88.0f) x = 88.0f;
   if (x < -87.0f) x = -87.0f;
   const float t = x * 1.44269504f;           /* x / ln 2 */
   const float n = nearbyintf(t);             /* nearest integer, ties even */
-  float r = x - n * 0.693359375f;            /* ln 2, high part (exact product) */
-  r = r - n * -2.12194440e-4f;               /* ln 2, low part */
+  float r = fmaf(-n, 0.693359375f, x);       /* x - n*C1 */
+  r = fmaf(-n, -2.12194440e-4f, r);          /* - n*C2 */
   float p = 1.98412698e-4f;                  /* 1/7! */
-  p = p * r + 1.38888889e-3f;                /* 1/6! */
-  p = p * r + 8.33333333e-3f;                /* 1/5! */
-  p = p * r + 4.16666667e-2f;                /* 1/4! */
-  p = p * r + 1.66666667e-1f;                /* 1/3! */
-  p = p * r + 0.5f;                          /* 1/2! */
-  p = p * r + 1.0f;                          /* 1/1! */
-  p = p * r + 1.0f;                          /* 1/0! */
+  p = fmaf(p, r, 1.38888889e-3f);            /* 1/6! */
+  p = fmaf(p, r, 8.33333333e-3f);            /* 1/5! */
+  p = fmaf(p, r, 4.16666667e-2f);            /* 1/4! */
+  p = fmaf(p, r, 1.66666667e-1f);            /* 1/3! */
+  p = fmaf(p, r, 0.5f);                      /* 1/2! */
+  p = fmaf(p, r, 1.0f);                      /* 1/1! */
+  p = fmaf(p, r, 1.0f);                      /* 1/0! */
   const int ni = (int)n;                     /* -126 .. 127 after the clamp */
   const uint32_t bits = (uint32_t)(ni + 127) << 23;
   float two_n;

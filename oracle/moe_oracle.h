@@ -119,7 +119,9 @@ int oracle_token_layout(int R, int bs, int k, int epr, const int32_t* topk_idx,
 /* exp in fp32 by Cody and Waite's two-constant range reduction
  * (x = n*ln2 + r, |r| <= ln2/2) and the degree-7 Taylor polynomial of e^r
  * in Horner form, scaled by 2^n; input clamped to [-87, 88].  Every step is
- * one fp32 operation rounded to nearest even.  Exported for pinning. */
+ * one fp32 operation rounded to nearest even; the two reduction steps and the
+ * Horner steps are fused multiply-adds (one rounding each).  Exported for
+ * pinning. */
 void oracle_exp_f32(const float* in, float* out, int64_t n);
 
 /* GMM1 epilogue of the fused deep MoE (section 4.8.1 PerTokenDequantSwiGLU,

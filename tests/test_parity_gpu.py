@@ -487,3 +487,44 @@ def test_swiglu_quant_full(oracle_mod, ep, M, I):
 def test_swiglu_quant_dsv3_size(oracle_mod, ep):
     """DeepSeek-V3 shape: one row per dispatched pair (262,144), I = 2048."""
     _check_swiglu(oracle_mod, ep, 262144, 2048, sample=1500)
+
+
+# ---------------------------------------------------------------------------
+# CUDA graph capture and replay of the four calls
+# ---------------------------------------------------------------------------
+
+def test_pipeline_graph_capture_and_replay(oracle_mod, pl):
+    """The four entry points enqueue nothing but kernels (and memsets) on the
+    caller's stream, so the pipeline can be captured once and replayed; the
+    layout workspace's epoch protocol works across replays."""
+    w = W.Workload("graph", R=4, epr=4, bs=600, k=4, H=256)    # 3 tiles/rank
+    b = pl.PipelineBuffers(w.R, w.bs, w.k, w.epr, w.H, w.dtype, w.quant)
+    idx_d = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
+    wt_d = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
+    x_d = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    y_d = torch.empty((w.P, w.H), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    # warm up (lazy module loading, attribute setting) outside the capture
+    with torch.cuda.stream(s):
+        pl.run_pipeline(b, x_d.zero_(), idx_d.zero_(), wt_d.zero_(), y_d.zero_(), s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pl.run_pipeline(b, x_d, idx_d, wt_d, y_d, s)
+    for seed in (11, 12):
+        ww = w.with_(seed=seed)
+        idx, wt = W.routing(ww)
+        x, y = W.tokens(ww), W.expert_outputs(ww)
+        idx_d.copy_(idx)
+        wt_d.copy_(wt)
+        x_d.copy_(x)
+        y_d.copy_(y)
+        b.dev_status.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert b.status() == 0
+        ref = _oracle_all(oracle_mod, ww, idx.numpy(), wt.numpy(), x, y)
+        _check_layout_notify(b, ref)
+        _eq("recv(graph)", b.recv.cpu().numpy(), ref["recv"])
+        _eq("out(graph)", b.out.view(torch.int16).cpu().numpy().view(np.uint16),
+            ref["out"])
