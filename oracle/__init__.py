@@ -26,6 +26,7 @@ _i32p = ctypes.POINTER(ctypes.c_int32)
 _i64p = ctypes.POINTER(ctypes.c_int64)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _u8p = ctypes.POINTER(ctypes.c_uint8)
+_i8p = ctypes.POINTER(ctypes.c_int8)
 _f32p = ctypes.POINTER(ctypes.c_float)
 
 
@@ -66,6 +67,12 @@ def lib():
         L.oracle_combine_quant_tokens.argtypes = [i, i, i, i, i, i, _u8p, i64,
                                                   _i32p, _f32p, _i32p, _i32p,
                                                   _i64p, _i64p, i64, _u16p]
+        L.oracle_grouped_gemm_i8.argtypes = [i, _i64p, i, i, _i8p, i64, _i8p,
+                                             _i64p, i64, _i32p]
+        L.oracle_deq_combine_tokens.argtypes = [i, i, i, i, i, i, _i32p, i64,
+                                                _f32p, _f32p, _i32p, _f32p,
+                                                _i32p, _i32p, _i64p, _i64p,
+                                                i64, _u16p]
         _lib = L
     return _lib
 
@@ -319,3 +326,128 @@ def swiglu_quant(acc, weight_scale, token_scale, rows=None):
                                    None if rr is None else _p(rr, _i64p), n,
                                    _p(out, _u8p))
     return out
+
+
+# ---- fused deep MoE (section 4.3: GMM1 -> DeqSwigluQuant -> GMM2 ->
+#      DeqCombine), on top of the dispatch above ----------------------------
+
+def group_offsets(rank_recv_base, put_offset, R, epr):
+    """First receive row of every expert (int64 [E+1]): expert e's rows
+    start at rank_recv_base[e // epr] + put_offset[e*R + 0] (its first
+    source rank); the last entry is the total row count."""
+    base = _c(rank_recv_base, np.int64)
+    po = _c(put_offset, np.int32)
+    E = R * epr
+    off = np.empty(E + 1, np.int64)
+    for e in range(E):
+        off[e] = int(base[e // epr]) + int(po[e * R])
+    off[E] = int(base[R])
+    return off
+
+
+def grouped_gemm(a, group_off, b, rows=None):
+    """c[i][n] = sum_k a[i][k] * b[g][n][k] (int32), g the group of the
+    row.  a: int8 codes, uint8/int8 [n, lda] (first K = b.shape[2] bytes
+    used); b: int8 [G, N, K].  rows: global row of each a row (None: a
+    holds all rows in order)."""
+    a = _c(a, np.uint8).view(np.int8)
+    b = _c(b, np.int8)
+    G, N, K = b.shape
+    off = _c(group_off, np.int64)
+    assert off.size == G + 1 and a.shape[1] >= K
+    n = a.shape[0]
+    rr = None if rows is None else _c(rows, np.int64)
+    if rr is None:
+        assert n == int(off[G])
+    else:
+        assert rr.size == n
+    c = np.zeros((n, N), np.int32)
+    st = lib().oracle_grouped_gemm_i8(G, _p(off, _i64p), K, N, _p(a, _i8p),
+                                      a.shape[1], _p(b, _i8p),
+                                      None if rr is None else _p(rr, _i64p), n,
+                                      _p(c, _i32p))
+    assert st == 0, "grouped_gemm: invalid row or int32 overflow"
+    return c
+
+
+def deq_combine(acc2, weight_scale, row_scale, topk_idx, topk_weights,
+                send_idx, put_offset, rank_recv_base, R, epr, dtype,
+                tokens=None):
+    """DeqCombine.  acc2 int32 [rows, H] (by receive row, or [n*k, H] in
+    (token, k) order with ``tokens``), weight_scale fp32 [E, H], row_scale
+    fp32 per acc2 row.  Returns (out uint16 [n, H], status)."""
+    acc2 = _c(acc2, np.int32)
+    ws = _c(weight_scale, np.float32)
+    rs = _c(row_scale, np.float32)
+    idx = _c(topk_idx, np.int32)
+    w = _c(topk_weights, np.float32)
+    T, k = idx.shape
+    bs = T // R
+    H = acc2.shape[1]
+    assert ws.shape == (R * epr, H) and rs.size == acc2.shape[0]
+    if tokens is None:
+        toks, n = None, T
+    else:
+        toks = _c(tokens, np.int64)
+        n = toks.size
+        assert acc2.shape[0] == n * k
+    out = np.zeros((n, H), np.uint16)
+    st = lib().oracle_deq_combine_tokens(
+        R, bs, k, epr, H, dtype, _p(acc2, _i32p), acc2.shape[0], _p(ws, _f32p),
+        _p(rs, _f32p), _p(idx, _i32p), _p(w, _f32p),
+        _p(_c(send_idx, np.int32), _i32p), _p(_c(put_offset, np.int32), _i32p),
+        _p(_c(rank_recv_base, np.int64), _i64p),
+        None if toks is None else _p(toks, _i64p), n, _p(out, _u16p))
+    return out, st
+
+
+def row_inv_scale(images, K):
+    """The fp32 1/scale stored at byte align32(K) of INT8 row images."""
+    im = _c(images, np.uint8)
+    ka = (K + 31) // 32 * 32
+    return im[:, ka:ka + 4].copy().view(np.float32)[:, 0].copy()
+
+
+def deep_moe(x_bits, topk_idx, topk_weights, R, epr, dtype, w1, ws1, w2, ws2,
+             tokens=None):
+    """The fused deep MoE's data path (section 4.3) for all tokens, or for
+    the listed ones: dispatch with INT8 quantisation; GMM1 = codes x w1[e]
+    (int8 [E, 2I, H]); DeqSwigluQuant with weight_scale ws1[e] and the
+    dispatch row's 1/scale as per-token scale; GMM2 = codes x w2[e] (int8
+    [E, H, I]); DeqCombine with ws2 [E, H] and the requantised row's
+    1/scale.  Returns dict(out uint16 [n, H], acc1, x2, acc2, rows)."""
+    idx = _c(topk_idx, np.int32)
+    T, k = idx.shape
+    H = x_bits.shape[1]
+    E, N1, K1 = w1.shape
+    I = N1 // 2
+    assert K1 == H and w2.shape == (E, H, I) and E == R * epr
+    L = layout(idx, R, epr)
+    Nn = notify(L["count"], R, T // R, epr)
+    off = group_offsets(Nn["rank_recv_base"], Nn["put_offset"], R, epr)
+    if tokens is None:
+        recv, st = dispatch(x_bits, idx, L["send_idx"], Nn["put_offset"],
+                            Nn["rank_recv_base"], R, epr, dtype, True)
+        rows = np.arange(int(off[E]), dtype=np.int64)
+        a1, r1 = recv, None
+    else:
+        toks = _c(tokens, np.int64)
+        images, row_ids, st = dispatch_tokens(
+            x_bits, idx, L["send_idx"], Nn["put_offset"], Nn["rank_recv_base"],
+            R, epr, dtype, True, toks)
+        rows = row_ids.reshape(-1)
+        a1, r1 = images.reshape(rows.size, -1), rows
+    assert st == 0
+    acc1 = grouped_gemm(a1, off, w1, rows=r1)
+    ts1 = row_inv_scale(a1, H)
+    grp = np.searchsorted(off, rows, side="right") - 1
+    x2 = np.zeros((rows.size, row_bytes(I, 1)), np.uint8)
+    for e in np.unique(grp):
+        sel = np.nonzero(grp == e)[0]
+        x2[sel] = swiglu_quant(acc1[sel], ws1[e], ts1[sel])
+    acc2 = grouped_gemm(x2, off, w2, rows=r1)
+    out, st2 = deq_combine(acc2, ws2, row_inv_scale(x2, I), idx, topk_weights,
+                           L["send_idx"], Nn["put_offset"], Nn["rank_recv_base"],
+                           R, epr, dtype, tokens=tokens)
+    assert st2 == 0
+    return dict(out=out, acc1=acc1, x2=x2, acc2=acc2, rows=rows, group_off=off)

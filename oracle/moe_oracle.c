@@ -496,3 +496,78 @@ void oracle_swiglu_quant_rows(int64_t M, int I, const int32_t* acc,
   }
   free(h);
 }
+
+/* ---- fused deep MoE: grouped INT8 GEMM (sections 4.1, 4.3: GMM1 / GMM2,
+ *      INT8 x INT8 -> INT32) ----------------------------------------------- */
+
+int oracle_grouped_gemm_i8(int G, const int64_t* group_off, int K, int N,
+                           const int8_t* a, int64_t lda, const int8_t* b,
+                           const int64_t* rows, int64_t nrows, int32_t* c) {
+  if (G < 1 || K < 0 || N < 1) return ST_INVALID;
+  const int64_t M = group_off[G];
+  if (!rows) nrows = M;
+  for (int64_t i = 0; i < nrows; ++i) {
+    const int64_t m = rows ? rows[i] : i;
+    if (m < 0 || m >= M) return ST_INVALID;
+    int g = 0;                                 /* the group that owns row m */
+    while (!(group_off[g] <= m && m < group_off[g + 1])) ++g;
+    const int8_t* arow = a + (rows ? i : m) * lda;
+    for (int n = 0; n < N; ++n) {
+      const int8_t* brow = b + ((int64_t)g * N + n) * K;
+      int64_t acc = 0;
+      for (int kk = 0; kk < K; ++kk) acc += (int64_t)arow[kk] * (int64_t)brow[kk];
+      if (acc > INT32_MAX || acc < INT32_MIN) return ST_INVALID;
+      c[i * (int64_t)N + n] = (int32_t)acc;
+    }
+  }
+  return ST_OK;
+}
+
+/* ---- fused deep MoE: DeqCombine (section 4.3, stage 3) ------------------- */
+
+int oracle_deq_combine_tokens(int R, int bs, int k, int epr, int H, int dtype,
+                              const int32_t* acc2, int64_t y_rows,
+                              const float* weight_scale, const float* row_scale,
+                              const int32_t* topk_idx, const float* topk_weights,
+                              const int32_t* send_idx, const int32_t* put_offset,
+                              const int64_t* rank_recv_base,
+                              const int64_t* tokens, int64_t ntok, uint16_t* out) {
+  const int64_t T = (int64_t)R * bs;
+  if (!tokens) ntok = T;
+  float* acc = (float*)malloc(sizeof(float) * (size_t)(H > 0 ? H : 1));
+  if (!acc) return ST_INVALID;
+  int status = ST_OK;
+  for (int64_t i = 0; i < ntok; ++i) {
+    const int64_t g = tokens ? tokens[i] : i;
+    for (int h = 0; h < H; ++h) acc[h] = 0.0f;
+    for (int kk = 0; kk < k; ++kk) {
+      const int64_t row = oracle_dst_row(R, bs, k, epr, topk_idx, send_idx,
+                                         put_offset, rank_recv_base, g, kk);
+      if (row < 0) {
+        if (!status) status = ST_EXPERT_ID;
+        continue;
+      }
+      if (!tokens && row >= y_rows) {
+        if (!status) status = ST_CAPACITY;
+        continue;
+      }
+      const int32_t e = topk_idx[g * k + kk];
+      const int64_t yr = tokens ? i * k + kk : row;  /* listed: (token, k) order */
+      const int32_t* yrow = acc2 + yr * (int64_t)H;
+      const float* ws = weight_scale + (int64_t)e * H;
+      const float ts = row_scale[yr];
+      const float w = topk_weights[g * k + kk];
+      for (int h = 0; h < H; ++h) {
+        /* Cast FP32 (RINT), x weight_scale (column), x per-token scale */
+        float y = (float)yrow[h];
+        y = y * ws[h];
+        y = y * ts;
+        const float prod = y * w;                      /* Muls by the score */
+        acc[h] = acc[h] + prod;                        /* Add */
+      }
+    }
+    for (int h = 0; h < H; ++h) out[i * (int64_t)H + h] = from_f32(dtype, acc[h]);
+  }
+  free(acc);
+  return status;
+}

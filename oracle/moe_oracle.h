@@ -154,6 +154,35 @@ int oracle_combine_quant_tokens(int R, int bs, int k, int epr, int H, int dtype,
                                 const int64_t* tokens, int64_t ntok,
                                 uint16_t* out);
 
+/* Grouped INT8 GEMM of the fused deep MoE (section 4.3, GMM1 and GMM2:
+ * INT8 x INT8 -> INT32).  Group g owns rows [group_off[g], group_off[g+1])
+ * of a (int8 codes at byte 0 of rows lda bytes apart, K codes each) and
+ * weight matrix b[g] (int8 [N][K], row n = output column n):
+ * c[m][n] = sum_k a[m][k] * b[g][n][k], summed in int64 and stored as
+ * int32.  With rows == NULL, a holds all M = group_off[G] rows and c is
+ * [M][N]; else a holds nrows rows in list order (row i of a is global row
+ * rows[i], which selects the group) and c[i][:] is its result.  Returns 1
+ * (invalid) for a row outside [0, M) or a sum outside int32. */
+int oracle_grouped_gemm_i8(int G, const int64_t* group_off, int K, int N,
+                           const int8_t* a, int64_t lda, const int8_t* b,
+                           const int64_t* rows, int64_t nrows, int32_t* c);
+
+/* DeqCombine of the fused deep MoE (section 4.3, stage 3): expert-output
+ * rows are int32 GMM2 accumulators acc2 [y_rows][H].  For token g and
+ * k-slot kk (row = the dispatch row of (g, kk), e = its expert):
+ * y = ((float)acc2[row][h] * weight_scale[e][h]) * row_scale[row], one
+ * rounding each; then the combine of section 2.6: acc = acc + (y * w),
+ * k in order, RNE to the token dtype.  With tokens == NULL acc2 and
+ * row_scale are indexed by receive row; with a token list they hold the
+ * ntok*k rows of the listed tokens in (token, k) order. */
+int oracle_deq_combine_tokens(int R, int bs, int k, int epr, int H, int dtype,
+                              const int32_t* acc2, int64_t y_rows,
+                              const float* weight_scale, const float* row_scale,
+                              const int32_t* topk_idx, const float* topk_weights,
+                              const int32_t* send_idx, const int32_t* put_offset,
+                              const int64_t* rank_recv_base,
+                              const int64_t* tokens, int64_t ntok, uint16_t* out);
+
 #ifdef __cplusplus
 }
 #endif

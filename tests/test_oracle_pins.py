@@ -533,6 +533,131 @@ def check_swiglu_quant(oracle, seed=10):
                (float(np.float32(1e-12)) / 127) - 1) < 1e-6
 
 
+def check_grouped_gemm(oracle, seed=11):
+    rng = np.random.default_rng(seed)
+    # numpy int64 matmul per group, with an empty group and a ragged K
+    for G, N, K, sizes in ((3, 5, 37, (3, 0, 7)), (4, 16, 130, (1, 9, 0, 20))):
+        off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+        M = int(off[-1])
+        lda = K + 11                            # codes at byte 0 of wider rows
+        a = rng.integers(-127, 128, (M, lda)).astype(np.int8)
+        b = rng.integers(-127, 128, (G, N, K)).astype(np.int8)
+        c = oracle.grouped_gemm(a.view(np.uint8), off, b)
+        for g in range(G):
+            ref = a[off[g]:off[g + 1], :K].astype(np.int64) @ b[g].T.astype(np.int64)
+            np.testing.assert_array_equal(c[off[g]:off[g + 1]], ref)
+        # listed rows (a holds only those rows) give the same results
+        rows = np.array([M - 1, 0, 2], np.int64)
+        np.testing.assert_array_equal(
+            oracle.grouped_gemm(a[rows].view(np.uint8), off, b, rows=rows), c[rows])
+    # identity weights return the codes; group g's weights g*I scale by g
+    K = 24
+    off = np.array([0, 4, 9], np.int64)
+    a = rng.integers(-127, 128, (9, K)).astype(np.int8)
+    b = np.stack([np.eye(K, dtype=np.int8), 2 * np.eye(K, dtype=np.int8)])
+    c = oracle.grouped_gemm(a.view(np.uint8), off, b)
+    np.testing.assert_array_equal(c[:4], a[:4].astype(np.int32))
+    np.testing.assert_array_equal(c[4:], 2 * a[4:].astype(np.int32))
+    # the extreme sum: K = 7168 products of 127 * 127 (and of -127 * 127)
+    K = 7168
+    a = np.full((2, K), 127, np.int8)
+    a[1] = -127
+    b = np.full((1, 1, K), 127, np.int8)
+    c = oracle.grouped_gemm(a.view(np.uint8), np.array([0, 2], np.int64), b)
+    assert c[0, 0] == 127 * 127 * K and c[1, 0] == -127 * 127 * K
+
+
+def check_deq_combine(oracle, seed=12):
+    rng = np.random.default_rng(seed)
+    R, epr, bs, k, H = 2, 3, 9, 3, 40
+    wl = W.Workload("dq", R=R, epr=epr, bs=bs, H=H, k=k, seed=seed)
+    idx, wt = W.routing(wl)
+    idx, wt = idx.numpy(), wt.numpy()
+    L = oracle.layout(idx, R, epr)
+    N = oracle.notify(L["count"], R, bs, epr)
+    P = R * bs * k
+    args = (idx, wt, L["send_idx"], N["put_offset"], N["rank_recv_base"], R, epr, 0)
+    # unit scales and bf16-exact accumulators: the pinned combine of those values
+    acc2 = rng.integers(-256, 257, (P, H)).astype(np.int32)
+    ones_w = np.ones((R * epr, H), np.float32)
+    ones_r = np.ones(P, np.float32)
+    out, st = oracle.deq_combine(acc2, ones_w, ones_r, *args)
+    assert st == 0
+    y_bits = oracle.from_f32(acc2.astype(np.float32), 0)
+    ref, _ = oracle.combine(y_bits, idx, wt, L["send_idx"], N["put_offset"],
+                            N["rank_recv_base"], R, epr, 0)
+    np.testing.assert_array_equal(out, ref)
+    # general scales: float64 bound
+    acc2 = rng.integers(-2 ** 20, 2 ** 20, (P, H)).astype(np.int32)
+    ws = rng.uniform(0.5, 1.5, (R * epr, H)).astype(np.float32) * 1e-4
+    rs = rng.uniform(0.001, 0.05, P).astype(np.float32)
+    out, st = oracle.deq_combine(acc2, ws, rs, *args)
+    assert st == 0
+    rows = oracle.dst_rows(idx, L["send_idx"], N["put_offset"], N["rank_recv_base"], R, epr)
+    y = (acc2[rows].astype(np.float64) * ws[idx].astype(np.float64)
+         * rs[rows].astype(np.float64)[..., None])
+    exact = (y * wt[..., None].astype(np.float64)).sum(axis=1)
+    got = oracle.to_f32(out, 0).astype(np.float64)
+    bound = np.abs(exact) * 2.0 ** -8 + (np.abs(y) * wt[..., None]).sum(axis=1) * 2.0 ** -20
+    assert (np.abs(got - exact) <= bound + 1e-30).all()
+    # two roundings per term, checked where they show in bf16: (1 + 2^-8)
+    # then + 673 * (24929 * 2^-48) = 2^-24 + 2^-48.  Rounded product:
+    # 1 + 2^-8 + 2^-24 is an fp32 tie (-> 1 + 2^-8), a bf16 tie (-> 1.0);
+    # a fused multiply-add would give 1 + 2^-8 + 2^-23 -> 1 + 2^-7.
+    idx2 = np.array([[0, 1]], np.int32)
+    wt2 = np.array([[2.0 ** -8, 24929 * 2.0 ** -48]], np.float32)
+    L2 = oracle.layout(idx2, 1, 2)
+    N2 = oracle.notify(L2["count"], 1, 1, 2)
+    r2 = oracle.dst_rows(idx2, L2["send_idx"], N2["put_offset"], N2["rank_recv_base"], 1, 2)
+    a2 = np.zeros((2, 8), np.int32)
+    a2[r2[0, 0]] = 257
+    a2[r2[0, 1]] = 673
+    out2, st = oracle.deq_combine(a2, np.ones((2, 8), np.float32), np.ones(2, np.float32),
+                                  idx2, wt2, L2["send_idx"], N2["put_offset"],
+                                  N2["rank_recv_base"], 1, 2, 0)
+    assert st == 0 and (out2 == 0x3F80).all()
+    # listed tokens: rows in (token, k) order give the same output rows
+    toks = np.array([5, 0, R * bs - 1], np.int64)
+    sub, st = oracle.deq_combine(acc2[rows[toks].reshape(-1)], ws,
+                                 rs[rows[toks].reshape(-1)], *args, tokens=toks)
+    assert st == 0
+    np.testing.assert_array_equal(sub, out[toks])
+
+
+def check_deep_moe(oracle, seed=13):
+    R, epr, bs, k, H, I = 2, 2, 12, 2, 64, 32
+    wl = W.Workload("deep", R=R, epr=epr, bs=bs, H=H, k=k, seed=seed)
+    idx, wt = W.routing(wl)
+    idx, wt = idx.numpy(), wt.numpy()
+    x = W.tokens(wl)
+    w1, ws1, w2, ws2 = (t.numpy() for t in W.moe_weights(R * epr, H, I, seed=seed))
+    ws1 = ws1 * 40.0                           # gate values of order 1
+    ws2 = ws2 * 40.0
+    res = oracle.deep_moe(W.bits(x), idx, wt, R, epr, 0, w1, ws1, w2, ws2)
+    # expert groups: the exclusive prefix of the per-expert row counts
+    L = oracle.layout(idx, R, epr)
+    N = oracle.notify(L["count"], R, bs, epr)
+    np.testing.assert_array_equal(
+        res["group_off"], np.concatenate([[0], np.cumsum(N["recv_per_expert"])]))
+    # float64 MoE without quantisation: agreement within the INT8 noise
+    xf = x.float().numpy().astype(np.float64)
+    ref = np.zeros_like(xf)
+    for t in range(R * bs):
+        for kk in range(k):
+            e = idx[t, kk]
+            v = (w1[e].astype(np.float64) * ws1[e][:, None]) @ xf[t]
+            h = v[:I] / (1 + np.exp(-v[:I])) * v[I:]
+            y = (w2[e].astype(np.float64) * ws2[e][:, None]) @ h
+            ref[t] += wt[t, kk] * y
+    got = oracle.to_f32(res["out"], 0).astype(np.float64)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel < 0.03, rel
+    # listed tokens give the same rows
+    toks = np.array([3, 0, R * bs - 1], np.int64)
+    sub = oracle.deep_moe(W.bits(x), idx, wt, R, epr, 0, w1, ws1, w2, ws2, tokens=toks)
+    np.testing.assert_array_equal(sub["out"], res["out"][toks])
+
+
 ALL_CHECKS = [
     check_handworked_layout_notify, check_layout_brute_force,
     check_layout_invariants, check_notify_closed_form, check_rows_closed_form,
@@ -540,6 +665,7 @@ ALL_CHECKS = [
     check_quant_zero_row, check_conversions, check_combine_special_cases,
     check_combine_one_hot_and_bound, check_combine_k1, check_dispatch_capacity,
     check_combine_quant, check_token_layout, check_exp, check_swiglu_quant,
+    check_grouped_gemm, check_deq_combine, check_deep_moe,
 ]
 
 
@@ -590,6 +716,13 @@ MUTANTS = {
     "swiglu_sigmoid_not_silu": ("const float sg = gate / d;", "const float sg = 1.0f / d;"),
     "exp_sign_error": ("const float e = exp_cw(-gate);", "const float e = exp_cw(gate);"),
     "exp_low_part_dropped": ("r = fmaf(-n, -2.12194440e-4f, r);", "r = fmaf(-n, 0.0f, r);"),
+    "gemm_always_group_zero": ("b + ((int64_t)g * N + n) * K;", "b + ((int64_t)0 * N + n) * K;"),
+    "gemm_listed_rows_by_global_index": ("a + (rows ? i : m) * lda;", "a + m * lda;"),
+    "deq_combine_scale_of_expert_zero": ("weight_scale + (int64_t)e * H;",
+                                         "weight_scale + (int64_t)0 * H;"),
+    "deq_combine_no_row_scale": ("        y = y * ts;\n", "        y = y * 1.0f;\n"),
+    "deq_combine_fused_multiply_add": ("acc[h] = acc[h] + prod;",
+                                       "acc[h] = fmaf(y, w, acc[h]);", 2),
     "exp_horner_coefficient_order": ("p = fmaf(p, r, 4.16666667e-2f);", "p = fmaf(p, r, 8.33333333e-3f);"),
 }
 

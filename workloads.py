@@ -190,6 +190,23 @@ def gmm1_accumulators(M: int, I: int, seed: int = 99):
     return acc, ws.to(torch.float32), ts.to(torch.float32)
 
 
+def moe_weights(E: int, H: int, I: int, seed: int = 7, device="cpu"):
+    """Synthetic INT8 expert weights for the fused deep MoE: w1 int8
+    [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up; row n = output column n),
+    w2 int8 [E, H, I], codes uniform in [-127, 127]; per-output-column
+    weight scales ws1 [E, 2I] and ws2 [E, H] ~ U(0.5, 1.5) * 1e-4 (fp32).
+    Drawn with a generator on ``device`` (CPU and CUDA streams differ)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 16 + 8)
+    w1 = torch.randint(-127, 128, (E, 2 * I, H), generator=g, dtype=torch.int8,
+                       device=device)
+    w2 = torch.randint(-127, 128, (E, H, I), generator=g, dtype=torch.int8,
+                       device=device)
+    ws1 = (torch.rand((E, 2 * I), generator=g, device=device) + 0.5) * 1e-4
+    ws2 = (torch.rand((E, H), generator=g, device=device) + 0.5) * 1e-4
+    return w1, ws1.float(), w2, ws2.float()
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     """uint16 bit patterns of a bf16/fp16 CPU tensor (no copy)."""
     assert t.dtype in (torch.bfloat16, torch.float16)
