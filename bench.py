@@ -90,6 +90,18 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_tflops():
+    """(burst, sustained) dense bf16 TFLOP/s from MEASURED_PEAKS.json, else
+    the fallback figures."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, 1700.0, "fallback"
+
+
 def _file_hash(rel):
     with open(os.path.join(ROOT, rel), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -386,6 +398,12 @@ def run_gpu(args, w):
     tl_us = float(np.mean([a.elapsed_time(c) for a, c in tl_ev])) * 1e3
     del tpr, inr
 
+    # ---- fused deep MoE (dispatch -> GMM1 -> DeqSwigluQuant -> GMM2 ->
+    #      DeqCombine) on the same routing and tokens ------------------------
+    deep = None
+    if w.quant and w.E <= 256 and not args.no_deep_moe:   # weights: E x 44 M codes
+        deep = run_deep_moe_bench(args, w, ep, pl, x, idx, wt, stream, dev, flush)
+
     # ---- end to end through the public API with host buffers --------------
     e2e = run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush)
     e2e_max_ms = reduce_max(e2e["ms_per_step"], world, dev)
@@ -441,6 +459,7 @@ def run_gpu(args, w):
         "token_layout_us": tl_us,
         "graph_step_us": graph_us,
         "swiglu_quant": sw,
+        "deep_moe": deep,
         "dispatch_fused": {"us": fused_us, "separate_us": separate_us,
                            "note": "layout+notify+dispatch in one cooperative "
                                    "launch vs three launches"},
@@ -461,6 +480,89 @@ def run_gpu(args, w):
         "cpu_baseline": cpu,
     }
     return rec
+
+
+def run_deep_moe_bench(args, w, ep, pl, x, idx, wt, stream, dev, flush):
+    """Times the deep MoE pipeline stage by stage (CUDA events on the
+    stream) with synthetic INT8 expert weights drawn on the device; the two
+    grouped GEMMs are reported against the dense bf16 tensor peak."""
+    I = SWIGLU_INTERMEDIATE
+    w1, ws1, w2, ws2 = W.moe_weights(w.E, w.H, I, seed=31, device=dev)
+    wts = pl.DeepMoeWeights(w1, ws1 * 40.0, w2, ws2 * 40.0, stream)
+    torch.cuda.synchronize()
+    del w1, w2
+    b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype, device=dev)
+    P, H = w.P, w.H
+    names = ["layout+notify", "dispatch", "offsets+a1_bf16", "gemm1", "swiglu_quant",
+             "a2_bf16", "gemm2", "deq_combine"]
+
+    def step(evs=None):
+        def mark(j):
+            if evs:
+                evs[j].record(stream)
+        mark(0)
+        pl.run_layout_notify(b, idx, stream)
+        mark(1)
+        pl.run_dispatch(b, x, idx, stream)
+        mark(2)
+        ep.moe_group_offsets(b.recv_per_expert, b.group_off, b.dev_status, stream)
+        ep.moe_codes_to_bf16(b.recv, P, b.row_bytes, H, b.a1, stream)
+        mark(3)
+        ep.moe_grouped_gemm_i8(b.a1, wts.w1, b.recv_per_expert, b.acc1, b.dev_status,
+                               stream)
+        mark(4)
+        ep.moe_swiglu_quant_grouped(b.acc1, wts.ws1, b.group_off,
+                                    (b.recv, (H + 31) // 32 * 32, b.row_bytes), b.x2,
+                                    b.dev_status, stream)
+        mark(5)
+        ep.moe_codes_to_bf16(b.x2, P, b.row2, I, b.a2, stream)
+        mark(6)
+        ep.moe_grouped_gemm_i8(b.a2, wts.w2, b.recv_per_expert, b.acc2, b.dev_status,
+                               stream)
+        mark(7)
+        pl.run_deq_combine(b, wts, idx, wt, stream)
+        mark(8)
+
+    for i in range(3):
+        step()
+    torch.cuda.synchronize()
+    if b.status() != 0:
+        raise RuntimeError("device status %d in the deep MoE" % b.status())
+    n = max(3, min(args.steps, 10))
+    all_evs = []
+    for i in range(n):
+        flush.fill_(i & 0xff)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(9)]
+        step(evs)
+        all_evs.append(evs)
+    torch.cuda.synchronize()
+    if b.status() != 0:
+        raise RuntimeError("device status %d in the deep MoE" % b.status())
+    st_ms = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(8)] for e in all_evs])
+    mean = st_ms.mean(axis=0)
+    burst, sustained, src = measured_bf16_tflops()
+    flops1 = 2.0 * P * H * 2 * I
+    flops2 = 2.0 * P * I * H
+
+    def gemm(flops, ms):
+        tf = flops / (ms * 1e-3) / 1e12
+        return {"us": ms * 1e3, "flops": flops, "achieved": tf, "unit": "TFLOP/s",
+                "bound": "tensor", "peak": sustained, "frac": tf / sustained,
+                "frac_of_burst": tf / burst, "peak_source": src,
+                "note": "bf16 tensor-core MMA on int8-valued operands (exact int32)"}
+    res = {
+        "config": {"rows": P, "H": H, "I": I, "experts": w.E,
+                   "weights": "synthetic int8 codes U[-127,127], bf16 copies resident"},
+        "step_ms": float(mean.sum()),
+        "tokens_per_s": w.T / (mean.sum() * 1e-3),
+        "stages_us": {nm: float(mean[j] * 1e3) for j, nm in enumerate(names)},
+        "gemm1": gemm(flops1, float(mean[3])),
+        "gemm2": gemm(flops2, float(mean[6])),
+        "steps": n,
+    }
+    del b, wts
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush):
@@ -635,6 +737,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=30)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-deep-moe", action="store_true",
+                   help="skip the fused deep MoE section")
     p.add_argument("--ref-tokens", type=int, default=32)
     p.add_argument("--bs", type=int, default=None,
                    help="override tokens per rank (small profiling cases)")

@@ -70,9 +70,21 @@ def _load():
     L.moe_fused_workspace_bytes.argtypes = [sp]
     L.moe_fused_workspace_bytes.restype = ctypes.c_size_t
     L.moe_dispatch_fused.argtypes = [sp, vp, vp, ctypes.c_int] + [vp] * 9 + [i64, vp, vp, vp]
+    L.moe_group_offsets.argtypes = [vp, ctypes.c_int32, vp, vp, vp]
+    L.moe_codes_to_bf16.argtypes = [vp, i64, i64, ctypes.c_int32, vp, vp]
+    L.moe_gmm_block_n.argtypes = []
+    L.moe_gmm_block_n.restype = ctypes.c_int32
+    L.moe_grouped_gemm_i8.argtypes = [vp, i64, ctypes.c_int32, vp, ctypes.c_int32,
+                                      ctypes.c_int32, vp, vp, vp, vp]
+    L.moe_swiglu_quant_grouped.argtypes = [vp, i64, ctypes.c_int32, vp, vp,
+                                           ctypes.c_int32, vp, i64, vp, vp, vp]
+    L.moe_deq_combine.argtypes = [sp, vp, i64, vp, vp, i64, vp, vp, vp, vp, vp,
+                                  vp, vp, vp]
     for name in ("moe_dispatch_layout", "moe_notify_dispatch", "moe_dispatch",
                  "moe_combine", "moe_combine_quant", "moe_token_layout",
-                 "moe_dispatch_fused", "moe_swiglu_quant"):
+                 "moe_dispatch_fused", "moe_swiglu_quant", "moe_group_offsets",
+                 "moe_codes_to_bf16", "moe_grouped_gemm_i8",
+                 "moe_swiglu_quant_grouped", "moe_deq_combine"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -298,3 +310,107 @@ def moe_swiglu_quant(acc, weight_scale, token_scale, out, dev_status,
         _ptr(out, None, None, "out"),
         _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
     return _check(st, "moe_swiglu_quant")
+
+
+# ---- fused deep MoE ---------------------------------------------------------
+
+def _strided(src, rows, name):
+    """(tensor, byte_offset, byte_stride) -> pointer to the fp32 at
+    offset + r * stride for r < rows, checked against the tensor's bytes."""
+    t, off, stride = src
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous CUDA tensor" % name)
+    nbytes = t.numel() * t.element_size()
+    if off < 0 or stride < 4 or (rows > 0 and off + (rows - 1) * stride + 4 > nbytes):
+        raise ValueError("%s: rows reach past the tensor" % name)
+    return ctypes.c_void_p(t.data_ptr() + int(off)), int(stride)
+
+
+def gmm_block_n():
+    """Output-column tile of moe_grouped_gemm_i8."""
+    return int(_lib.moe_gmm_block_n())
+
+
+def moe_group_offsets(group_rows, group_off, dev_status, stream=None):
+    """group_off int64 [G+1] = exclusive prefix of group_rows int32 [G]."""
+    G = group_rows.numel()
+    st = _lib.moe_group_offsets(
+        _ptr(group_rows, torch.int32, G, "group_rows"), int(G),
+        _ptr(group_off, torch.int64, G + 1, "group_off"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_group_offsets")
+
+
+def moe_codes_to_bf16(codes, rows, row_stride, K, out, stream=None):
+    """INT8 codes at byte 0 of rows ``row_stride`` bytes apart -> bf16
+    out [rows, K] (exact)."""
+    if codes.numel() * codes.element_size() < rows * row_stride:
+        raise ValueError("codes is smaller than rows x row_stride bytes")
+    st = _lib.moe_codes_to_bf16(
+        _ptr(codes, (torch.uint8, torch.int8), None, "codes"), int(rows),
+        int(row_stride), int(K), _ptr(out, torch.bfloat16, rows * K, "out"),
+        _stream(stream))
+    return _check(st, "moe_codes_to_bf16")
+
+
+def moe_grouped_gemm_i8(a, w, group_rows, c, dev_status, stream=None):
+    """c [a_rows, N] int32 = per-group a [a_rows, K] x w[g] [N, K]^T on the
+    tensor cores (int8 values held as bf16; exact)."""
+    if a.dim() != 2 or w.dim() != 3 or w.shape[2] != a.shape[1]:
+        raise ValueError("a must be [rows, K] and w [G, N, K]")
+    rows, K = a.shape
+    G, N = w.shape[0], w.shape[1]
+    if group_rows.numel() != G:
+        raise ValueError("group_rows must have G entries")
+    st = _lib.moe_grouped_gemm_i8(
+        _ptr(a, torch.bfloat16, rows * K, "a"), int(rows), int(K),
+        _ptr(w, torch.bfloat16, G * N * K, "w"), int(G), int(N),
+        _ptr(group_rows, torch.int32, G, "group_rows"),
+        _ptr(c, torch.int32, rows * N, "c"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_grouped_gemm_i8")
+
+
+def moe_swiglu_quant_grouped(acc, weight_scale, group_off, token_scale, out,
+                             dev_status, stream=None):
+    """GMM1 epilogue with per-expert weight scales [G, 2I]; token_scale is
+    (tensor, byte_offset, byte_stride) of each row's fp32 scale."""
+    if acc.dim() != 2 or acc.shape[1] % 2 or weight_scale.dim() != 2:
+        raise ValueError("acc must be [M, 2I] and weight_scale [G, 2I]")
+    M, I = acc.shape[0], acc.shape[1] // 2
+    G = weight_scale.shape[0]
+    if weight_scale.shape[1] != 2 * I or group_off.numel() != G + 1:
+        raise ValueError("weight_scale / group_off do not match acc")
+    rb = (I + 31) // 32 * 32 + 32
+    if out.numel() * out.element_size() < M * rb:
+        raise ValueError("out is smaller than M rows")
+    tp, tstride = _strided(token_scale, M, "token_scale")
+    st = _lib.moe_swiglu_quant_grouped(
+        _ptr(acc, torch.int32, M * 2 * I, "acc"), int(M), int(I),
+        _ptr(weight_scale, torch.float32, G * 2 * I, "weight_scale"),
+        _ptr(group_off, torch.int64, G + 1, "group_off"), int(G), tp, tstride,
+        _ptr(out, None, None, "out"), _ptr(dev_status, torch.int32, 1, "dev_status"),
+        _stream(stream))
+    return _check(st, "moe_swiglu_quant_grouped")
+
+
+def moe_deq_combine(shape, expert_acc, weight_scale, row_scale, topk_idx,
+                    topk_weights, send_idx, put_offset, rank_recv_base, out,
+                    dev_status, stream=None):
+    """DeqCombine over int32 expert outputs [rows, H]; row_scale is
+    (tensor, byte_offset, byte_stride) of each row's fp32 scale."""
+    T, k, H = shape.R * shape.bs, shape.k, shape.H
+    E = shape.R * shape.experts_per_rank
+    rows = expert_acc.shape[0]
+    rp, rstride = _strided(row_scale, rows, "row_scale")
+    st = _lib.moe_deq_combine(
+        ctypes.byref(shape), _ptr(expert_acc, torch.int32, rows * H, "expert_acc"),
+        int(rows), _ptr(weight_scale, torch.float32, E * H, "weight_scale"), rp,
+        rstride, _ptr(topk_idx, torch.int32, T * k, "topk_idx"),
+        _ptr(topk_weights, torch.float32, T * k, "topk_weights"),
+        _ptr(send_idx, torch.int32, T * k, "send_idx"),
+        _ptr(put_offset, torch.int32, E * shape.R, "put_offset"),
+        _ptr(rank_recv_base, torch.int64, shape.R + 1, "rank_recv_base"),
+        _ptr(out, None, T * H, "out"), _ptr(dev_status, torch.int32, 1, "dev_status"),
+        _stream(stream))
+    return _check(st, "moe_deq_combine")

@@ -2,6 +2,7 @@
 // include/moe_ep.h): argument validation, then one launch per stage.
 // Every check here is a host-side check; nothing touches the GPU before the
 // arguments have been accepted.
+#include <climits>
 #include <cstdint>
 
 #include "moe_ep_internal.cuh"
@@ -231,6 +232,90 @@ moe_status moe_combine_quant(const moe_shape* shape, const void* expert_out_q,
   return from_cuda(moe_ep::launch_combine_quant(
       s, expert_out_q, expert_out_rows, topk_idx, topk_weights, send_idx, put_offset,
       rank_recv_base, out, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_swiglu_quant_grouped(const int32_t* acc, int64_t M, int32_t I,
+                                    const float* weight_scale, const int64_t* group_off,
+                                    int32_t G, const void* token_scale,
+                                    int64_t token_scale_stride, void* out,
+                                    int32_t* dev_status, void* stream) {
+  if (M < 0 || I < 8 || I > 16384 || I % 8 != 0 || G < 1 || G > MOE_EP_MAX_EXPERTS ||
+      token_scale_stride < 4 || token_scale_stride % 4 != 0 || !dev_status)
+    return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  if (!acc || !weight_scale || !group_off || !token_scale || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(acc, 16) || !aligned(weight_scale, 16) || !aligned(group_off, 8) ||
+      !aligned(token_scale, 4) || !aligned(out, 16) || !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_swiglu_quant_grouped(
+      acc, M, I, weight_scale, group_off, G, token_scale, token_scale_stride, out,
+      static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_codes_to_bf16(const void* codes, int64_t rows, int64_t row_stride, int32_t K,
+                             void* out, void* stream) {
+  if (rows < 0 || K < 8 || K > MOE_EP_MAX_HIDDEN || K % 8 != 0 || row_stride < K ||
+      row_stride % 8 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!codes || !out || !aligned(codes, 8) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_codes_to_bf16(codes, rows, row_stride, K, out,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+int32_t moe_gmm_block_n(void) { return moe_ep::gmm_block_n(); }
+
+moe_status moe_grouped_gemm_i8(const void* a, int64_t a_rows, int32_t K, const void* w,
+                               int32_t G, int32_t N, const int32_t* group_rows, int32_t* c,
+                               int32_t* dev_status, void* stream) {
+  const int64_t bn = moe_ep::gmm_block_n();
+  if (a_rows < 1 || a_rows > INT32_MAX || K < 8 || K > MOE_EP_MAX_HIDDEN || K % 8 != 0 ||
+      G < 1 || G > MOE_EP_MAX_EXPERTS || N < 8 || N > MOE_EP_MAX_HIDDEN || N % 8 != 0 ||
+      !dev_status)
+    return MOE_ERR_INVALID_ARG;
+  if ((a_rows / 128 + G) * ((N + bn - 1) / bn) > INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if (!a || !w || !group_rows || !c) return MOE_ERR_INVALID_ARG;
+  if (!aligned(a, 16) || !aligned(w, 16) || !aligned(group_rows, 4) || !aligned(c, 16) ||
+      !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_grouped_gemm(a, a_rows, K, w, G, N, group_rows, c,
+                                               dev_status,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_group_offsets(const int32_t* group_rows, int32_t G, int64_t* group_off,
+                             int32_t* dev_status, void* stream) {
+  if (G < 1 || G > MOE_EP_MAX_EXPERTS || !group_rows || !group_off || !dev_status ||
+      !aligned(group_rows, 4) || !aligned(group_off, 8) || !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_group_offsets(group_rows, G, group_off, dev_status,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_deq_combine(const moe_shape* shape, const int32_t* expert_acc,
+                           int64_t expert_rows, const float* weight_scale,
+                           const void* row_scale, int64_t row_scale_stride,
+                           const int32_t* topk_idx, const float* topk_weights,
+                           const int32_t* send_idx, const int32_t* put_offset,
+                           const int64_t* rank_recv_base, void* out, int32_t* dev_status,
+                           void* stream) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return MOE_ERR_INVALID_ARG;
+  if (expert_rows < 0 || row_scale_stride < 4 || row_scale_stride % 4 != 0 || !dev_status)
+    return MOE_ERR_INVALID_ARG;
+  if (s.T() == 0) return MOE_OK;
+  if ((expert_rows > 0 && (!expert_acc || !row_scale)) || !weight_scale || !topk_idx ||
+      !topk_weights || !send_idx || !put_offset || !rank_recv_base || !out)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(expert_acc, 16) || !aligned(weight_scale, 16) || !aligned(row_scale, 4) ||
+      !aligned(out, 16) || !aligned(topk_idx, 4) || !aligned(topk_weights, 4) ||
+      !aligned(send_idx, 4) || !aligned(put_offset, 4) || !aligned(rank_recv_base, 8) ||
+      !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_deq_combine(
+      s, expert_acc, expert_rows, weight_scale, row_scale, row_scale_stride, topk_idx,
+      topk_weights, send_idx, put_offset, rank_recv_base, out, dev_status,
+      static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -109,7 +109,7 @@ fused_dispatch_kernel(Params p) {
 
   // ---- A: layout tiles -------------------------------------------------------
   for (int tile = blockIdx.x; tile < p.num_tiles; tile += G) {
-    for (int i = tid; i < kWarps * E / 2; i += kThreads)
+    for (int i = tid; i < (kWarps * E + 1) / 2; i += kThreads)
       reinterpret_cast<uint32_t*>(wcnt)[i] = 0u;
     __syncthreads();
     const int s = tile / p.tiles_per_rank;

@@ -1,0 +1,468 @@
+// gmm.cu -- grouped GEMM of the fused deep MoE (UMDK/CAM deep analysis v2,
+// sections 4.1 and 4.3: GMM1 and GMM2, "INT8 x INT8 -> INT32", one weight
+// matrix per expert, each expert's rows contiguous in the receive buffer).
+//
+// sm_103a has no INT8 tensor-core MMA (tcgen05 .kind::i8 is not available on
+// this target), so the products run on the bf16 tensor path and stay exact:
+//   * an int8 code is exact in bf16, and a product of two codes (|p| <= 2^14)
+//     is exact in the fp32 accumulator;
+//   * K is split into chunks of 1024: a chunk's partial sums are integers of
+//     magnitude <= 1024 * 128 * 128 = 2^24, all exactly representable in fp32,
+//     so every accumulation step inside a chunk is exact;
+//   * the epilogue converts each chunk's fp32 sums to int32 (exact) and adds
+//     the chunks in int32.
+// The result is the int32 GEMM bit for bit.
+//
+// Kernel: persistent CTAs (one per SM) walk 128 x 128 output tiles (the last
+// column tile may be ragged: its B rows past the expert are computed from
+// the next expert's rows, or zero-filled by TMA, and never stored; tiles of
+// one expert together, m fastest, so the expert's weights and rows are
+// reused from L2).  Warp 0 streams 128 x 64 bf16 tiles of A and B into a
+// 4-stage shared-memory ring with TMA (cp.async.bulk.tensor, 128-byte
+// swizzle); warp 1 allocates 256 TMEM columns and one elected lane issues
+// tcgen05.mma (M = 128, N = 128, K = 16, fp32 accumulate) into one of two
+// 128-column accumulators, alternating per K chunk; warps 2-5 drain a
+// finished chunk accumulator (tcgen05.ld, one TMEM lane = one output row per
+// thread) into int32 registers while the next chunk accumulates, then store
+// the tile's rows.  Every mbarrier wait is bounded: a timeout sets
+// MOE_ERR_TIMEOUT and the CTA stops issuing work.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "moe_ep_internal.cuh"
+
+namespace moe_ep {
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64;   // BK bf16 = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kChunkBlocks = 16;             // 16 x 64 = 1024: exact fp32 partial sums
+constexpr uint32_t kTmemCols = 2 * BN;       // two chunk accumulators
+constexpr int kThreads = 192;                // TMA warp, MMA warp, 4 epilogue warps
+constexpr uint32_t kTileABytes = BM * BK * 2;
+constexpr uint32_t kTileBBytes = BN * BK * 2;
+constexpr uint32_t kSpin = 1u << 20;         // polls per wait (about a second at the least)
+
+// Dynamic shared memory, from a 1024-byte aligned base.
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kTileABytes;
+constexpr uint32_t kOffBar = kOffB + kStages * kTileBBytes;
+constexpr uint32_t kOffTables = kOffBar + 256;
+size_t smem_bytes(int G) {
+  return 1024 + kOffTables + size_t(G + 1) * (sizeof(int64_t) + sizeof(int32_t));
+}
+
+// ---- tcgen05 / TMA wrappers ---------------------------------------------------
+
+__device__ __forceinline__ void tma_load_2d(uint32_t sdst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(sdst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major tile, rows of 128 bytes with the
+// 128-byte swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= uint64_t(1) << 16;                           // leading offset (unused when swizzled)
+  d |= uint64_t(1024 >> 4) << 32;                   // stride offset: 8 rows x 128 B
+  d |= uint64_t(1) << 46;                           // descriptor version
+  d |= uint64_t(2) << 61;                           // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on `bar` once every tcgen05.mma issued so far by this thread is done.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// 16 consecutive TMEM columns of this warp's 32 lanes (one row per thread).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+      " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---- tile bookkeeping ------------------------------------------------------------
+
+// Rows of group g (a negative count is reported and read as 0).
+__device__ __forceinline__ int64_t group_count(const int32_t* group_rows, int g,
+                                               int32_t* dev_status) {
+  const int32_t c = __ldg(group_rows + g);
+  if (c < 0 && dev_status) set_status(dev_status, MOE_ERR_INVALID_ARG);
+  return c < 0 ? 0 : c;
+}
+
+struct Tile {
+  int g;          // group (expert)
+  int64_t row0;   // first A row of the tile
+  int64_t rows;   // valid rows (<= BM)
+  int n0;         // first output column
+};
+
+__device__ __forceinline__ Tile decode_tile(int64_t t, const int64_t* goff,
+                                            const int32_t* tpre, int G, int ntn) {
+  int lo = 0, hi = G;                 // largest g with tpre[g] <= t
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tpre[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int g = lo;
+  const int64_t cnt = goff[g + 1] - goff[g];
+  const int mt = static_cast<int>((cnt + BM - 1) / BM);
+  const int local = static_cast<int>(t - tpre[g]);
+  const int m = local % mt, n = local / mt;
+  Tile tl;
+  tl.g = g;
+  tl.row0 = goff[g] + int64_t(m) * BM;
+  const int64_t left = cnt - int64_t(m) * BM;
+  tl.rows = left < BM ? left : BM;
+  tl.n0 = n * BN;
+  return tl;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                    const __grid_constant__ CUtensorMap tmB,
+                    const int32_t* __restrict__ group_rows, int G, int64_t a_rows, int K,
+                    int N, int32_t* __restrict__ C, int32_t* dev_status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+  int64_t* goff = reinterpret_cast<int64_t*>(smem + kOffTables);
+  int32_t* tpre = reinterpret_cast<int32_t*>(goff + G + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntn = (N + BN - 1) / BN;
+
+  // ---- group tables: row offsets and tile prefix (block scan over G) ----------
+  {
+    const int per = (G + kThreads - 1) / kThreads;
+    const int g0 = tid * per < G ? tid * per : G, g1 = g0 + per < G ? g0 + per : G;
+    int64_t rsum = 0;
+    int32_t tsum = 0;
+    for (int g = g0; g < g1; ++g) {
+      const int64_t c = group_count(group_rows, g, dev_status);
+      rsum += c;
+      tsum += static_cast<int32_t>((c + BM - 1) / BM) * ntn;
+    }
+    __shared__ int64_t s_r[kThreads];
+    __shared__ int32_t s_t[kThreads];
+    s_r[tid] = rsum;
+    s_t[tid] = tsum;
+    __syncthreads();
+    if (tid == 0) {
+      int64_t r = 0;
+      int32_t tt = 0;
+      for (int i = 0; i < kThreads; ++i) {
+        const int64_t a = s_r[i];
+        const int32_t b = s_t[i];
+        s_r[i] = r;
+        s_t[i] = tt;
+        r += a;
+        tt += b;
+      }
+      goff[G] = r;
+      tpre[G] = tt;
+    }
+    __syncthreads();
+    int64_t r = s_r[tid];
+    int32_t tt = s_t[tid];
+    for (int g = g0; g < g1; ++g) {
+      goff[g] = r;
+      tpre[g] = tt;
+      const int64_t c = group_count(group_rows, g, nullptr);
+      r += c;
+      tt += static_cast<int32_t>((c + BM - 1) / BM) * ntn;
+    }
+  }
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull + b, 1);
+      mbar_init(tempty + b, 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {   // TMEM: 256 columns for this CTA (one CTA per SM)
+    __syncwarp();
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem = *tmem_slot;
+  const int64_t total_rows = goff[G];
+  const int64_t tiles = tpre[G];
+  const int nkb = (K + BK - 1) / BK;
+  const int nchunks = (nkb + kChunkBlocks - 1) / kChunkBlocks;
+  if (total_rows > a_rows) {              // more rows than the A buffer holds
+    if (tid == 0) set_status(dev_status, MOE_ERR_CAPACITY);
+  } else if (warp == 0) {
+    // ---- TMA producer ---------------------------------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int64_t t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+        const Tile tl = decode_tile(t, goff, tpre, G, ntn);
+        const int brow = tl.g * N + tl.n0;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_bounded(empty + stage, phase ^ 1u, kSpin)) {
+            set_status(dev_status, MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(full + stage, kTileABytes + kTileBBytes);
+          tma_load_2d(smem_addr(smem + kOffA + stage * kTileABytes), &tmA, kb * BK,
+                      static_cast<int>(tl.row0), full + stage);
+          tma_load_2d(smem_addr(smem + kOffB + stage * kTileBBytes), &tmB, kb * BK, brow,
+                      full + stage);
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // every stage's last MMA read has completed before the CTA retires
+      for (int s = 0; s < kStages && !*abort_flag; ++s) {
+        if (!mbar_wait_bounded(empty + stage, phase ^ 1u, kSpin)) {
+          set_status(dev_status, MOE_ERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer -----------------------------------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, chunk_ctr = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+        for (int c = 0; ok && c < nchunks; ++c, ++chunk_ctr) {
+          const uint32_t b = chunk_ctr & 1u, use = (chunk_ctr >> 1) & 1u;
+          if (!mbar_wait_bounded(tempty + b, use ^ 1u, kSpin) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + b * BN;
+          const int kb1 = (c + 1) * kChunkBlocks < nkb ? (c + 1) * kChunkBlocks : nkb;
+          for (int kb = c * kChunkBlocks; kb < kb1; ++kb) {
+            if (!mbar_wait_bounded(full + stage, phase, kSpin) || *abort_flag) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad = sdesc(smem_addr(smem + kOffA + stage * kTileABytes));
+            const uint64_t bd = sdesc(smem_addr(smem + kOffB + stage * kTileBBytes));
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)   // +32 bytes along K per step
+              mma_bf16(d, ad + 2 * kk, bd + 2 * kk,
+                       (kb != c * kChunkBlocks || kk != 0) ? 1u : 0u);
+            mma_commit(empty + stage);             // frees the stage when read
+            if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          }
+          mma_commit(tfull + b);                   // the chunk's sums are final
+        }
+      }
+      if (!ok) {
+        set_status(dev_status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+  } else {
+    // ---- epilogue: chunk sums -> int32, tile rows -> C -------------------------
+    const int q = warp & 3;                  // TMEM lanes 32q .. 32q+31
+    uint32_t chunk_ctr = 0;
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const Tile tl = decode_tile(t, goff, tpre, G, ntn);
+      int32_t acc[BN];
+#pragma unroll
+      for (int j = 0; j < BN; ++j) acc[j] = 0;
+      bool ok = true;
+      for (int c = 0; c < nchunks; ++c, ++chunk_ctr) {
+        const uint32_t b = chunk_ctr & 1u, use = (chunk_ctr >> 1) & 1u;
+        const bool got = mbar_wait_bounded(tfull + b, use, kSpin) && !*abort_flag;
+        if (!__all_sync(0xffffffffu, got)) {   // the warp stays converged
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int cb = 0; cb < BN / 16; ++cb) {
+          uint32_t v[16];
+          tmem_ld16(tmem + (uint32_t(q * 32) << 16) + b * BN + cb * 16, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[cb * 16 + j] += __float2int_rn(__uint_as_float(v[j]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty + b);
+      }
+      if (!ok) {
+        if (lane == 0) set_status(dev_status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      const int r = q * 32 + lane;
+      if (r < tl.rows) {
+        int4* dst = reinterpret_cast<int4*>(C + (tl.row0 + r) * int64_t(N) + tl.n0);
+        const int ncols = N - tl.n0;         // a ragged last column tile
+#pragma unroll
+        for (int j = 0; j < BN / 4; ++j)
+          if (4 * j < ncols)
+            dst[j] = make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---- int8 codes -> bf16 ------------------------------------------------------------
+
+__global__ void codes_to_bf16_kernel(const uint8_t* __restrict__ src, int64_t rows,
+                                     int64_t stride, int K, uint16_t* __restrict__ dst) {
+  const int per_row = K / 8;                       // 8 codes -> 16 bytes of bf16
+  const int64_t n = rows * per_row;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / per_row;
+    const int c = static_cast<int>(i - r * per_row);
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src + r * stride + 8 * c));
+    const uint32_t b[2] = {w.x, w.y};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t word = b[j >> 1] >> (16 * (j & 1));
+      const float lo = static_cast<float>(static_cast<int8_t>(word & 0xffu));
+      const float hi = static_cast<float>(static_cast<int8_t>((word >> 8) & 0xffu));
+      o[j] = narrow_rn<MOE_BF16>(lo) | (narrow_rn<MOE_BF16>(hi) << 16);   // exact
+    }
+    reinterpret_cast<uint4*>(dst + r * int64_t(K))[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ---- host: tensor maps -------------------------------------------------------------
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t encode_kmajor(CUtensorMap* map, const void* base, int64_t rows, int K,
+                          uint32_t box_rows) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess) return e;
+  if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
+  const cuuint32_t box[2] = {cuuint32_t(BK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = reinterpret_cast<EncodeTiled>(fn)(
+      map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_codes_to_bf16(const void* src, int64_t rows, int64_t stride, int K,
+                                 void* dst, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t n = rows * (K / 8);
+  const int threads = 256;
+  const int64_t grid = std::min<int64_t>((n + threads - 1) / threads, int64_t(sms) * 8);
+  codes_to_bf16_kernel<<<static_cast<unsigned>(grid), threads, 0, st>>>(
+      static_cast<const uint8_t*>(src), rows, stride, K, static_cast<uint16_t*>(dst));
+  return cudaGetLastError();
+}
+
+int gmm_block_n() { return BN; }
+
+cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void* b, int G,
+                                int N, const int32_t* group_rows, int32_t* c,
+                                int32_t* dev_status, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  cudaError_t e = encode_kmajor(&ma, a, a_rows, K, BM);
+  if (e == cudaSuccess) e = encode_kmajor(&mb, b, int64_t(G) * N, K, BN);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t smem = smem_bytes(G);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  grouped_gemm_kernel<<<sms, kThreads, smem, st>>>(ma, mb, group_rows, G, a_rows, K, N, c,
+                                                    dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe_ep

@@ -115,7 +115,7 @@ layout_kernel(const int32_t* __restrict__ topk_idx, int R, int epr,
       s_epoch = 0u;
     }
   }
-  for (int i = tid; i < kWarps * E / 2; i += kThreads)
+  for (int i = tid; i < (kWarps * E + 1) / 2; i += kThreads)   // odd W*E: the last half word too
     reinterpret_cast<uint32_t*>(wcnt)[i] = 0u;
   __syncthreads();
 

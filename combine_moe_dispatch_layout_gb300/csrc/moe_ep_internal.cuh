@@ -237,6 +237,31 @@ cudaError_t launch_swiglu_quant(const int32_t* acc, int64_t M, int I,
                                 const float* weight_scale, const float* token_scale,
                                 void* out, cudaStream_t st);
 
+cudaError_t launch_swiglu_quant_grouped(const int32_t* acc, int64_t M, int I,
+                                        const float* weight_scale, const int64_t* group_off,
+                                        int G, const void* token_scale,
+                                        int64_t token_scale_stride, void* out,
+                                        cudaStream_t st);
+
+cudaError_t launch_codes_to_bf16(const void* src, int64_t rows, int64_t stride, int K,
+                                 void* dst, cudaStream_t st);
+
+int gmm_block_n();
+
+cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void* b, int G,
+                                int N, const int32_t* group_rows, int32_t* c,
+                                int32_t* dev_status, cudaStream_t st);
+
+cudaError_t launch_group_offsets(const int32_t* counts, int G, int64_t* off,
+                                 int32_t* dev_status, cudaStream_t st);
+
+cudaError_t launch_deq_combine(const Shape& s, const int32_t* acc2, int64_t y_rows,
+                               const float* weight_scale, const void* row_scale,
+                               int64_t row_scale_stride, const int32_t* topk_idx,
+                               const float* weights, const int32_t* send_idx,
+                               const int32_t* put_offset, const int64_t* rank_recv_base,
+                               void* out, int32_t* dev_status, cudaStream_t st);
+
 cudaError_t launch_notify(const Shape& s, const int32_t* count,
                           int32_t* put_offset, int32_t* total_recv,
                           int64_t* rank_recv_base, int32_t* recv_per_expert,

@@ -58,11 +58,23 @@ __device__ __forceinline__ float exp_cody_waite(float x) {
   return __fmul_rn(p, __uint_as_float((__float_as_uint(s) + 127u) << 23));
 }
 
+// Where a row's scales come from.  Plain: one weight-scale vector for all
+// rows, token scales packed fp32.  Grouped (fused deep MoE): row m belongs to
+// the expert g with group_off[g] <= m < group_off[g + 1] and uses
+// weight_scale + g * 2I; its token scale is the fp32 at ts_base + m * ts_stride
+// (e.g. the 1/scale inside the dispatched row image); rows at or past
+// group_off[G] are not written.
+struct ScaleSrc {
+  const float* weight_scale;
+  const int64_t* group_off;   // nullptr: plain
+  int G;
+  const unsigned char* ts_base;
+  int64_t ts_stride;          // bytes
+};
+
 template <int kCpt>
 __global__ void __launch_bounds__(kMaxThreads)
-swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I,
-                    const float* __restrict__ weight_scale,
-                    const float* __restrict__ token_scale,
+swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc sc,
                     unsigned char* __restrict__ out, int64_t row_bytes) {
   __shared__ float s_wmax[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -71,10 +83,23 @@ swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I,
   const int i_align = static_cast<int>(align_up(I, 32));
   const int ntail = static_cast<int>((row_bytes - I) / 8);
   const int inv_word = (i_align - I) / 8;
+  if (sc.group_off) {
+    const int64_t rows = __ldg(sc.group_off + sc.G);
+    if (rows < M) M = rows;
+  }
 
   for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
     const int32_t* row = acc + m * 2 * int64_t(I);
-    const float ts = __ldg(token_scale + m);
+    const float ts = __ldg(reinterpret_cast<const float*>(sc.ts_base + m * sc.ts_stride));
+    const float* weight_scale = sc.weight_scale;
+    if (sc.group_off) {                  // largest g with group_off[g] <= m
+      int lo = 0, hi = sc.G;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(sc.group_off + mid) <= m) lo = mid; else hi = mid;
+      }
+      weight_scale += int64_t(lo) * 2 * I;
+    }
     float h[kCpt][8];
     float amax = 0.0f;
 #pragma unroll
@@ -143,8 +168,8 @@ swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I,
 }
 
 template <int kCpt>
-cudaError_t launch_t(const int32_t* acc, int64_t M, int I, const float* weight_scale,
-                     const float* token_scale, void* out, cudaStream_t st) {
+cudaError_t launch_t(const int32_t* acc, int64_t M, int I, const ScaleSrc& sc, void* out,
+                     cudaStream_t st) {
   const int nch = I / 8;
   const int threads = std::max(32, std::min(kMaxThreads, ((nch + kCpt - 1) / kCpt + 31) / 32 * 32));
   int dev = 0, sms = 0, per_sm = 0;
@@ -155,8 +180,7 @@ cudaError_t launch_t(const int32_t* acc, int64_t M, int I, const float* weight_s
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(M, int64_t(std::max(1, per_sm)) * sms);
   swiglu_quant_kernel<kCpt><<<static_cast<unsigned>(grid), threads, 0, st>>>(
-      acc, M, I, weight_scale, token_scale, static_cast<unsigned char*>(out),
-      align_up(I, 32) + 32);
+      acc, M, I, sc, static_cast<unsigned char*>(out), align_up(I, 32) + 32);
   return cudaGetLastError();
 }
 
@@ -166,10 +190,22 @@ cudaError_t launch_swiglu_quant(const int32_t* acc, int64_t M, int I,
                                 const float* weight_scale, const float* token_scale,
                                 void* out, cudaStream_t st) {
   if (M == 0) return cudaSuccess;
-  const int nch = I / 8;
-  return nch <= 2 * kMaxThreads
-             ? launch_t<2>(acc, M, I, weight_scale, token_scale, out, st)
-             : launch_t<4>(acc, M, I, weight_scale, token_scale, out, st);
+  const ScaleSrc sc{weight_scale, nullptr, 1,
+                    reinterpret_cast<const unsigned char*>(token_scale), 4};
+  return I / 8 <= 2 * kMaxThreads ? launch_t<2>(acc, M, I, sc, out, st)
+                                  : launch_t<4>(acc, M, I, sc, out, st);
+}
+
+cudaError_t launch_swiglu_quant_grouped(const int32_t* acc, int64_t M, int I,
+                                        const float* weight_scale, const int64_t* group_off,
+                                        int G, const void* token_scale,
+                                        int64_t token_scale_stride, void* out,
+                                        cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  const ScaleSrc sc{weight_scale, group_off, G,
+                    static_cast<const unsigned char*>(token_scale), token_scale_stride};
+  return I / 8 <= 2 * kMaxThreads ? launch_t<2>(acc, M, I, sc, out, st)
+                                  : launch_t<4>(acc, M, I, sc, out, st);
 }
 
 }  // namespace moe_ep

@@ -10,9 +10,10 @@ synchronisation is needed between the stages.
 import torch
 
 from . import (fused_workspace_bytes, make_shape, layout_workspace_bytes,
-               moe_combine, moe_combine_quant, moe_dispatch,
-               moe_dispatch_fused, moe_dispatch_layout, moe_notify_dispatch,
-               recv_row_bytes)
+               moe_codes_to_bf16, moe_combine, moe_combine_quant,
+               moe_deq_combine, moe_dispatch, moe_dispatch_fused,
+               moe_dispatch_layout, moe_group_offsets, moe_grouped_gemm_i8,
+               moe_notify_dispatch, moe_swiglu_quant_grouped, recv_row_bytes)
 
 
 class PipelineBuffers:
@@ -98,3 +99,73 @@ def run_pipeline(b, x, topk_idx, topk_weights, y, stream=None):
     run_layout_notify(b, topk_idx, stream)
     run_dispatch(b, x, topk_idx, stream)
     run_combine(b, y, topk_idx, topk_weights, stream)
+
+
+# ---- fused deep MoE: dispatch -> GMM1 -> DeqSwigluQuant -> GMM2 -> DeqCombine
+
+def _align32(n):
+    return (n + 31) // 32 * 32
+
+
+class DeepMoeWeights:
+    """Expert weights for the deep MoE: INT8 codes converted once to bf16
+    (exact) for the tensor-core GEMMs, plus fp32 per-column scales.
+    w1 int8 [E, 2I, H], ws1 [E, 2I], w2 int8 [E, H, I], ws2 [E, H]."""
+
+    def __init__(self, w1, ws1, w2, ws2, stream=None):
+        E, N1, H = w1.shape
+        I = N1 // 2
+        assert w2.shape == (E, H, I)
+        self.E, self.H, self.I = E, H, I
+        self.w1 = torch.empty((E, N1, H), dtype=torch.bfloat16, device=w1.device)
+        self.w2 = torch.empty((E, H, I), dtype=torch.bfloat16, device=w2.device)
+        moe_codes_to_bf16(w1, E * N1, H, H, self.w1, stream)
+        moe_codes_to_bf16(w2, E * H, I, I, self.w2, stream)
+        self.ws1 = ws1.contiguous()
+        self.ws2 = ws2.contiguous()
+
+
+class DeepMoeBuffers(PipelineBuffers):
+    """PipelineBuffers (INT8 dispatch) plus the deep MoE's intermediates,
+    all sized for T*k rows: bf16 GEMM operands, int32 accumulators, the
+    GMM1 epilogue's INT8 row images and the expert row offsets."""
+
+    def __init__(self, R, bs, k, epr, H, I, dtype, device="cuda"):
+        super().__init__(R, bs, k, epr, H, dtype, True, device)
+        P = R * bs * k
+        self.I = I
+        self.group_off = torch.empty((R * epr + 1,), dtype=torch.int64, device=device)
+        self.a1 = torch.empty((P, H), dtype=torch.bfloat16, device=device)
+        self.acc1 = torch.empty((P, 2 * I), dtype=torch.int32, device=device)
+        self.row2 = _align32(I) + 32
+        self.x2 = torch.empty((P, self.row2), dtype=torch.uint8, device=device)
+        self.a2 = torch.empty((P, I), dtype=torch.bfloat16, device=device)
+        self.acc2 = torch.empty((P, H), dtype=torch.int32, device=device)
+
+
+def run_deep_moe_experts(b, wts, stream=None):
+    """From the dispatched INT8 rows in ``b.recv`` to GMM2's int32
+    accumulators ``b.acc2`` (GMM1, DeqSwigluQuant, GMM2)."""
+    P, H, I = b.capacity, b.shape.H, b.I
+    moe_group_offsets(b.recv_per_expert, b.group_off, b.dev_status, stream)
+    moe_codes_to_bf16(b.recv, P, b.row_bytes, H, b.a1, stream)
+    moe_grouped_gemm_i8(b.a1, wts.w1, b.recv_per_expert, b.acc1, b.dev_status, stream)
+    moe_swiglu_quant_grouped(b.acc1, wts.ws1, b.group_off,
+                             (b.recv, _align32(H), b.row_bytes), b.x2, b.dev_status,
+                             stream)
+    moe_codes_to_bf16(b.x2, P, b.row2, I, b.a2, stream)
+    moe_grouped_gemm_i8(b.a2, wts.w2, b.recv_per_expert, b.acc2, b.dev_status, stream)
+
+
+def run_deq_combine(b, wts, topk_idx, topk_weights, stream=None):
+    moe_deq_combine(b.shape, b.acc2, wts.ws2, (b.x2, _align32(b.I), b.row2), topk_idx,
+                    topk_weights, b.send_idx, b.put_offset, b.rank_recv_base, b.out,
+                    b.dev_status, stream)
+
+
+def run_deep_moe(b, wts, x, topk_idx, topk_weights, stream=None):
+    """The whole deep MoE on one stream; the result is ``b.out``."""
+    run_layout_notify(b, topk_idx, stream)
+    run_dispatch(b, x, topk_idx, stream)
+    run_deep_moe_experts(b, wts, stream)
+    run_deq_combine(b, wts, topk_idx, topk_weights, stream)

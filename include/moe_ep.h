@@ -251,7 +251,8 @@ moe_status moe_dispatch_fused(const moe_shape* shape, const void* x,
  * then h is quantised like moe_dispatch's INT8 rows (scale = 127/(max|h| +
  * 1e-12f), round half to even, 1/scale at byte align32(I)).  Each step is
  * one fp32 round-to-nearest operation; exp is Cody-Waite reduction plus a
- * degree-7 Taylor polynomial (deterministic, within 2 ulp of exp).
+ * degree-7 Taylor polynomial whose reduction and Horner steps are fused
+ * multiply-adds (deterministic, within 1 ulp of exp).
  *   acc           int32 [M][2I], 16-byte aligned (gate half, then up half)
  *   weight_scale  fp32 [2I] per column, 16-byte aligned
  *   token_scale   fp32 [M] per row (e.g. the dispatched rows' 1/scale)
@@ -278,6 +279,88 @@ moe_status moe_combine_quant(const moe_shape* shape, const void* expert_out_q,
                              const int32_t* put_offset,
                              const int64_t* rank_recv_base, void* out,
                              int32_t* dev_status, void* stream);
+
+/* ---- fused deep MoE (section 4: dispatch -> GMM1 -> DeqSwigluQuant ->
+ * GMM2 -> DeqCombine, section 4.3's three-stage pipeline) -----------------
+ * On one GPU the stages are separate calls on one stream; expert e's rows
+ * are contiguous in the receive buffer (rows group_off[e] ..
+ * group_off[e+1]-1, group_off = exclusive prefix of recv_per_expert). */
+
+/* group_off[g] = sum of group_rows[0..g-1] (int64 [G+1], the last entry is
+ * the total).  Negative counts are read as 0 and set MOE_ERR_INVALID_ARG in
+ * *dev_status.  1 <= G <= MOE_EP_MAX_EXPERTS.  One launch. */
+moe_status moe_group_offsets(const int32_t* group_rows, int32_t G, int64_t* group_off,
+                             int32_t* dev_status, void* stream);
+
+/* INT8 codes -> bf16 (exact): out[r][j] = (bf16) codes[r * row_stride + j]
+ * for j < K.  Feeds moe_grouped_gemm_i8 with the dispatched rows (row_stride
+ * = moe_recv_row_bytes(shape, 1)), GMM1-epilogue rows (align32(I) + 32) or
+ * INT8 weights (row_stride = K).
+ *   codes  rows x row_stride bytes, 8-byte aligned, row_stride % 8 == 0
+ *   out    bf16 [rows][K], 16-byte aligned
+ * 8 <= K <= MOE_EP_MAX_HIDDEN, K % 8 == 0.  One launch. */
+moe_status moe_codes_to_bf16(const void* codes, int64_t rows, int64_t row_stride, int32_t K,
+                             void* out, void* stream);
+
+/* Output-column tile of moe_grouped_gemm_i8. */
+int32_t moe_gmm_block_n(void);
+
+/* Grouped INT8 GEMM (section 4.3, GMM1 / GMM2: INT8 x INT8 -> INT32) on the
+ * tensor cores.  Group g (an expert) owns the group_rows[g] consecutive rows
+ * of a that follow the rows of groups 0..g-1, and weight matrix w[g]:
+ *   c[m][n] = sum_{j<K} a[m][j] * w[g][n][j]        (exact int32)
+ * Operands hold int8 values (-128..127) stored as bf16 (moe_codes_to_bf16):
+ * GB300's tensor cores have no INT8 MMA, and with values of this range the
+ * bf16 MMA with fp32 accumulation over K chunks of 1024 is exact, so c is
+ * the integer GEMM bit for bit.
+ *   a           bf16 [a_rows][K], 16-byte aligned; a_rows <= 2^31 - 1
+ *   w           bf16 [G][N][K] (K-major), 16-byte aligned
+ *   group_rows  int32 [G] device (e.g. recv_per_expert of moe_notify_dispatch)
+ *   c           int32 [a_rows][N], 16-byte aligned; rows past the groups'
+ *               total are not written
+ * 8 <= K, N <= MOE_EP_MAX_HIDDEN with K % 8 == 0 and N % 8 == 0;
+ * 1 <= G <= MOE_EP_MAX_EXPERTS.
+ * Data-dependent errors: groups totalling more than a_rows rows ->
+ * MOE_ERR_CAPACITY (nothing written); negative counts -> MOE_ERR_INVALID_ARG;
+ * a pipeline wait that exceeds about a second -> MOE_ERR_TIMEOUT.  One
+ * launch (one CTA per SM). */
+moe_status moe_grouped_gemm_i8(const void* a, int64_t a_rows, int32_t K, const void* w,
+                               int32_t G, int32_t N, const int32_t* group_rows, int32_t* c,
+                               int32_t* dev_status, void* stream);
+
+/* GMM1 epilogue with per-expert weight scales (section 4.3 stage 2,
+ * DeqSwigluQuant): as moe_swiglu_quant, except that row m uses
+ * weight_scale + g*2I for the expert g with group_off[g] <= m <
+ * group_off[g+1], and its token scale is the fp32 at byte
+ * m * token_scale_stride of token_scale (the dispatched row image's 1/scale:
+ * token_scale = recv + align32(H), stride moe_recv_row_bytes(shape, 1)).
+ * Rows at or past group_off[G] are not written.
+ *   weight_scale  fp32 [G][2I], 16-byte aligned
+ *   group_off     int64 [G+1] (moe_group_offsets)
+ * token_scale_stride >= 4 and a multiple of 4.  One launch. */
+moe_status moe_swiglu_quant_grouped(const int32_t* acc, int64_t M, int32_t I,
+                                    const float* weight_scale, const int64_t* group_off,
+                                    int32_t G, const void* token_scale,
+                                    int64_t token_scale_stride, void* out,
+                                    int32_t* dev_status, void* stream);
+
+/* DeqCombine (section 4.3, stage 3): combine over GMM2's int32 outputs.
+ * For token g, slot k (row = its dispatch row, e = its expert):
+ *   y = (fp32(expert_acc[row][h]) * weight_scale[e][h]) * row_scale(row)
+ *   acc = acc + (y * topk_weights[g][k])     (k in order, acc starts at 0)
+ * out[g][h] = acc rounded to nearest even in the token dtype; every step is
+ * one fp32 rounding.  row_scale(row) is the fp32 at byte
+ * row * row_scale_stride of row_scale (the GMM1 epilogue rows' 1/scale).
+ *   expert_acc    int32 [expert_rows][H], 16-byte aligned
+ *   weight_scale  fp32 [E][H], 16-byte aligned
+ *   other arguments as moe_combine.  One launch. */
+moe_status moe_deq_combine(const moe_shape* shape, const int32_t* expert_acc,
+                           int64_t expert_rows, const float* weight_scale,
+                           const void* row_scale, int64_t row_scale_stride,
+                           const int32_t* topk_idx, const float* topk_weights,
+                           const int32_t* send_idx, const int32_t* put_offset,
+                           const int64_t* rank_recv_base, void* out, int32_t* dev_status,
+                           void* stream);
 
 #ifdef __cplusplus
 }

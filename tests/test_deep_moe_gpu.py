@@ -1,0 +1,218 @@
+"""GPU parity of the fused deep MoE path (grouped INT8 GEMM on the tensor
+cores, per-expert GMM1 epilogue, DeqCombine, and the whole pipeline) against
+the CPU oracle, through the C ABI.  Integer results (the GEMMs' int32
+accumulators, INT8 row images) and the bf16 outputs are compared bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ep():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    import combine_moe_dispatch_layout_gb300 as ep
+    return ep
+
+
+@pytest.fixture(scope="module")
+def pl(ep):
+    from combine_moe_dispatch_layout_gb300 import pipeline
+    return pipeline
+
+
+def _eq(name, got, want):
+    g = got.detach().cpu().numpy() if isinstance(got, torch.Tensor) else got
+    g = g.reshape(want.shape)
+    if not np.array_equal(g, want):
+        bad = np.argwhere(g != want)
+        raise AssertionError("%s: %d mismatches, first at %s: got %s want %s"
+                             % (name, len(bad), bad[0].tolist(), g[tuple(bad[0])],
+                                want[tuple(bad[0])]))
+
+
+def _gemm_gpu(ep, a_i8, w_i8, sizes, a_rows=None, fill=-7):
+    """Runs codes_to_bf16 + grouped GEMM; returns (c int32 numpy, status)."""
+    dev = torch.device("cuda")
+    M, K = a_i8.shape
+    G, N, _ = w_i8.shape
+    rows = M if a_rows is None else a_rows
+    a_d = torch.from_numpy(a_i8.view(np.uint8)).to(dev)
+    w_d = torch.from_numpy(w_i8.view(np.uint8)).to(dev)
+    a_bf = torch.empty((rows, K), dtype=torch.bfloat16, device=dev)
+    a_bf.zero_()
+    w_bf = torch.empty((G, N, K), dtype=torch.bfloat16, device=dev)
+    ep.moe_codes_to_bf16(a_d, M, K, K, a_bf)
+    ep.moe_codes_to_bf16(w_d, G * N, K, K, w_bf)
+    gr = torch.tensor(sizes, dtype=torch.int32, device=dev)
+    c = torch.full((rows, N), fill, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ep.moe_grouped_gemm_i8(a_bf, w_bf, gr, c, st)
+    torch.cuda.synchronize()
+    return c.cpu().numpy(), int(st.item())
+
+
+GEMM_CASES = [
+    # (G, N, K, group sizes): ragged row tiles, empty groups, one K block,
+    # a ragged K block, several exact 1024-wide chunks
+    (3, 128, 64, (5, 0, 130)),
+    (4, 256, 200, (128, 1, 0, 257)),
+    (2, 128, 1096, (300, 45)),
+    (5, 384, 2056, (64, 129, 0, 200, 3)),
+    (3, 136, 520, (70, 0, 200)),          # a ragged last column tile
+    (2, 8, 32, (3, 140)),                 # N and K below one tile
+]
+
+
+@pytest.mark.parametrize("case", GEMM_CASES, ids=lambda c: "G%d_N%d_K%d" % c[:3])
+def test_grouped_gemm_exact(oracle_mod, ep, case):
+    G, N, K, sizes = case
+    rng = np.random.default_rng(sum(sizes) + K)
+    M = sum(sizes)
+    a = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    w = rng.integers(-127, 128, (G, N, K)).astype(np.int8)
+    c, st = _gemm_gpu(ep, a, w, sizes)
+    assert st == 0
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    _eq("c", c, oracle_mod.grouped_gemm(a.view(np.uint8), off, w))
+
+
+def test_grouped_gemm_extreme_sums(oracle_mod, ep):
+    """Codes of one sign make every 1024-wide chunk sum reach 1024*127*127
+    (just under 2^24), and the whole row 7168*127*127; alternating rows
+    flip the sign; a row of -128 codes reaches exactly 2^24 per chunk."""
+    K, N = 7168, 128
+    a = np.full((6, K), 127, np.int8)
+    a[1] = -127
+    a[2, ::2] = -127
+    a[3] = -128
+    a[4] = np.arange(K) % 255 - 127
+    a[5] = 1
+    w = np.full((1, N, K), 127, np.int8)
+    w[0, 1::2] = -128
+    c, st = _gemm_gpu(ep, a, w, (6,))
+    assert st == 0
+    want = oracle_mod.grouped_gemm(a.view(np.uint8), np.array([0, 6], np.int64), w)
+    _eq("c", c, want)
+    assert want[0, 0] == 127 * 127 * K and want[3, 1] == 128 * 128 * K
+
+
+def test_grouped_gemm_rows_beyond_groups_untouched_and_capacity(ep):
+    rng = np.random.default_rng(5)
+    K, N = 64, 128
+    a = rng.integers(-127, 128, (40, K)).astype(np.int8)
+    w = rng.integers(-127, 128, (2, N, K)).astype(np.int8)
+    c, st = _gemm_gpu(ep, a, w, (10, 20), fill=-7)       # 30 of 40 rows used
+    assert st == 0 and (c[30:] == -7).all()
+    c, st = _gemm_gpu(ep, a, w, (30, 20), fill=-7)       # 50 rows > 40
+    assert st == ep.MOE_ERR_CAPACITY and (c == -7).all()
+
+
+def test_grouped_gemm_rejects_bad_shapes(ep):
+    dev = torch.device("cuda")
+    a = torch.zeros((16, 64), dtype=torch.bfloat16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    gr = torch.tensor([16], dtype=torch.int32, device=dev)
+    for N, K in ((100, 64), (128, 60)):   # N % 8, K % 8
+        w = torch.zeros((1, N, K), dtype=torch.bfloat16, device=dev)
+        aa = torch.zeros((16, K), dtype=torch.bfloat16, device=dev)
+        c = torch.zeros((16, N), dtype=torch.int32, device=dev)
+        with pytest.raises(ep.MoeError):
+            ep.moe_grouped_gemm_i8(aa, w, gr, c, st)
+    del a
+
+
+def _deep_inputs(w, I, seed, device="cpu"):
+    idx, wt = W.routing(w)
+    x = W.tokens(w)
+    w1, ws1, w2, ws2 = W.moe_weights(w.E, w.H, I, seed=seed, device=device)
+    return idx, wt, x, (w1, ws1 * 40.0, w2, ws2 * 40.0)
+
+
+DEEP_CASES = [
+    W.Workload("deep_small", R=2, epr=4, bs=96, H=256, k=4, seed=21),
+    W.Workload("deep_ragged", R=3, epr=3, bs=70, H=1096, k=3, routing="zipf",
+               weights="sigmoid", x_scale=2.0, seed=22),
+]
+
+
+@pytest.mark.parametrize("w", DEEP_CASES, ids=lambda w: w.name)
+def test_deep_moe_pipeline(oracle_mod, pl, w):
+    I = 136 if w.H > 512 else 128
+    idx, wt, x, (w1, ws1, w2, ws2) = _deep_inputs(w, I, w.seed)
+    ref = oracle_mod.deep_moe(W.bits(x), idx.numpy(), wt.numpy(), w.R, w.epr, w.dtype,
+                              w1.numpy(), ws1.numpy(), w2.numpy(), ws2.numpy())
+    dev = torch.device("cuda")
+    b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype)
+    wts = pl.DeepMoeWeights(w1.to(dev), ws1.to(dev), w2.to(dev), ws2.to(dev))
+    idx_d, wt_d = idx.to(dev), wt.to(dev)
+    pl.run_layout_notify(b, idx_d)
+    pl.run_dispatch(b, x.to(dev), idx_d)
+    assert b.status() == 0, "dispatch"
+    L = oracle_mod.layout(idx.numpy(), w.R, w.epr)
+    N = oracle_mod.notify(L["count"], w.R, w.bs, w.epr)
+    recv, _ = oracle_mod.dispatch(W.bits(x), idx.numpy(), L["send_idx"], N["put_offset"],
+                                  N["rank_recv_base"], w.R, w.epr, w.dtype, True)
+    _eq("recv", b.recv, recv)
+    pl.run_deep_moe_experts(b, wts)
+    assert b.status() == 0, "experts"
+    pl.run_deq_combine(b, wts, idx_d, wt_d)
+    assert b.status() == 0, "deq_combine"
+    _eq("group_off", b.group_off, ref["group_off"])
+    _eq("acc1", b.acc1, ref["acc1"])
+    _eq("x2", b.x2, ref["x2"])
+    _eq("acc2", b.acc2, ref["acc2"])
+    _eq("out", b.out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"])
+
+
+def test_deep_moe_dsv3_size_sampled(oracle_mod, pl):
+    """DeepSeek-V3 shape (R = 8, E = 256, bs = 4096, k = 8, H = 7168,
+    I = 2048), weights drawn on the device; sampled tokens are checked
+    against the oracle run on their rows only (the needed experts' weights
+    copied back)."""
+    w = W.WORKLOADS["dsv3"]
+    I = 2048
+    dev = torch.device("cuda")
+    idx, wt = W.routing(w)
+    x = W.tokens(w)
+    w1, ws1, w2, ws2 = W.moe_weights(w.E, w.H, I, seed=31, device=dev)
+    ws1, ws2 = ws1 * 40.0, ws2 * 40.0
+    b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype)
+    wts = pl.DeepMoeWeights(w1, ws1, w2, ws2)
+    pl.run_deep_moe(b, wts, x.to(dev), idx.to(dev), wt.to(dev))
+    torch.cuda.synchronize()
+    assert b.status() == 0
+    toks = np.array([0, 12345, w.T - 1], np.int64)
+    idx_n, wt_n = idx.numpy(), wt.numpy()
+    L = oracle_mod.layout(idx_n, w.R, w.epr)
+    N = oracle_mod.notify(L["count"], w.R, w.bs, w.epr)
+    images, row_ids, st = oracle_mod.dispatch_tokens(
+        W.bits(x), idx_n, L["send_idx"], N["put_offset"], N["rank_recv_base"], w.R,
+        w.epr, w.dtype, True, toks)
+    assert st == 0
+    n = toks.size * w.k
+    acc2 = np.zeros((n, w.H), np.int32)
+    x2 = np.zeros((n, (I + 31) // 32 * 32 + 32), np.uint8)
+    one = np.array([0, 1], np.int64)
+    for i in range(n):
+        t, kk = divmod(i, w.k)
+        e = int(idx_n[toks[t], kk])
+        img = images[t, kk][None]
+        a1 = oracle_mod.grouped_gemm(img, one, w1[e].cpu().numpy()[None])
+        _eq("acc1 row", b.acc1[int(row_ids[t, kk])], a1[0])
+        ts = oracle_mod.row_inv_scale(img, w.H)
+        x2[i] = oracle_mod.swiglu_quant(a1, ws1[e].cpu().numpy(), ts)[0]
+        _eq("x2 row", b.x2[int(row_ids[t, kk])], x2[i])
+        acc2[i] = oracle_mod.grouped_gemm(x2[i:i + 1], one, w2[e].cpu().numpy()[None])[0]
+        _eq("acc2 row", b.acc2[int(row_ids[t, kk])], acc2[i])
+    out, st = oracle_mod.deq_combine(acc2, ws2.cpu().numpy(), oracle_mod.row_inv_scale(x2, I),
+                                     idx_n, wt_n, L["send_idx"], N["put_offset"],
+                                     N["rank_recv_base"], w.R, w.epr, w.dtype, tokens=toks)
+    assert st == 0
+    _eq("out rows", b.out[torch.from_numpy(toks).to(dev)].view(torch.int16).cpu().numpy()
+        .view(np.uint16), out)

@@ -179,6 +179,21 @@ def test_mid_size(oracle_mod, pl, case):
     _check_full(oracle_mod, pl, w)
 
 
+@pytest.mark.parametrize("case", [
+    dict(R=3, epr=3, bs=70, k=3, H=1096, routing="zipf"),   # one-warp tiles, E = 9
+    dict(R=7, epr=1, bs=333, k=1, H=2048),                   # E = 7
+    dict(R=5, epr=3, bs=40, k=2, H=64),                      # E = 15
+], ids=lambda c: "R%d-epr%d" % (c["R"], c["epr"]))
+def test_odd_expert_count_after_dirty_shared_memory(oracle_mod, pl, case):
+    """One-warp layout tiles keep E uint16 counters; with E odd the last one
+    sits in half of a 32-bit word.  A dispatch with 14 KB rows first leaves
+    nonzero bytes in every SM's shared memory, so an uncleared counter would
+    show up in send_idx / count."""
+    dirty = W.Workload("dirty", R=2, epr=4, bs=2048, k=4, H=7168, seed=3)
+    _run_gpu(pl, dirty, *W.routing(dirty), W.tokens(dirty), W.expert_outputs(dirty))
+    _check_full(oracle_mod, pl, W.Workload("odd", **case))
+
+
 def test_duplicate_experts_in_token(oracle_mod, pl):
     w = W.Workload("dup", R=3, epr=2, bs=500, k=6, H=96)
     rng = np.random.default_rng(11)
