@@ -565,6 +565,46 @@ def run_deep_moe_bench(args, w, ep, pl, x, idx, wt, stream, dev, flush):
     return res
 
 
+def run_gemm_only(args):
+    """--gemm G,ROWS,N,K: times moe_grouped_gemm_i8 alone on G groups of ROWS
+    rows (int8-valued bf16 operands drawn on the device) and prints one JSON
+    line.  A kernel benchmark, not the step contract."""
+    import combine_moe_dispatch_layout_gb300 as ep
+    G, rows, N, K = (int(v) for v in args.gemm.split(","))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    M = G * rows
+    a = torch.randint(-127, 128, (M, K), generator=g, device=dev).to(torch.bfloat16)
+    w = torch.randint(-127, 128, (G, N, K), generator=g, device=dev).to(torch.bfloat16)
+    gr = torch.full((G,), rows, dtype=torch.int32, device=dev)
+    c = torch.empty((M, N), dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        ep.moe_grouped_gemm_i8(a, w, gr, c, st, stream)
+    evs = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ep.moe_grouped_gemm_i8(a, w, gr, c, st, stream)
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError("device status %d" % int(st.item()))
+    us = float(np.mean([x.elapsed_time(y) for x, y in evs])) * 1e3
+    burst, sustained, src = measured_bf16_tflops()
+    tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+    print(json.dumps({"kernel": "grouped_gemm_i8", "groups": G, "rows_per_group": rows,
+                      "N": N, "K": K, "us": us, "tflops": tf, "frac_of_burst": tf / burst,
+                      "peak_source": src, "steps": args.steps}))
+
+
 def run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush):
     """Throughput through the public API with the inputs in pinned host
     memory: every step copies x, topk_idx and topk_weights to the device,
@@ -739,6 +779,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-deep-moe", action="store_true",
                    help="skip the fused deep MoE section")
+    p.add_argument("--gemm", default=None, metavar="G,ROWS,N,K",
+                   help="time the grouped GEMM alone and exit")
     p.add_argument("--ref-tokens", type=int, default=32)
     p.add_argument("--bs", type=int, default=None,
                    help="override tokens per rank (small profiling cases)")
@@ -752,6 +794,9 @@ def main(argv=None):
     args = parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.gemm:
+        run_gemm_only(args)
+        return
     w = W.WORKLOADS[args.workload]
     if args.bs is not None:
         w = w.with_(bs=args.bs)

@@ -14,7 +14,8 @@
 // Same persistent producer / compute structure as the combine: the last
 // warp resolves the next token's rows, weights, experts and row scales into
 // a double-buffered shared table; compute threads own 8 outputs each (two
-// 16-byte loads of int32 per row, 8 rows in flight).  HBM-bound: 4H bytes
+// 16-byte loads of int32 and of the expert's weight scales per row, 4 rows
+// in flight).  HBM-bound: 4H bytes
 // read per (token, k), 2H written per token; the per-expert weight scales
 // (E x H fp32) stay in L2.
 #include <algorithm>
@@ -24,7 +25,7 @@
 namespace moe_ep {
 namespace {
 
-constexpr int kBatch = 8;
+constexpr int kBatch = 4;          // rows (accumulators + weight scales) in flight
 constexpr int kMaxThreads = 512;   // <= 128 registers per thread
 
 template <int DT>
@@ -77,16 +78,21 @@ deq_combine_kernel(const int32_t* __restrict__ acc2, int64_t y_rows,
         for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
         for (int k0 = 0; k0 < k; k0 += kBatch) {
           uint4 v[kBatch][2];
+          float4 wsv[kBatch][2];
 #pragma unroll
           for (int b = 0; b < kBatch; ++b) {
             const int kk = k0 + b;
             const int64_t row = kk < k ? rows[kk] : -1;
             if (row >= 0) {
               const int32_t* src = acc2 + row * H + 8 * c;
+              const float* ws = weight_scale + int64_t(s_e[buf][kk]) * H + 8 * c;
               v[b][0] = ld_stream_16(src);
               v[b][1] = ld_stream_16(src + 4);
+              wsv[b][0] = __ldg(reinterpret_cast<const float4*>(ws));
+              wsv[b][1] = __ldg(reinterpret_cast<const float4*>(ws + 4));
             } else {
               v[b][0] = v[b][1] = make_uint4(0u, 0u, 0u, 0u);
+              wsv[b][0] = wsv[b][1] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
           }
 #pragma unroll
@@ -94,16 +100,14 @@ deq_combine_kernel(const int32_t* __restrict__ acc2, int64_t y_rows,
             const int kk = k0 + b;
             if (kk < k && rows[kk] >= 0) {
               const float wk = s_w[buf][kk], ts = s_ts[buf][kk];
-              const float* ws = weight_scale + int64_t(s_e[buf][kk]) * H + 8 * c;
-              const float4 w0 = __ldg(reinterpret_cast<const float4*>(ws));
-              const float4 w1 = __ldg(reinterpret_cast<const float4*>(ws + 4));
-              const float wsv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+              const float wsr[8] = {wsv[b][0].x, wsv[b][0].y, wsv[b][0].z, wsv[b][0].w,
+                                    wsv[b][1].x, wsv[b][1].y, wsv[b][1].z, wsv[b][1].w};
               const uint32_t a[8] = {v[b][0].x, v[b][0].y, v[b][0].z, v[b][0].w,
                                      v[b][1].x, v[b][1].y, v[b][1].z, v[b][1].w};
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 float y = __int2float_rn(static_cast<int32_t>(a[j]));   // Cast FP32
-                y = __fmul_rn(y, wsv[j]);                               // x weight_scale
+                y = __fmul_rn(y, wsr[j]);                               // x weight_scale
                 y = __fmul_rn(y, ts);                                   // x per-token scale
                 acc[j] = __fadd_rn(acc[j], __fmul_rn(y, wk));           // Muls, Add
               }

@@ -13,19 +13,20 @@
 //     the chunks in int32.
 // The result is the int32 GEMM bit for bit.
 //
-// Kernel: persistent CTAs (one per SM) walk 128 x 128 output tiles (the last
+// Kernel: persistent CTAs (one per SM) walk 128 x 256 output tiles (the last
 // column tile may be ragged: its B rows past the expert are computed from
 // the next expert's rows, or zero-filled by TMA, and never stored; tiles of
 // one expert together, m fastest, so the expert's weights and rows are
-// reused from L2).  Warp 0 streams 128 x 64 bf16 tiles of A and B into a
-// 4-stage shared-memory ring with TMA (cp.async.bulk.tensor, 128-byte
-// swizzle); warp 1 allocates 256 TMEM columns and one elected lane issues
-// tcgen05.mma (M = 128, N = 128, K = 16, fp32 accumulate) into one of two
-// 128-column accumulators, alternating per K chunk; warps 2-5 drain a
-// finished chunk accumulator (tcgen05.ld, one TMEM lane = one output row per
-// thread) into int32 registers while the next chunk accumulates, then store
-// the tile's rows.  Every mbarrier wait is bounded: a timeout sets
-// MOE_ERR_TIMEOUT and the CTA stops issuing work.
+// reused from L2).  Warp 0 streams 128 x 64 (A) and 256 x 64 (B) bf16 tiles
+// into a 4-stage shared-memory ring with TMA (cp.async.bulk.tensor, 128-byte
+// swizzle; 192 KB in flight per SM, which the L2 latency needs); warp 1
+// allocates all 512 TMEM columns and one elected lane issues tcgen05.mma
+// (M = 128, N = 256, K = 16, fp32 accumulate) into one of two 256-column
+// accumulators, alternating per K chunk; warps 2-9 drain a finished chunk
+// accumulator (tcgen05.ld; a warp reads its TMEM lane quarter, one output row
+// per thread, and one half of the columns) into int32 registers while the
+// next chunk accumulates, then store the tile's rows.  Every mbarrier wait is
+// bounded: a timeout sets MOE_ERR_TIMEOUT and the CTA stops issuing work.
 #include <cuda.h>
 
 #include <algorithm>
@@ -35,23 +36,28 @@
 namespace moe_ep {
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64;   // BK bf16 = one 128-byte swizzle row
-constexpr int kStages = 4;
+constexpr int BM = 128, BN = 256, BK = 64;   // BK bf16 = one 128-byte swizzle row
 constexpr int kChunkBlocks = 16;             // 16 x 64 = 1024: exact fp32 partial sums
-constexpr uint32_t kTmemCols = 2 * BN;       // two chunk accumulators
-constexpr int kThreads = 192;                // TMA warp, MMA warp, 4 epilogue warps
+constexpr uint32_t kTmemCols = 2 * BN;       // two chunk accumulators (all of TMEM)
+constexpr int kEpiWarps = 8;                 // 4 TMEM lane quarters x 2 column halves
+constexpr int kThreads = 64 + 32 * kEpiWarps;   // TMA warp, MMA warp, epilogue
+constexpr int kEpiCols = BN / 2;             // columns per epilogue thread
 constexpr uint32_t kTileABytes = BM * BK * 2;
 constexpr uint32_t kTileBBytes = BN * BK * 2;
 constexpr uint32_t kSpin = 1u << 20;         // polls per wait (about a second at the least)
 
-// Dynamic shared memory, from a 1024-byte aligned base.
-constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffB = kOffA + kStages * kTileABytes;
-constexpr uint32_t kOffBar = kOffB + kStages * kTileBBytes;
-constexpr uint32_t kOffTables = kOffBar + 256;
-size_t smem_bytes(int G) {
-  return 1024 + kOffTables + size_t(G + 1) * (sizeof(int64_t) + sizeof(int32_t));
-}
+// Dynamic shared memory, from a 1024-byte aligned base: STAGES A tiles,
+// STAGES B tiles, barriers, then the group tables.
+template <int STAGES>
+struct SmemLayout {
+  static constexpr uint32_t kOffA = 0;
+  static constexpr uint32_t kOffB = kOffA + STAGES * kTileABytes;
+  static constexpr uint32_t kOffBar = kOffB + STAGES * kTileBBytes;
+  static constexpr uint32_t kOffTables = kOffBar + 256;
+  static size_t bytes(int G) {
+    return 1024 + kOffTables + size_t(G + 1) * (sizeof(int64_t) + sizeof(int32_t));
+  }
+};
 
 // ---- tcgen05 / TMA wrappers ---------------------------------------------------
 
@@ -157,6 +163,7 @@ __device__ __forceinline__ Tile decode_tile(int64_t t, const int64_t* goff,
   return tl;
 }
 
+template <int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -165,13 +172,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  using L = SmemLayout<STAGES>;
+  constexpr int kStages = STAGES;
+  constexpr uint32_t kOffA = L::kOffA, kOffB = L::kOffB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
-  int64_t* goff = reinterpret_cast<int64_t*>(smem + kOffTables);
+  int64_t* goff = reinterpret_cast<int64_t*>(smem + L::kOffTables);
   int32_t* tpre = reinterpret_cast<int32_t*>(goff + G + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -225,12 +235,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
-      mbar_init(tempty + b, 4);
+      mbar_init(tempty + b, kEpiWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {   // TMEM: 256 columns for this CTA (one CTA per SM)
+  if (warp == 1) {   // TMEM: all 512 columns for this CTA (one CTA per SM)
     __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
@@ -322,12 +332,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   } else {
     // ---- epilogue: chunk sums -> int32, tile rows -> C -------------------------
     const int q = warp & 3;                  // TMEM lanes 32q .. 32q+31
+    const int half = (warp - 2) >> 2;        // columns half*128 .. half*128+127
     uint32_t chunk_ctr = 0;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
       const Tile tl = decode_tile(t, goff, tpre, G, ntn);
-      int32_t acc[BN];
+      int32_t acc[kEpiCols];
 #pragma unroll
-      for (int j = 0; j < BN; ++j) acc[j] = 0;
+      for (int j = 0; j < kEpiCols; ++j) acc[j] = 0;
       bool ok = true;
       for (int c = 0; c < nchunks; ++c, ++chunk_ctr) {
         const uint32_t b = chunk_ctr & 1u, use = (chunk_ctr >> 1) & 1u;
@@ -337,10 +348,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           break;
         }
         tc_fence_after();
+        const uint32_t base = tmem + (uint32_t(q * 32) << 16) + b * BN + half * kEpiCols;
 #pragma unroll
-        for (int cb = 0; cb < BN / 16; ++cb) {
+        for (int cb = 0; cb < kEpiCols / 16; ++cb) {
           uint32_t v[16];
-          tmem_ld16(tmem + (uint32_t(q * 32) << 16) + b * BN + cb * 16, v);
+          tmem_ld16(base + cb * 16, v);
 #pragma unroll
           for (int j = 0; j < 16; ++j) acc[cb * 16 + j] += __float2int_rn(__uint_as_float(v[j]));
         }
@@ -354,11 +366,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         break;
       }
       const int r = q * 32 + lane;
+      const int col0 = tl.n0 + half * kEpiCols;
       if (r < tl.rows) {
-        int4* dst = reinterpret_cast<int4*>(C + (tl.row0 + r) * int64_t(N) + tl.n0);
-        const int ncols = N - tl.n0;         // a ragged last column tile
+        int4* dst = reinterpret_cast<int4*>(C + (tl.row0 + r) * int64_t(N) + col0);
+        const int ncols = N - col0;          // a ragged last column tile
 #pragma unroll
-        for (int j = 0; j < BN / 4; ++j)
+        for (int j = 0; j < kEpiCols / 4; ++j)
           if (4 * j < ncols)
             dst[j] = make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
       }
@@ -445,6 +458,24 @@ cudaError_t launch_codes_to_bf16(const void* src, int64_t rows, int64_t stride, 
 
 int gmm_block_n() { return BN; }
 
+namespace {
+
+template <int STAGES>
+cudaError_t launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const int32_t* group_rows,
+                          int G, int64_t a_rows, int K, int N, int32_t* c, int32_t* dev_status,
+                          int sms, cudaStream_t st) {
+  const size_t smem = SmemLayout<STAGES>::bytes(G);
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<STAGES>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  grouped_gemm_kernel<STAGES><<<sms, kThreads, smem, st>>>(ma, mb, group_rows, G, a_rows, K, N,
+                                                           c, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
 cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void* b, int G,
                                 int N, const int32_t* group_rows, int32_t* c,
                                 int32_t* dev_status, cudaStream_t st) {
@@ -452,17 +483,17 @@ cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void
   cudaError_t e = encode_kmajor(&ma, a, a_rows, K, BM);
   if (e == cudaSuccess) e = encode_kmajor(&mb, b, int64_t(G) * N, K, BN);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
+  int dev = 0, sms = 0, optin = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const size_t smem = smem_bytes(G);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(grouped_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  grouped_gemm_kernel<<<sms, kThreads, smem, st>>>(ma, mb, group_rows, G, a_rows, K, N, c,
-                                                    dev_status);
-  return cudaGetLastError();
+  // four stages unless the group tables (12 bytes per group) crowd them out
+  const size_t static_smem = 12 * kThreads + 256;
+  if (SmemLayout<4>::bytes(G) + static_smem <= size_t(optin))
+    return launch_stages<4>(ma, mb, group_rows, G, a_rows, K, N, c, dev_status, sms, st);
+  return launch_stages<3>(ma, mb, group_rows, G, a_rows, K, N, c, dev_status, sms, st);
 }
 
 }  // namespace moe_ep

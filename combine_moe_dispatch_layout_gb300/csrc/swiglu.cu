@@ -88,17 +88,14 @@ swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc 
     if (rows < M) M = rows;
   }
 
+  int grp = 0;                           // rows only increase: the group moves forward
   for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
     const int32_t* row = acc + m * 2 * int64_t(I);
     const float ts = __ldg(reinterpret_cast<const float*>(sc.ts_base + m * sc.ts_stride));
     const float* weight_scale = sc.weight_scale;
     if (sc.group_off) {                  // largest g with group_off[g] <= m
-      int lo = 0, hi = sc.G;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(sc.group_off + mid) <= m) lo = mid; else hi = mid;
-      }
-      weight_scale += int64_t(lo) * 2 * I;
+      while (grp + 1 < sc.G && __ldg(sc.group_off + grp + 1) <= m) ++grp;
+      weight_scale += int64_t(grp) * 2 * I;
     }
     float h[kCpt][8];
     float amax = 0.0f;

@@ -66,6 +66,7 @@ GEMM_CASES = [
     (5, 384, 2056, (64, 129, 0, 200, 3)),
     (3, 136, 520, (70, 0, 200)),          # a ragged last column tile
     (2, 8, 32, (3, 140)),                 # N and K below one tile
+    (3000, 136, 72, tuple((7 * i) % 5 for i in range(3000))),   # many groups: 3 stages
 ]
 
 
