@@ -488,13 +488,13 @@ def run_deep_moe_bench(args, w, ep, pl, x, idx, wt, stream, dev, flush):
     grouped GEMMs are reported against the dense bf16 tensor peak."""
     I = SWIGLU_INTERMEDIATE
     w1, ws1, w2, ws2 = W.moe_weights(w.E, w.H, I, seed=31, device=dev)
-    wts = pl.DeepMoeWeights(w1, ws1 * 40.0, w2, ws2 * 40.0, stream)
+    wts = pl.DeepMoeWeights(w1, ws1, w2, ws2, stream)
     torch.cuda.synchronize()
     del w1, w2
     b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype, device=dev)
     P, H = w.P, w.H
     names = ["layout+notify", "dispatch", "offsets+a1_bf16", "gemm1", "swiglu_quant",
-             "a2_bf16", "gemm2", "deq_combine"]
+             "a2_bf16", "gemm2+dequant", "combine_f32"]
 
     def step(evs=None):
         def mark(j):
@@ -517,8 +517,9 @@ def run_deep_moe_bench(args, w, ep, pl, x, idx, wt, stream, dev, flush):
         mark(5)
         ep.moe_codes_to_bf16(b.x2, P, b.row2, I, b.a2, stream)
         mark(6)
-        ep.moe_grouped_gemm_i8(b.a2, wts.w2, b.recv_per_expert, b.acc2, b.dev_status,
-                               stream)
+        ep.moe_grouped_gemm_i8_dequant(b.a2, wts.w2, b.recv_per_expert, wts.ws2,
+                                       (b.x2, (I + 31) // 32 * 32, b.row2), b.y2,
+                                       b.dev_status, stream)
         mark(7)
         pl.run_deq_combine(b, wts, idx, wt, stream)
         mark(8)

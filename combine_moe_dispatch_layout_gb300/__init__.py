@@ -80,11 +80,15 @@ def _load():
                                            ctypes.c_int32, vp, i64, vp, vp, vp]
     L.moe_deq_combine.argtypes = [sp, vp, i64, vp, vp, i64, vp, vp, vp, vp, vp,
                                   vp, vp, vp]
+    L.moe_grouped_gemm_i8_dequant.argtypes = [vp, i64, ctypes.c_int32, vp, ctypes.c_int32,
+                                              ctypes.c_int32, vp, vp, vp, i64, vp, vp, vp]
+    L.moe_combine_f32.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     for name in ("moe_dispatch_layout", "moe_notify_dispatch", "moe_dispatch",
                  "moe_combine", "moe_combine_quant", "moe_token_layout",
                  "moe_dispatch_fused", "moe_swiglu_quant", "moe_group_offsets",
                  "moe_codes_to_bf16", "moe_grouped_gemm_i8",
-                 "moe_swiglu_quant_grouped", "moe_deq_combine"):
+                 "moe_swiglu_quant_grouped", "moe_deq_combine",
+                 "moe_grouped_gemm_i8_dequant", "moe_combine_f32"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -414,3 +418,42 @@ def moe_deq_combine(shape, expert_acc, weight_scale, row_scale, topk_idx,
         _ptr(out, None, T * H, "out"), _ptr(dev_status, torch.int32, 1, "dev_status"),
         _stream(stream))
     return _check(st, "moe_deq_combine")
+
+
+def moe_grouped_gemm_i8_dequant(a, w, group_rows, col_scale, row_scale, y, dev_status,
+                                stream=None):
+    """y [a_rows, N] fp32 = (fp32(a x w[g]^T) * col_scale[g]) * row scale;
+    row_scale is (tensor, byte_offset, byte_stride)."""
+    if a.dim() != 2 or w.dim() != 3 or w.shape[2] != a.shape[1]:
+        raise ValueError("a must be [rows, K] and w [G, N, K]")
+    rows, K = a.shape
+    G, N = w.shape[0], w.shape[1]
+    if group_rows.numel() != G:
+        raise ValueError("group_rows must have G entries")
+    rp, rstride = _strided(row_scale, rows, "row_scale")
+    st = _lib.moe_grouped_gemm_i8_dequant(
+        _ptr(a, torch.bfloat16, rows * K, "a"), int(rows), int(K),
+        _ptr(w, torch.bfloat16, G * N * K, "w"), int(G), int(N),
+        _ptr(group_rows, torch.int32, G, "group_rows"),
+        _ptr(col_scale, torch.float32, G * N, "col_scale"), rp, rstride,
+        _ptr(y, torch.float32, rows * N, "y"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_grouped_gemm_i8_dequant")
+
+
+def moe_combine_f32(shape, expert_out, topk_idx, topk_weights, send_idx, put_offset,
+                    rank_recv_base, out, dev_status, stream=None):
+    """Combine over fp32 expert outputs [rows, H]."""
+    T, k, H = shape.R * shape.bs, shape.k, shape.H
+    E = shape.R * shape.experts_per_rank
+    rows = expert_out.shape[0]
+    st = _lib.moe_combine_f32(
+        ctypes.byref(shape), _ptr(expert_out, torch.float32, rows * H, "expert_out"),
+        int(rows), _ptr(topk_idx, torch.int32, T * k, "topk_idx"),
+        _ptr(topk_weights, torch.float32, T * k, "topk_weights"),
+        _ptr(send_idx, torch.int32, T * k, "send_idx"),
+        _ptr(put_offset, torch.int32, E * shape.R, "put_offset"),
+        _ptr(rank_recv_base, torch.int64, shape.R + 1, "rank_recv_base"),
+        _ptr(out, None, T * H, "out"), _ptr(dev_status, torch.int32, 1, "dev_status"),
+        _stream(stream))
+    return _check(st, "moe_combine_f32")

@@ -278,9 +278,53 @@ moe_status moe_grouped_gemm_i8(const void* a, int64_t a_rows, int32_t K, const v
   if (!aligned(a, 16) || !aligned(w, 16) || !aligned(group_rows, 4) || !aligned(c, 16) ||
       !aligned(dev_status, 4))
     return MOE_ERR_INVALID_ARG;
-  return from_cuda(moe_ep::launch_grouped_gemm(a, a_rows, K, w, G, N, group_rows, c,
+  return from_cuda(moe_ep::launch_grouped_gemm(a, a_rows, K, w, G, N, group_rows, c, nullptr,
+                                               nullptr, 0, dev_status,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_gemm_i8_dequant(const void* a, int64_t a_rows, int32_t K,
+                                       const void* w, int32_t G, int32_t N,
+                                       const int32_t* group_rows, const float* col_scale,
+                                       const void* row_scale, int64_t row_scale_stride,
+                                       float* y, int32_t* dev_status, void* stream) {
+  const int64_t bn = moe_ep::gmm_block_n();
+  if (a_rows < 1 || a_rows > INT32_MAX || K < 8 || K > MOE_EP_MAX_HIDDEN || K % 8 != 0 ||
+      G < 1 || G > MOE_EP_MAX_EXPERTS || N < 8 || N > MOE_EP_MAX_HIDDEN || N % 8 != 0 ||
+      row_scale_stride < 4 || row_scale_stride % 4 != 0 || !dev_status)
+    return MOE_ERR_INVALID_ARG;
+  if ((a_rows / 128 + G) * ((N + bn - 1) / bn) > INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if (!a || !w || !group_rows || !col_scale || !row_scale || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned(a, 16) || !aligned(w, 16) || !aligned(group_rows, 4) ||
+      !aligned(col_scale, 16) || !aligned(row_scale, 4) || !aligned(y, 16) ||
+      !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_grouped_gemm(a, a_rows, K, w, G, N, group_rows, y,
+                                               col_scale, row_scale, row_scale_stride,
                                                dev_status,
                                                static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_combine_f32(const moe_shape* shape, const float* expert_out,
+                           int64_t expert_out_rows, const int32_t* topk_idx,
+                           const float* topk_weights, const int32_t* send_idx,
+                           const int32_t* put_offset, const int64_t* rank_recv_base,
+                           void* out, int32_t* dev_status, void* stream) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return MOE_ERR_INVALID_ARG;
+  if (expert_out_rows < 0 || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (s.T() == 0) return MOE_OK;
+  if ((!expert_out && expert_out_rows > 0) || !topk_idx || !topk_weights || !send_idx ||
+      !put_offset || !rank_recv_base || !out)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(expert_out, 16) || !aligned(out, 16) || !aligned(topk_idx, 4) ||
+      !aligned(topk_weights, 4) || !aligned(send_idx, 4) || !aligned(put_offset, 4) ||
+      !aligned(rank_recv_base, 8) || !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_combine_f32(s, expert_out, expert_out_rows, topk_idx,
+                                              topk_weights, send_idx, put_offset,
+                                              rank_recv_base, out, dev_status,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_group_offsets(const int32_t* group_rows, int32_t G, int64_t* group_off,

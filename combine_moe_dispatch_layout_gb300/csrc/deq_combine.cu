@@ -11,6 +11,10 @@
 // is one fp32 operation rounded to nearest even (_rn intrinsics; the unit is
 // built with -fmad=false).
 //
+// moe_combine_f32 runs the same kernel on fp32 rows that the GMM2 epilogue
+// has already dequantised (the two multiplies in the same order), so the
+// combine reads 4H bytes per (token, k) and no weight scales.
+//
 // Same persistent producer / compute structure as the combine: the last
 // warp resolves the next token's rows, weights, experts and row scales into
 // a double-buffered shared table; compute threads own 8 outputs each (two
@@ -25,10 +29,12 @@
 namespace moe_ep {
 namespace {
 
-constexpr int kBatch = 4;          // rows (accumulators + weight scales) in flight
 constexpr int kMaxThreads = 512;   // <= 128 registers per thread
 
-template <int DT>
+// DEQ: int32 rows dequantised with the expert's column scales and the row
+// scale (DeqCombine).  !DEQ: fp32 rows already dequantised (by the GEMM's
+// epilogue), weight_scale and row_scale unused.
+template <int DT, bool DEQ>
 __global__ void __launch_bounds__(kMaxThreads)
 deq_combine_kernel(const int32_t* __restrict__ acc2, int64_t y_rows,
                    const float* __restrict__ weight_scale,
@@ -39,6 +45,7 @@ deq_combine_kernel(const int32_t* __restrict__ acc2, int64_t y_rows,
                    const int64_t* __restrict__ rank_recv_base, int R, int bs, int k,
                    int epr, int H, int64_t T, uint4* __restrict__ out,
                    int32_t* dev_status) {
+  constexpr int kBatch = DEQ ? 4 : 8;   // rows in flight (DEQ: + weight scales)
   __shared__ int64_t s_rows[2][MOE_EP_MAX_TOPK];
   __shared__ float s_w[2][MOE_EP_MAX_TOPK];
   __shared__ int32_t s_e[2][MOE_EP_MAX_TOPK];
@@ -52,7 +59,7 @@ deq_combine_kernel(const int32_t* __restrict__ acc2, int64_t y_rows,
     resolve_token(gt, topk_idx, weights, send_idx, put_offset, rank_recv_base, R, bs, k,
                   epr, y_rows, s_rows[b], s_w[b], dev_status, lane);
     __syncwarp();
-    for (int kk = lane; kk < k; kk += 32) {
+    for (int kk = lane; DEQ && kk < k; kk += 32) {
       const int64_t row = s_rows[b][kk];
       s_e[b][kk] = row >= 0 ? __ldg(topk_idx + gt * k + kk) : 0;
       s_ts[b][kk] = row >= 0 ? __ldg(reinterpret_cast<const float*>(row_scale + row * rs_stride))
@@ -85,11 +92,13 @@ deq_combine_kernel(const int32_t* __restrict__ acc2, int64_t y_rows,
             const int64_t row = kk < k ? rows[kk] : -1;
             if (row >= 0) {
               const int32_t* src = acc2 + row * H + 8 * c;
-              const float* ws = weight_scale + int64_t(s_e[buf][kk]) * H + 8 * c;
               v[b][0] = ld_stream_16(src);
               v[b][1] = ld_stream_16(src + 4);
-              wsv[b][0] = __ldg(reinterpret_cast<const float4*>(ws));
-              wsv[b][1] = __ldg(reinterpret_cast<const float4*>(ws + 4));
+              if (DEQ) {
+                const float* ws = weight_scale + int64_t(s_e[buf][kk]) * H + 8 * c;
+                wsv[b][0] = __ldg(reinterpret_cast<const float4*>(ws));
+                wsv[b][1] = __ldg(reinterpret_cast<const float4*>(ws + 4));
+              }
             } else {
               v[b][0] = v[b][1] = make_uint4(0u, 0u, 0u, 0u);
               wsv[b][0] = wsv[b][1] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -106,9 +115,14 @@ deq_combine_kernel(const int32_t* __restrict__ acc2, int64_t y_rows,
                                      v[b][1].x, v[b][1].y, v[b][1].z, v[b][1].w};
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
-                float y = __int2float_rn(static_cast<int32_t>(a[j]));   // Cast FP32
-                y = __fmul_rn(y, wsr[j]);                               // x weight_scale
-                y = __fmul_rn(y, ts);                                   // x per-token scale
+                float y;
+                if (DEQ) {
+                  y = __int2float_rn(static_cast<int32_t>(a[j]));       // Cast FP32
+                  y = __fmul_rn(y, wsr[j]);                             // x weight_scale
+                  y = __fmul_rn(y, ts);                                 // x per-token scale
+                } else {
+                  y = __uint_as_float(a[j]);                            // already fp32
+                }
                 acc[j] = __fadd_rn(acc[j], __fmul_rn(y, wk));           // Muls, Add
               }
             }
@@ -126,7 +140,7 @@ int compute_threads(int nch) {
   return std::max(32, std::min(kMaxThreads - 32, t));
 }
 
-template <int DT>
+template <int DT, bool DEQ>
 cudaError_t launch_t(const Shape& s, const int32_t* acc2, int64_t y_rows,
                      const float* weight_scale, const void* row_scale, int64_t rs_stride,
                      const int32_t* topk_idx, const float* weights, const int32_t* send_idx,
@@ -137,11 +151,11 @@ cudaError_t launch_t(const Shape& s, const int32_t* acc2, int64_t y_rows,
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, deq_combine_kernel<DT>, threads,
-                                                      0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, deq_combine_kernel<DT, DEQ>,
+                                                      threads, 0);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(s.T(), int64_t(std::max(1, per_sm)) * sms);
-  deq_combine_kernel<DT><<<static_cast<unsigned>(grid), threads, 0, st>>>(
+  deq_combine_kernel<DT, DEQ><<<static_cast<unsigned>(grid), threads, 0, st>>>(
       acc2, y_rows, weight_scale, static_cast<const unsigned char*>(row_scale), rs_stride,
       topk_idx, weights, send_idx, put_offset, rank_recv_base, s.R, s.bs, s.k, s.epr, s.H,
       s.T(), static_cast<uint4*>(out), dev_status);
@@ -189,12 +203,26 @@ cudaError_t launch_deq_combine(const Shape& s, const int32_t* acc2, int64_t y_ro
                                void* out, int32_t* dev_status, cudaStream_t st) {
   if (s.T() == 0) return cudaSuccess;
   if (s.dtype == MOE_BF16)
-    return launch_t<MOE_BF16>(s, acc2, y_rows, weight_scale, row_scale, row_scale_stride,
-                              topk_idx, weights, send_idx, put_offset, rank_recv_base, out,
-                              dev_status, st);
-  return launch_t<MOE_FP16>(s, acc2, y_rows, weight_scale, row_scale, row_scale_stride,
-                            topk_idx, weights, send_idx, put_offset, rank_recv_base, out,
-                            dev_status, st);
+    return launch_t<MOE_BF16, true>(s, acc2, y_rows, weight_scale, row_scale, row_scale_stride,
+                                    topk_idx, weights, send_idx, put_offset, rank_recv_base,
+                                    out, dev_status, st);
+  return launch_t<MOE_FP16, true>(s, acc2, y_rows, weight_scale, row_scale, row_scale_stride,
+                                  topk_idx, weights, send_idx, put_offset, rank_recv_base, out,
+                                  dev_status, st);
+}
+
+cudaError_t launch_combine_f32(const Shape& s, const float* y, int64_t y_rows,
+                               const int32_t* topk_idx, const float* weights,
+                               const int32_t* send_idx, const int32_t* put_offset,
+                               const int64_t* rank_recv_base, void* out, int32_t* dev_status,
+                               cudaStream_t st) {
+  if (s.T() == 0) return cudaSuccess;
+  const int32_t* yy = reinterpret_cast<const int32_t*>(y);
+  if (s.dtype == MOE_BF16)
+    return launch_t<MOE_BF16, false>(s, yy, y_rows, nullptr, nullptr, 4, topk_idx, weights,
+                                     send_idx, put_offset, rank_recv_base, out, dev_status, st);
+  return launch_t<MOE_FP16, false>(s, yy, y_rows, nullptr, nullptr, 4, topk_idx, weights,
+                                   send_idx, put_offset, rank_recv_base, out, dev_status, st);
 }
 
 cudaError_t launch_group_offsets(const int32_t* counts, int G, int64_t* off,

@@ -46,13 +46,22 @@ constexpr uint32_t kTileABytes = BM * BK * 2;
 constexpr uint32_t kTileBBytes = BN * BK * 2;
 constexpr uint32_t kSpin = 1u << 20;         // polls per wait (about a second at the least)
 
+// Epilogue stores: each epilogue warp stages 32 rows x 16 columns (2 KB, the
+// TMA store box) in shared memory with the 64-byte swizzle and writes it with
+// one cp.async.bulk.tensor store.
+constexpr int kStoreCols = 16;
+constexpr uint32_t kStageBytes = 32 * kStoreCols * 4;
+
 // Dynamic shared memory, from a 1024-byte aligned base: STAGES A tiles,
-// STAGES B tiles, barriers, then the group tables.
+// STAGES B tiles, the epilogue store buffers, barriers, then the group
+// tables.  The block scan that builds the tables borrows the A area before
+// the first TMA load.
 template <int STAGES>
 struct SmemLayout {
   static constexpr uint32_t kOffA = 0;
   static constexpr uint32_t kOffB = kOffA + STAGES * kTileABytes;
-  static constexpr uint32_t kOffBar = kOffB + STAGES * kTileBBytes;
+  static constexpr uint32_t kOffOut = kOffB + STAGES * kTileBBytes;
+  static constexpr uint32_t kOffBar = kOffOut + kEpiWarps * kStageBytes;
   static constexpr uint32_t kOffTables = kOffBar + 256;
   static size_t bytes(int G) {
     return 1024 + kOffTables + size_t(G + 1) * (sizeof(int64_t) + sizeof(int32_t));
@@ -67,6 +76,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t sdst, const CUtensorMap* ma
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(sdst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// shared -> global tile store (clipped at the tensor's bounds), bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t ssrc, int x,
+                                             int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(ssrc), "r"(x), "r"(y)
       : "memory");
 }
 
@@ -163,12 +182,24 @@ __device__ __forceinline__ Tile decode_tile(int64_t t, const int64_t* goff,
   return tl;
 }
 
+// Optional dequantising epilogue (the page's "Cast FP32 -> x weight_scale ->
+// x per_token_scale" after GMM2): out = (fp32(c) * col_scale[g][n]) * the fp32
+// at row_scale + m * row_scale_stride, each product rounded to nearest even.
+struct Dequant {
+  const float* col_scale;            // [G][N]; nullptr: int32 output
+  const unsigned char* row_scale;
+  int64_t row_scale_stride;          // bytes
+};
+
+// One CTA per SM; registers are allocated per SM sub-partition (16 K each),
+// and 10 warps put 3 on some of them, so at most 168 registers per thread.
 template <int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC,
                     const int32_t* __restrict__ group_rows, int G, int64_t a_rows, int K,
-                    int N, int32_t* __restrict__ C, int32_t* dev_status) {
+                    int N, int32_t* __restrict__ C, Dequant dq, int32_t* dev_status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -198,8 +229,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       rsum += c;
       tsum += static_cast<int32_t>((c + BM - 1) / BM) * ntn;
     }
-    __shared__ int64_t s_r[kThreads];
-    __shared__ int32_t s_t[kThreads];
+    int64_t* s_r = reinterpret_cast<int64_t*>(smem + kOffA);            // [kThreads]
+    int32_t* s_t = reinterpret_cast<int32_t*>(s_r + kThreads);           // [kThreads]
     s_r[tid] = rsum;
     s_t[tid] = tsum;
     __syncthreads();
@@ -367,15 +398,56 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       const int r = q * 32 + lane;
       const int col0 = tl.n0 + half * kEpiCols;
-      if (r < tl.rows) {
+      const int ncols = N - col0;            // a ragged last column tile
+      if (dq.col_scale) {                    // dequantise in registers
+        const float ts = r < tl.rows ? __ldg(reinterpret_cast<const float*>(
+                                           dq.row_scale + (tl.row0 + r) * dq.row_scale_stride))
+                                     : 0.0f;
+        const float* cs = dq.col_scale + int64_t(tl.g) * N + col0;
+#pragma unroll
+        for (int j = 0; j < kEpiCols / 4; ++j) {
+          if (4 * j < ncols) {
+            const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs + 4 * j));
+            const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              acc[4 * j + i] = __float_as_int(
+                  __fmul_rn(__fmul_rn(__int2float_rn(acc[4 * j + i]), cv[i]), ts));
+          }
+        }
+      }
+      if (q * 32 + 32 <= tl.rows) {
+        // all 32 rows of this warp are the group's: swizzled staging + TMA store
+        uint8_t* stg = smem + L::kOffOut + (warp - 2) * kStageBytes;
+        const uint32_t sw = (lane >> 1) & 3u;             // 64-byte swizzle of row `lane`
+#pragma unroll
+        for (int blk = 0; blk < kEpiCols / kStoreCols; ++blk) {
+          if (blk * kStoreCols < ncols) {
+            if (lane == 0) bulk_wait_read<0>();           // the buffer's last store has read it
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<int4*>(stg + lane * 64 + ((c ^ sw) << 4)) =
+                  make_int4(acc[blk * 16 + 4 * c], acc[blk * 16 + 4 * c + 1],
+                            acc[blk * 16 + 4 * c + 2], acc[blk * 16 + 4 * c + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, smem_addr(stg), col0 + blk * kStoreCols,
+                           static_cast<int>(tl.row0 + q * 32));
+              bulk_commit();
+            }
+          }
+        }
+      } else if (r < tl.rows) {              // the group's last rows: plain stores
         int4* dst = reinterpret_cast<int4*>(C + (tl.row0 + r) * int64_t(N) + col0);
-        const int ncols = N - col0;          // a ragged last column tile
 #pragma unroll
         for (int j = 0; j < kEpiCols / 4; ++j)
           if (4 * j < ncols)
             dst[j] = make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
       }
     }
+    if (lane == 0) bulk_wait_all<0>();       // every tile store has landed
   }
 
   tc_fence_before();
@@ -420,14 +492,36 @@ using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, 
                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+cudaError_t get_encoder(void** fn) {
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess) return e;
+  return q == cudaDriverEntryPointSuccess && *fn != nullptr ? cudaSuccess
+                                                            : cudaErrorNotSupported;
+}
+
+// 32-bit outputs [rows][N]: 32-row x 16-column store boxes, 64-byte swizzle.
+cudaError_t encode_out(CUtensorMap* map, void* base, int64_t rows, int N) {
+  void* fn = nullptr;
+  cudaError_t e = get_encoder(&fn);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(N) * 4};
+  const cuuint32_t box[2] = {cuuint32_t(kStoreCols), 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = reinterpret_cast<EncodeTiled>(fn)(
+      map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, base, dims, strides, box, estr,
+      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+      CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t encode_kmajor(CUtensorMap* map, const void* base, int64_t rows, int K,
                           uint32_t box_rows) {
   void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                   cudaEnableDefault, &q);
+  cudaError_t e = get_encoder(&fn);
   if (e != cudaSuccess) return e;
-  if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
   const cuuint64_t strides[1] = {cuuint64_t(K) * 2};
   const cuuint32_t box[2] = {cuuint32_t(BK), box_rows};
@@ -461,27 +555,31 @@ int gmm_block_n() { return BN; }
 namespace {
 
 template <int STAGES>
-cudaError_t launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const int32_t* group_rows,
-                          int G, int64_t a_rows, int K, int N, int32_t* c, int32_t* dev_status,
-                          int sms, cudaStream_t st) {
+cudaError_t launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                          const int32_t* group_rows, int G, int64_t a_rows, int K, int N,
+                          int32_t* c, const Dequant& dq, int32_t* dev_status, int sms,
+                          cudaStream_t st) {
   const size_t smem = SmemLayout<STAGES>::bytes(G);
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<STAGES>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  grouped_gemm_kernel<STAGES><<<sms, kThreads, smem, st>>>(ma, mb, group_rows, G, a_rows, K, N,
-                                                           c, dev_status);
+  grouped_gemm_kernel<STAGES><<<sms, kThreads, smem, st>>>(ma, mb, mc, group_rows, G, a_rows, K,
+                                                           N, c, dq, dev_status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void* b, int G,
-                                int N, const int32_t* group_rows, int32_t* c,
-                                int32_t* dev_status, cudaStream_t st) {
-  CUtensorMap ma, mb;
+                                int N, const int32_t* group_rows, void* c,
+                                const float* col_scale, const void* row_scale,
+                                int64_t row_scale_stride, int32_t* dev_status,
+                                cudaStream_t st) {
+  CUtensorMap ma, mb, mc;
   cudaError_t e = encode_kmajor(&ma, a, a_rows, K, BM);
   if (e == cudaSuccess) e = encode_kmajor(&mb, b, int64_t(G) * N, K, BN);
+  if (e == cudaSuccess) e = encode_out(&mc, c, a_rows, N);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0, optin = 0;
   e = cudaGetDevice(&dev);
@@ -489,11 +587,13 @@ cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
+  const Dequant dq{col_scale, static_cast<const unsigned char*>(row_scale), row_scale_stride};
+  int32_t* out = static_cast<int32_t*>(c);
   // four stages unless the group tables (12 bytes per group) crowd them out
-  const size_t static_smem = 12 * kThreads + 256;
-  if (SmemLayout<4>::bytes(G) + static_smem <= size_t(optin))
-    return launch_stages<4>(ma, mb, group_rows, G, a_rows, K, N, c, dev_status, sms, st);
-  return launch_stages<3>(ma, mb, group_rows, G, a_rows, K, N, c, dev_status, sms, st);
+  if (SmemLayout<4>::bytes(G) <= size_t(optin))
+    return launch_stages<4>(ma, mb, mc, group_rows, G, a_rows, K, N, out, dq, dev_status, sms,
+                            st);
+  return launch_stages<3>(ma, mb, mc, group_rows, G, a_rows, K, N, out, dq, dev_status, sms, st);
 }
 
 }  // namespace moe_ep

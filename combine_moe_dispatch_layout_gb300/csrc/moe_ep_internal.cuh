@@ -249,8 +249,10 @@ cudaError_t launch_codes_to_bf16(const void* src, int64_t rows, int64_t stride, 
 int gmm_block_n();
 
 cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void* b, int G,
-                                int N, const int32_t* group_rows, int32_t* c,
-                                int32_t* dev_status, cudaStream_t st);
+                                int N, const int32_t* group_rows, void* c,
+                                const float* col_scale, const void* row_scale,
+                                int64_t row_scale_stride, int32_t* dev_status,
+                                cudaStream_t st);
 
 cudaError_t launch_group_offsets(const int32_t* counts, int G, int64_t* off,
                                  int32_t* dev_status, cudaStream_t st);
@@ -261,6 +263,12 @@ cudaError_t launch_deq_combine(const Shape& s, const int32_t* acc2, int64_t y_ro
                                const float* weights, const int32_t* send_idx,
                                const int32_t* put_offset, const int64_t* rank_recv_base,
                                void* out, int32_t* dev_status, cudaStream_t st);
+
+cudaError_t launch_combine_f32(const Shape& s, const float* y, int64_t y_rows,
+                               const int32_t* topk_idx, const float* weights,
+                               const int32_t* send_idx, const int32_t* put_offset,
+                               const int64_t* rank_recv_base, void* out, int32_t* dev_status,
+                               cudaStream_t st);
 
 cudaError_t launch_notify(const Shape& s, const int32_t* count,
                           int32_t* put_offset, int32_t* total_recv,

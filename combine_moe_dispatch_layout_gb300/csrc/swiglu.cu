@@ -18,8 +18,8 @@
 // multiply-adds.  The CPU oracle evaluates the same textbook method in the
 // same order, so results match bit for bit.
 //
-// Persistent CTAs walk the rows; each thread owns 8-output chunks (two
-// 32-byte loads of the accumulator per chunk), max|h| is reduced with warp
+// Persistent CTAs walk contiguous blocks of rows; each thread owns 8-output
+// chunks (two 32-byte loads of the accumulator per chunk), max|h| is reduced with warp
 // shuffles and one shared step, and the row image is written with 8-byte
 // stores.  HBM-bound: 8I bytes read and align32(I) + 32 written per row.
 #include <algorithm>
@@ -88,8 +88,13 @@ swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc 
     if (rows < M) M = rows;
   }
 
-  int grp = 0;                           // rows only increase: the group moves forward
-  for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
+  // Each CTA takes a contiguous block of rows: neighbouring rows mostly share
+  // an expert, so its weight-scale vector stays in L1; the group pointer only
+  // moves forward.
+  const int64_t per_cta = (M + gridDim.x - 1) / gridDim.x;
+  const int64_t m_end = (blockIdx.x + 1) * per_cta < M ? (blockIdx.x + 1) * per_cta : M;
+  int grp = 0;
+  for (int64_t m = blockIdx.x * per_cta; m < m_end; ++m) {
     const int32_t* row = acc + m * 2 * int64_t(I);
     const float ts = __ldg(reinterpret_cast<const float*>(sc.ts_base + m * sc.ts_stride));
     const float* weight_scale = sc.weight_scale;

@@ -10,9 +10,9 @@ synchronisation is needed between the stages.
 import torch
 
 from . import (fused_workspace_bytes, make_shape, layout_workspace_bytes,
-               moe_codes_to_bf16, moe_combine, moe_combine_quant,
-               moe_deq_combine, moe_dispatch, moe_dispatch_fused,
-               moe_dispatch_layout, moe_group_offsets, moe_grouped_gemm_i8,
+               moe_codes_to_bf16, moe_combine, moe_combine_f32, moe_combine_quant,
+               moe_dispatch, moe_dispatch_fused, moe_dispatch_layout,
+               moe_group_offsets, moe_grouped_gemm_i8, moe_grouped_gemm_i8_dequant,
                moe_notify_dispatch, moe_swiglu_quant_grouped, recv_row_bytes)
 
 
@@ -127,8 +127,9 @@ class DeepMoeWeights:
 
 class DeepMoeBuffers(PipelineBuffers):
     """PipelineBuffers (INT8 dispatch) plus the deep MoE's intermediates,
-    all sized for T*k rows: bf16 GEMM operands, int32 accumulators, the
-    GMM1 epilogue's INT8 row images and the expert row offsets."""
+    all sized for T*k rows: bf16 GEMM operands, GMM1's int32 accumulators,
+    the GMM1 epilogue's INT8 row images, GMM2's dequantised fp32 outputs and
+    the expert row offsets."""
 
     def __init__(self, R, bs, k, epr, H, I, dtype, device="cuda"):
         super().__init__(R, bs, k, epr, H, dtype, True, device)
@@ -140,12 +141,13 @@ class DeepMoeBuffers(PipelineBuffers):
         self.row2 = _align32(I) + 32
         self.x2 = torch.empty((P, self.row2), dtype=torch.uint8, device=device)
         self.a2 = torch.empty((P, I), dtype=torch.bfloat16, device=device)
-        self.acc2 = torch.empty((P, H), dtype=torch.int32, device=device)
+        self.y2 = torch.empty((P, H), dtype=torch.float32, device=device)
 
 
 def run_deep_moe_experts(b, wts, stream=None):
-    """From the dispatched INT8 rows in ``b.recv`` to GMM2's int32
-    accumulators ``b.acc2`` (GMM1, DeqSwigluQuant, GMM2)."""
+    """From the dispatched INT8 rows in ``b.recv`` to the dequantised expert
+    outputs ``b.y2`` (GMM1, DeqSwigluQuant, GMM2 with its dequantising
+    epilogue)."""
     P, H, I = b.capacity, b.shape.H, b.I
     moe_group_offsets(b.recv_per_expert, b.group_off, b.dev_status, stream)
     moe_codes_to_bf16(b.recv, P, b.row_bytes, H, b.a1, stream)
@@ -154,13 +156,15 @@ def run_deep_moe_experts(b, wts, stream=None):
                              (b.recv, _align32(H), b.row_bytes), b.x2, b.dev_status,
                              stream)
     moe_codes_to_bf16(b.x2, P, b.row2, I, b.a2, stream)
-    moe_grouped_gemm_i8(b.a2, wts.w2, b.recv_per_expert, b.acc2, b.dev_status, stream)
+    moe_grouped_gemm_i8_dequant(b.a2, wts.w2, b.recv_per_expert, wts.ws2,
+                                (b.x2, _align32(I), b.row2), b.y2, b.dev_status, stream)
 
 
 def run_deq_combine(b, wts, topk_idx, topk_weights, stream=None):
-    moe_deq_combine(b.shape, b.acc2, wts.ws2, (b.x2, _align32(b.I), b.row2), topk_idx,
-                    topk_weights, b.send_idx, b.put_offset, b.rank_recv_base, b.out,
-                    b.dev_status, stream)
+    """DeqCombine's remaining step: the weighted sum over the fp32 rows."""
+    del wts
+    moe_combine_f32(b.shape, b.y2, topk_idx, topk_weights, b.send_idx, b.put_offset,
+                    b.rank_recv_base, b.out, b.dev_status, stream)
 
 
 def run_deep_moe(b, wts, x, topk_idx, topk_weights, stream=None):

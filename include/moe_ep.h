@@ -328,6 +328,34 @@ moe_status moe_grouped_gemm_i8(const void* a, int64_t a_rows, int32_t K, const v
                                int32_t G, int32_t N, const int32_t* group_rows, int32_t* c,
                                int32_t* dev_status, void* stream);
 
+/* moe_grouped_gemm_i8 with the GMM2 dequantisation of section 4.3 stage 3
+ * ("Read INT32 -> Cast FP32 -> x weight_scale -> x per_token_scale") done
+ * in the GEMM's epilogue registers: for row m of group g,
+ *   y[m][n] = (fp32(c[m][n]) * col_scale[g][n]) * row_scale(m)
+ * with each product rounded to nearest even, row_scale(m) the fp32 at byte
+ * m * row_scale_stride of row_scale (the GMM1 epilogue rows' 1/scale).  y
+ * feeds moe_combine_f32, which completes DeqCombine with the same results
+ * as moe_deq_combine on c.
+ *   col_scale  fp32 [G][N], 16-byte aligned
+ *   y          fp32 [a_rows][N], 16-byte aligned
+ * Other arguments and limits as moe_grouped_gemm_i8; row_scale_stride >= 4
+ * and a multiple of 4.  One launch. */
+moe_status moe_grouped_gemm_i8_dequant(const void* a, int64_t a_rows, int32_t K,
+                                       const void* w, int32_t G, int32_t N,
+                                       const int32_t* group_rows, const float* col_scale,
+                                       const void* row_scale, int64_t row_scale_stride,
+                                       float* y, int32_t* dev_status, void* stream);
+
+/* Combine over fp32 expert outputs [expert_out_rows][H] (e.g. the output of
+ * moe_grouped_gemm_i8_dequant): acc = acc + (y * w), k in order, acc from 0,
+ * RNE to the token dtype (section 2.6's arithmetic).  Arguments as
+ * moe_combine; expert_out 16-byte aligned.  One launch. */
+moe_status moe_combine_f32(const moe_shape* shape, const float* expert_out,
+                           int64_t expert_out_rows, const int32_t* topk_idx,
+                           const float* topk_weights, const int32_t* send_idx,
+                           const int32_t* put_offset, const int64_t* rank_recv_base,
+                           void* out, int32_t* dev_status, void* stream);
+
 /* GMM1 epilogue with per-expert weight scales (section 4.3 stage 2,
  * DeqSwigluQuant): as moe_swiglu_quant, except that row m uses
  * weight_scale + g*2I for the expert g with group_off[g] <= m <

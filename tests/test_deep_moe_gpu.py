@@ -128,11 +128,50 @@ def test_grouped_gemm_rejects_bad_shapes(ep):
     del a
 
 
+def _dequant_bits(oracle, ref, ws2, I):
+    """GMM2's dequantised rows, (fp32(acc2) * ws2[e]) * 1/scale of the
+    requantised row, as int32 bit patterns (numpy float32: one rounding per
+    product)."""
+    grp = np.searchsorted(ref["group_off"], ref["rows"], side="right") - 1
+    ts = oracle.row_inv_scale(ref["x2"], I)
+    y = (ref["acc2"].astype(np.float32) * ws2[grp]) * ts[:, None]
+    return y.astype(np.float32).view(np.int32)
+
+
+def test_grouped_gemm_dequant_epilogue(oracle_mod, ep):
+    rng = np.random.default_rng(9)
+    G, N, K, sizes = 3, 264, 200, (130, 0, 70)
+    M = sum(sizes)
+    dev = torch.device("cuda")
+    a = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    w = rng.integers(-127, 128, (G, N, K)).astype(np.int8)
+    cs = rng.uniform(0.5, 1.5, (G, N)).astype(np.float32) * 1e-3
+    rs_rows = np.zeros((M, 48), np.uint8)                   # scale at byte 20 of 48-byte rows
+    rs = rng.uniform(0.01, 0.1, M).astype(np.float32)
+    rs_rows[:, 20:24] = rs.view(np.uint8).reshape(M, 4)
+    a_bf = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    w_bf = torch.empty((G, N, K), dtype=torch.bfloat16, device=dev)
+    ep.moe_codes_to_bf16(torch.from_numpy(a.view(np.uint8)).to(dev), M, K, K, a_bf)
+    ep.moe_codes_to_bf16(torch.from_numpy(w.view(np.uint8)).to(dev), G * N, K, K, w_bf)
+    y = torch.full((M, N), -1.0, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ep.moe_grouped_gemm_i8_dequant(a_bf, w_bf, torch.tensor(sizes, dtype=torch.int32, device=dev),
+                                   torch.from_numpy(cs).to(dev),
+                                   (torch.from_numpy(rs_rows).to(dev), 20, 48), y, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    c = oracle_mod.grouped_gemm(a.view(np.uint8), off, w)
+    grp = np.searchsorted(off, np.arange(M), side="right") - 1
+    want = ((c.astype(np.float32) * cs[grp]) * rs[:, None]).astype(np.float32)
+    _eq("y", y.view(torch.int32), want.view(np.int32))
+
+
 def _deep_inputs(w, I, seed, device="cpu"):
     idx, wt = W.routing(w)
     x = W.tokens(w)
     w1, ws1, w2, ws2 = W.moe_weights(w.E, w.H, I, seed=seed, device=device)
-    return idx, wt, x, (w1, ws1 * 40.0, w2, ws2 * 40.0)
+    return idx, wt, x, (w1, ws1, w2, ws2)
 
 
 DEEP_CASES = [
@@ -167,8 +206,17 @@ def test_deep_moe_pipeline(oracle_mod, pl, w):
     _eq("group_off", b.group_off, ref["group_off"])
     _eq("acc1", b.acc1, ref["acc1"])
     _eq("x2", b.x2, ref["x2"])
-    _eq("acc2", b.acc2, ref["acc2"])
+    _eq("y2", b.y2.view(torch.int32), _dequant_bits(oracle_mod, ref, ws2.numpy(), I))
     _eq("out", b.out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"])
+    # DeqCombine on the int32 accumulators gives the same output
+    acc2 = torch.from_numpy(ref["acc2"]).to(dev)
+    b.out.zero_()
+    from combine_moe_dispatch_layout_gb300 import moe_deq_combine
+    moe_deq_combine(b.shape, acc2, ws2.to(dev), (b.x2, (I + 31) // 32 * 32, b.row2), idx_d,
+                    wt_d, b.send_idx, b.put_offset, b.rank_recv_base, b.out, b.dev_status)
+    assert b.status() == 0
+    _eq("out(int32 DeqCombine)", b.out.view(torch.int16).cpu().numpy().view(np.uint16),
+        ref["out"])
 
 
 def test_deep_moe_dsv3_size_sampled(oracle_mod, pl):
@@ -182,7 +230,6 @@ def test_deep_moe_dsv3_size_sampled(oracle_mod, pl):
     idx, wt = W.routing(w)
     x = W.tokens(w)
     w1, ws1, w2, ws2 = W.moe_weights(w.E, w.H, I, seed=31, device=dev)
-    ws1, ws2 = ws1 * 40.0, ws2 * 40.0
     b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype)
     wts = pl.DeepMoeWeights(w1, ws1, w2, ws2)
     pl.run_deep_moe(b, wts, x.to(dev), idx.to(dev), wt.to(dev))
@@ -198,6 +245,7 @@ def test_deep_moe_dsv3_size_sampled(oracle_mod, pl):
     assert st == 0
     n = toks.size * w.k
     acc2 = np.zeros((n, w.H), np.int32)
+    ws2_h = ws2.cpu().numpy()
     x2 = np.zeros((n, (I + 31) // 32 * 32 + 32), np.uint8)
     one = np.array([0, 1], np.int64)
     for i in range(n):
@@ -210,7 +258,9 @@ def test_deep_moe_dsv3_size_sampled(oracle_mod, pl):
         x2[i] = oracle_mod.swiglu_quant(a1, ws1[e].cpu().numpy(), ts)[0]
         _eq("x2 row", b.x2[int(row_ids[t, kk])], x2[i])
         acc2[i] = oracle_mod.grouped_gemm(x2[i:i + 1], one, w2[e].cpu().numpy()[None])[0]
-        _eq("acc2 row", b.acc2[int(row_ids[t, kk])], acc2[i])
+        y = (acc2[i].astype(np.float32) * ws2_h[e]) * oracle_mod.row_inv_scale(x2[i:i + 1], I)[0]
+        _eq("y2 row", b.y2[int(row_ids[t, kk])].view(torch.int32),
+            y.astype(np.float32).view(np.int32))
     out, st = oracle_mod.deq_combine(acc2, ws2.cpu().numpy(), oracle_mod.row_inv_scale(x2, I),
                                      idx_n, wt_n, L["send_idx"], N["put_offset"],
                                      N["rank_recv_base"], w.R, w.epr, w.dtype, tokens=toks)

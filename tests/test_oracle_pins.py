@@ -631,8 +631,6 @@ def check_deep_moe(oracle, seed=13):
     idx, wt = idx.numpy(), wt.numpy()
     x = W.tokens(wl)
     w1, ws1, w2, ws2 = (t.numpy() for t in W.moe_weights(R * epr, H, I, seed=seed))
-    ws1 = ws1 * 40.0                           # gate values of order 1
-    ws2 = ws2 * 40.0
     res = oracle.deep_moe(W.bits(x), idx, wt, R, epr, 0, w1, ws1, w2, ws2)
     # expert groups: the exclusive prefix of the per-expert row counts
     L = oracle.layout(idx, R, epr)

@@ -193,17 +193,20 @@ def gmm1_accumulators(M: int, I: int, seed: int = 99):
 def moe_weights(E: int, H: int, I: int, seed: int = 7, device="cpu"):
     """Synthetic INT8 expert weights for the fused deep MoE: w1 int8
     [E, 2I, H] (rows 0..I-1 gate, I..2I-1 up; row n = output column n),
-    w2 int8 [E, H, I], codes uniform in [-127, 127]; per-output-column
-    weight scales ws1 [E, 2I] and ws2 [E, H] ~ U(0.5, 1.5) * 1e-4 (fp32).
-    Drawn with a generator on ``device`` (CPU and CUDA streams differ)."""
+    w2 int8 [E, H, I], codes uniform in [-127, 127] (standard deviation
+    ~73.6); per-output-column weight scales ws1 [E, 2I] = U(0.5, 1.5) /
+    (73.6 sqrt(H)) and ws2 [E, H] = U(0.5, 1.5) / (73.6 sqrt(I)) (fp32), so
+    that a unit-variance input gives gate / up / output values of order one
+    whatever the sizes.  Drawn with a generator on ``device`` (CPU and CUDA
+    streams differ)."""
     g = torch.Generator(device=device)
     g.manual_seed(seed * 16 + 8)
     w1 = torch.randint(-127, 128, (E, 2 * I, H), generator=g, dtype=torch.int8,
                        device=device)
     w2 = torch.randint(-127, 128, (E, H, I), generator=g, dtype=torch.int8,
                        device=device)
-    ws1 = (torch.rand((E, 2 * I), generator=g, device=device) + 0.5) * 1e-4
-    ws2 = (torch.rand((E, H), generator=g, device=device) + 0.5) * 1e-4
+    ws1 = (torch.rand((E, 2 * I), generator=g, device=device) + 0.5) / (73.6 * H ** 0.5)
+    ws2 = (torch.rand((E, H), generator=g, device=device) + 0.5) / (73.6 * I ** 0.5)
     return w1, ws1.float(), w2, ws2.float()
 
 
