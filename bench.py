@@ -493,8 +493,8 @@ def run_deep_moe_bench(args, w, ep, pl, x, idx, wt, stream, dev, flush):
     del w1, w2
     b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype, device=dev)
     P, H = w.P, w.H
-    names = ["layout+notify", "dispatch", "offsets+a1_bf16", "gemm1", "swiglu_quant",
-             "a2_bf16", "gemm2+dequant", "combine_f32"]
+    names = ["layout+notify", "dispatch_expand", "group_offsets", "gemm1",
+             "swiglu_quant_bf16", "gemm2+dequant", "combine_f32"]
 
     def step(evs=None):
         def mark(j):
@@ -503,26 +503,21 @@ def run_deep_moe_bench(args, w, ep, pl, x, idx, wt, stream, dev, flush):
         mark(0)
         pl.run_layout_notify(b, idx, stream)
         mark(1)
-        pl.run_dispatch(b, x, idx, stream)
+        pl.run_dispatch_expand(b, x, idx, stream)
         mark(2)
         ep.moe_group_offsets(b.recv_per_expert, b.group_off, b.dev_status, stream)
-        ep.moe_codes_to_bf16(b.recv, P, b.row_bytes, H, b.a1, stream)
         mark(3)
         ep.moe_grouped_gemm_i8(b.a1, wts.w1, b.recv_per_expert, b.acc1, b.dev_status,
                                stream)
         mark(4)
-        ep.moe_swiglu_quant_grouped(b.acc1, wts.ws1, b.group_off,
-                                    (b.recv, (H + 31) // 32 * 32, b.row_bytes), b.x2,
-                                    b.dev_status, stream)
+        ep.moe_swiglu_quant_grouped_bf16(b.acc1, wts.ws1, b.group_off, (b.ts1, 0, 4), b.a2,
+                                         b.ts2, b.dev_status, stream)
         mark(5)
-        ep.moe_codes_to_bf16(b.x2, P, b.row2, I, b.a2, stream)
-        mark(6)
         ep.moe_grouped_gemm_i8_dequant(b.a2, wts.w2, b.recv_per_expert, wts.ws2,
-                                       (b.x2, (I + 31) // 32 * 32, b.row2), b.y2,
-                                       b.dev_status, stream)
+                                       (b.ts2, 0, 4), b.y2, b.dev_status, stream)
+        mark(6)
+        pl.run_deep_combine(b, idx, wt, stream)
         mark(7)
-        pl.run_deq_combine(b, wts, idx, wt, stream)
-        mark(8)
 
     for i in range(3):
         step()
@@ -533,13 +528,14 @@ def run_deep_moe_bench(args, w, ep, pl, x, idx, wt, stream, dev, flush):
     all_evs = []
     for i in range(n):
         flush.fill_(i & 0xff)
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(9)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
         step(evs)
         all_evs.append(evs)
     torch.cuda.synchronize()
     if b.status() != 0:
         raise RuntimeError("device status %d in the deep MoE" % b.status())
-    st_ms = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(8)] for e in all_evs])
+    st_ms = np.array([[e[j].elapsed_time(e[j + 1]) for j in range(len(names))]
+                      for e in all_evs])
     mean = st_ms.mean(axis=0)
     burst, sustained, src = measured_bf16_tflops()
     flops1 = 2.0 * P * H * 2 * I
@@ -558,7 +554,7 @@ def run_deep_moe_bench(args, w, ep, pl, x, idx, wt, stream, dev, flush):
         "tokens_per_s": w.T / (mean.sum() * 1e-3),
         "stages_us": {nm: float(mean[j] * 1e3) for j, nm in enumerate(names)},
         "gemm1": gemm(flops1, float(mean[3])),
-        "gemm2": gemm(flops2, float(mean[6])),
+        "gemm2": gemm(flops2, float(mean[5])),
         "steps": n,
     }
     del b, wts

@@ -83,12 +83,16 @@ def _load():
     L.moe_grouped_gemm_i8_dequant.argtypes = [vp, i64, ctypes.c_int32, vp, ctypes.c_int32,
                                               ctypes.c_int32, vp, vp, vp, i64, vp, vp, vp]
     L.moe_combine_f32.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_dispatch_expand.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp]
+    L.moe_swiglu_quant_grouped_bf16.argtypes = [vp, i64, ctypes.c_int32, vp, vp,
+                                                ctypes.c_int32, vp, i64, vp, vp, vp, vp]
     for name in ("moe_dispatch_layout", "moe_notify_dispatch", "moe_dispatch",
                  "moe_combine", "moe_combine_quant", "moe_token_layout",
                  "moe_dispatch_fused", "moe_swiglu_quant", "moe_group_offsets",
                  "moe_codes_to_bf16", "moe_grouped_gemm_i8",
                  "moe_swiglu_quant_grouped", "moe_deq_combine",
-                 "moe_grouped_gemm_i8_dequant", "moe_combine_f32"):
+                 "moe_grouped_gemm_i8_dequant", "moe_combine_f32",
+                 "moe_dispatch_expand", "moe_swiglu_quant_grouped_bf16"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -457,3 +461,43 @@ def moe_combine_f32(shape, expert_out, topk_idx, topk_weights, send_idx, put_off
         _ptr(out, None, T * H, "out"), _ptr(dev_status, torch.int32, 1, "dev_status"),
         _stream(stream))
     return _check(st, "moe_combine_f32")
+
+
+def moe_dispatch_expand(shape, x, topk_idx, send_idx, put_offset, rank_recv_base,
+                        expand_x, dynamic_scale, capacity_rows, dev_status, stream=None):
+    """Dispatch with INT8 quantisation into bf16-valued codes expand_x
+    [capacity_rows, H] and a packed fp32 1/scale per row."""
+    T, k, H = shape.R * shape.bs, shape.k, shape.H
+    E = shape.R * shape.experts_per_rank
+    st = _lib.moe_dispatch_expand(
+        ctypes.byref(shape), _ptr(x, None, T * H, "x"),
+        _ptr(topk_idx, torch.int32, T * k, "topk_idx"),
+        _ptr(send_idx, torch.int32, T * k, "send_idx"),
+        _ptr(put_offset, torch.int32, E * shape.R, "put_offset"),
+        _ptr(rank_recv_base, torch.int64, shape.R + 1, "rank_recv_base"),
+        _ptr(expand_x, torch.bfloat16, capacity_rows * H, "expand_x"),
+        _ptr(dynamic_scale, torch.float32, capacity_rows, "dynamic_scale"),
+        int(capacity_rows), _ptr(dev_status, torch.int32, 1, "dev_status"),
+        _stream(stream))
+    return _check(st, "moe_dispatch_expand")
+
+
+def moe_swiglu_quant_grouped_bf16(acc, weight_scale, group_off, token_scale, codes,
+                                  inv_scale, dev_status, stream=None):
+    """Grouped GMM1 epilogue writing bf16-valued codes [M, I] and a packed
+    fp32 1/scale per row; token_scale is (tensor, byte_offset, byte_stride)."""
+    if acc.dim() != 2 or acc.shape[1] % 2 or weight_scale.dim() != 2:
+        raise ValueError("acc must be [M, 2I] and weight_scale [G, 2I]")
+    M, I = acc.shape[0], acc.shape[1] // 2
+    G = weight_scale.shape[0]
+    if weight_scale.shape[1] != 2 * I or group_off.numel() != G + 1:
+        raise ValueError("weight_scale / group_off do not match acc")
+    tp, tstride = _strided(token_scale, M, "token_scale")
+    st = _lib.moe_swiglu_quant_grouped_bf16(
+        _ptr(acc, torch.int32, M * 2 * I, "acc"), int(M), int(I),
+        _ptr(weight_scale, torch.float32, G * 2 * I, "weight_scale"),
+        _ptr(group_off, torch.int64, G + 1, "group_off"), int(G), tp, tstride,
+        _ptr(codes, torch.bfloat16, M * I, "codes"),
+        _ptr(inv_scale, torch.float32, M, "inv_scale"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_swiglu_quant_grouped_bf16")

@@ -248,8 +248,50 @@ moe_status moe_swiglu_quant_grouped(const int32_t* acc, int64_t M, int32_t I,
       !aligned(token_scale, 4) || !aligned(out, 16) || !aligned(dev_status, 4))
     return MOE_ERR_INVALID_ARG;
   return from_cuda(moe_ep::launch_swiglu_quant_grouped(
-      acc, M, I, weight_scale, group_off, G, token_scale, token_scale_stride, out,
+      acc, M, I, weight_scale, group_off, G, token_scale, token_scale_stride, out, nullptr,
       static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_swiglu_quant_grouped_bf16(const int32_t* acc, int64_t M, int32_t I,
+                                         const float* weight_scale, const int64_t* group_off,
+                                         int32_t G, const void* token_scale,
+                                         int64_t token_scale_stride, void* codes,
+                                         float* inv_scale, int32_t* dev_status,
+                                         void* stream) {
+  if (M < 0 || I < 8 || I > 16384 || I % 8 != 0 || G < 1 || G > MOE_EP_MAX_EXPERTS ||
+      token_scale_stride < 4 || token_scale_stride % 4 != 0 || !dev_status)
+    return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  if (!acc || !weight_scale || !group_off || !token_scale || !codes || !inv_scale)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(acc, 16) || !aligned(weight_scale, 16) || !aligned(group_off, 8) ||
+      !aligned(token_scale, 4) || !aligned(codes, 16) || !aligned(inv_scale, 4) ||
+      !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_swiglu_quant_grouped(
+      acc, M, I, weight_scale, group_off, G, token_scale, token_scale_stride, codes,
+      inv_scale, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_dispatch_expand(const moe_shape* shape, const void* x,
+                               const int32_t* topk_idx, const int32_t* send_idx,
+                               const int32_t* put_offset, const int64_t* rank_recv_base,
+                               void* expand_x, float* dynamic_scale,
+                               int64_t capacity_rows, int32_t* dev_status, void* stream) {
+  Shape s;
+  if (!valid_shape(shape, &s)) return MOE_ERR_INVALID_ARG;
+  if (capacity_rows < 0 || !dev_status) return MOE_ERR_INVALID_ARG;
+  if (s.T() == 0) return MOE_OK;
+  if (!x || !topk_idx || !send_idx || !put_offset || !rank_recv_base ||
+      (capacity_rows > 0 && (!expand_x || !dynamic_scale)))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(expand_x, 16) || !aligned(dynamic_scale, 4) ||
+      !aligned(topk_idx, 4) || !aligned(send_idx, 4) || !aligned(put_offset, 4) ||
+      !aligned(rank_recv_base, 8) || !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_dispatch_expand(
+      s, x, topk_idx, send_idx, put_offset, rank_recv_base, expand_x, dynamic_scale,
+      capacity_rows, dev_status, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_codes_to_bf16(const void* codes, int64_t rows, int64_t row_stride, int32_t K,

@@ -26,6 +26,11 @@
 // of (f * scale) (one fp32 multiply, then cvt.rni); |q| <= 127, so the
 // page's int32 -> int16 -> int8 casts are exact.  1/scale (IEEE divide) goes
 // to byte align32(H) of the row, every other byte after the codes is zero.
+//
+// Expand variant (the fused deep MoE's stage-1 outputs, section 4.3:
+// expand_x [M, h] and dynamic_scale [M] as separate arrays): the same codes,
+// written as bf16 values (exact) so the tensor-core GEMM reads them directly,
+// and 1/scale into a packed fp32 array at the row's index.
 #include <algorithm>
 
 #include "moe_ep_internal.cuh"
@@ -69,6 +74,8 @@ struct SmemLayout {
   int bytes;       // total dynamic shared memory
 };
 
+// row_bytes: bytes of one output row image (INT8: align32(H) + 32; expand:
+// 2H bf16 codes; verbatim: 2H).
 __host__ __device__ inline SmemLayout smem_layout(int H, int64_t row_bytes, int stages,
                                                   bool quant) {
   SmemLayout L;
@@ -81,7 +88,9 @@ __host__ __device__ inline SmemLayout smem_layout(int H, int64_t row_bytes, int 
 // ---------------------------------------------------------------------------
 // INT8 path
 // ---------------------------------------------------------------------------
-template <int DT, int S>
+// EXPAND: the codes go out as bf16 values (2H bytes per row) and 1/scale to
+// dyn_scale[row]; otherwise the INT8 row image of row_bytes bytes.
+template <int DT, int S, bool EXPAND>
 __global__ void __launch_bounds__(kMaxThreads)
 dispatch_quant_kernel(const unsigned char* __restrict__ x,
                       const int32_t* __restrict__ topk_idx,
@@ -90,7 +99,8 @@ dispatch_quant_kernel(const unsigned char* __restrict__ x,
                       const int64_t* __restrict__ rank_recv_base, int R, int bs,
                       int k, int epr, int H, int64_t T,
                       unsigned char* __restrict__ recv, int64_t row_bytes,
-                      int64_t capacity, int32_t* dev_status) {
+                      float* __restrict__ dyn_scale, int64_t capacity,
+                      int32_t* dev_status) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int64_t s_rows[2][MOE_EP_MAX_TOPK];
   __shared__ float s_wmax[32];
@@ -179,18 +189,34 @@ dispatch_quant_kernel(const unsigned char* __restrict__ x,
         const uint4 v = *reinterpret_cast<const uint4*>(xs + c * 16);
         float f[8];
         unpack8<DT>(v, f);
-        uint32_t w2[2] = {0u, 0u};
+        if (EXPAND) {   // q as bf16: exact (|q| <= 127 has at most 7 significant bits)
+          uint32_t w4[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int q = __float2int_rn(__fmul_rn(f[j], scale));
-          w2[j >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (j & 3));
+          for (int j = 0; j < 4; ++j) {
+            const float q0 = static_cast<float>(__float2int_rn(__fmul_rn(f[2 * j], scale)));
+            const float q1 = static_cast<float>(__float2int_rn(__fmul_rn(f[2 * j + 1], scale)));
+            w4[j] = (__float_as_uint(q0) >> 16) | (__float_as_uint(q1) & 0xffff0000u);
+          }
+          *reinterpret_cast<uint4*>(os + c * 16) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        } else {
+          uint32_t w2[2] = {0u, 0u};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int q = __float2int_rn(__fmul_rn(f[j], scale));
+            w2[j >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (j & 3));
+          }
+          *reinterpret_cast<uint2*>(os + c * 8) = make_uint2(w2[0], w2[1]);
         }
-        *reinterpret_cast<uint2*>(os + c * 8) = make_uint2(w2[0], w2[1]);
       }
-      // zero pad to align32(H), fp32 1/scale, zero pad to the row end
-      if (tid < ntail)
+      if (EXPAND) {   // 1/scale of this token into each of its k rows' slots
+        for (int kk = tid; kk < k; kk += ncomp) {
+          const int64_t row = s_rows[it & 1][kk];
+          if (row >= 0) dyn_scale[row] = inv;
+        }
+      } else if (tid < ntail) {   // zero pad to align32(H), fp32 1/scale, zero pad
         *reinterpret_cast<uint2*>(os + H + 8 * tid) =
             make_uint2(tid == inv_word ? __float_as_uint(inv) : 0u, 0u);
+      }
       fence_proxy_async_smem();
     }
     __syncthreads();   // (B) the image is complete; x stage b may be refilled
@@ -308,23 +334,39 @@ cudaError_t launch_persistent(Kernel kernel, int threads, int smem, int64_t T,
   return cudaSuccess;
 }
 
-template <int DT, int S>
+template <int DT, int S, bool EXPAND>
 cudaError_t launch_quant(const Shape& s, const void* x, const int32_t* topk_idx,
                          const int32_t* send_idx, const int32_t* put_offset,
                          const int64_t* rank_recv_base, void* recv, int64_t row_bytes,
-                         int64_t capacity, int32_t* dev_status, cudaStream_t st) {
+                         float* dyn_scale, int64_t capacity, int32_t* dev_status,
+                         cudaStream_t st) {
   const int nch = s.H / 8;
   const int ncomp = std::max(32, std::min(kMaxThreads - 32, ((nch + 3) / 4 + 31) / 32 * 32));
   const int threads = ncomp + 32;
   const int smem = smem_layout(s.H, row_bytes, S, true).bytes;
   int grid = 0;
-  cudaError_t e = launch_persistent(dispatch_quant_kernel<DT, S>, threads, smem, s.T(), &grid);
+  cudaError_t e =
+      launch_persistent(dispatch_quant_kernel<DT, S, EXPAND>, threads, smem, s.T(), &grid);
   if (e != cudaSuccess) return e;
-  dispatch_quant_kernel<DT, S><<<grid, threads, smem, st>>>(
+  dispatch_quant_kernel<DT, S, EXPAND><<<grid, threads, smem, st>>>(
       static_cast<const unsigned char*>(x), topk_idx, send_idx, put_offset,
       rank_recv_base, s.R, s.bs, s.k, s.epr, s.H, s.T(),
-      static_cast<unsigned char*>(recv), row_bytes, capacity, dev_status);
+      static_cast<unsigned char*>(recv), row_bytes, dyn_scale, capacity, dev_status);
   return cudaGetLastError();
+}
+
+template <int DT, bool EXPAND>
+cudaError_t launch_quant_stages(const Shape& s, const void* x, const int32_t* topk_idx,
+                                const int32_t* send_idx, const int32_t* put_offset,
+                                const int64_t* rank_recv_base, void* recv,
+                                int64_t row_bytes, float* dyn_scale, int64_t capacity,
+                                int32_t* dev_status, cudaStream_t st) {
+  // two stages (prefetch one token ahead) unless the rows are too wide
+  if (smem_layout(s.H, row_bytes, 2, true).bytes <= kSmemBudget)
+    return launch_quant<DT, 2, EXPAND>(s, x, topk_idx, send_idx, put_offset, rank_recv_base,
+                                       recv, row_bytes, dyn_scale, capacity, dev_status, st);
+  return launch_quant<DT, 1, EXPAND>(s, x, topk_idx, send_idx, put_offset, rank_recv_base,
+                                     recv, row_bytes, dyn_scale, capacity, dev_status, st);
 }
 
 template <int S>
@@ -353,26 +395,37 @@ cudaError_t launch_dispatch(const Shape& s, const void* x,
                             int64_t capacity_rows, int32_t* dev_status,
                             cudaStream_t st) {
   if (s.T() == 0) return cudaSuccess;
-  // two stages (prefetch one token ahead) unless the rows are too wide
-  const bool two = smem_layout(s.H, row_bytes, 2, quant).bytes <= kSmemBudget;
-  if (!quant)
+  if (!quant) {
+    // two stages (prefetch one token ahead) unless the rows are too wide
+    const bool two = smem_layout(s.H, row_bytes, 2, false).bytes <= kSmemBudget;
     return two ? launch_copy<2>(s, x, topk_idx, send_idx, put_offset, rank_recv_base,
                                 recv, row_bytes, capacity_rows, dev_status, st)
                : launch_copy<1>(s, x, topk_idx, send_idx, put_offset, rank_recv_base,
                                 recv, row_bytes, capacity_rows, dev_status, st);
+  }
   if (s.dtype == MOE_BF16)
-    return two ? launch_quant<MOE_BF16, 2>(s, x, topk_idx, send_idx, put_offset,
-                                           rank_recv_base, recv, row_bytes,
-                                           capacity_rows, dev_status, st)
-               : launch_quant<MOE_BF16, 1>(s, x, topk_idx, send_idx, put_offset,
-                                           rank_recv_base, recv, row_bytes,
-                                           capacity_rows, dev_status, st);
-  return two ? launch_quant<MOE_FP16, 2>(s, x, topk_idx, send_idx, put_offset,
-                                         rank_recv_base, recv, row_bytes, capacity_rows,
-                                         dev_status, st)
-             : launch_quant<MOE_FP16, 1>(s, x, topk_idx, send_idx, put_offset,
-                                         rank_recv_base, recv, row_bytes, capacity_rows,
-                                         dev_status, st);
+    return launch_quant_stages<MOE_BF16, false>(s, x, topk_idx, send_idx, put_offset,
+                                                rank_recv_base, recv, row_bytes, nullptr,
+                                                capacity_rows, dev_status, st);
+  return launch_quant_stages<MOE_FP16, false>(s, x, topk_idx, send_idx, put_offset,
+                                              rank_recv_base, recv, row_bytes, nullptr,
+                                              capacity_rows, dev_status, st);
+}
+
+cudaError_t launch_dispatch_expand(const Shape& s, const void* x, const int32_t* topk_idx,
+                                   const int32_t* send_idx, const int32_t* put_offset,
+                                   const int64_t* rank_recv_base, void* expand_x,
+                                   float* dyn_scale, int64_t capacity_rows,
+                                   int32_t* dev_status, cudaStream_t st) {
+  if (s.T() == 0) return cudaSuccess;
+  const int64_t row_bytes = int64_t(s.H) * 2;
+  if (s.dtype == MOE_BF16)
+    return launch_quant_stages<MOE_BF16, true>(s, x, topk_idx, send_idx, put_offset,
+                                               rank_recv_base, expand_x, row_bytes, dyn_scale,
+                                               capacity_rows, dev_status, st);
+  return launch_quant_stages<MOE_FP16, true>(s, x, topk_idx, send_idx, put_offset,
+                                             rank_recv_base, expand_x, row_bytes, dyn_scale,
+                                             capacity_rows, dev_status, st);
 }
 
 }  // namespace moe_ep

@@ -241,7 +241,13 @@ cudaError_t launch_swiglu_quant_grouped(const int32_t* acc, int64_t M, int I,
                                         const float* weight_scale, const int64_t* group_off,
                                         int G, const void* token_scale,
                                         int64_t token_scale_stride, void* out,
-                                        cudaStream_t st);
+                                        float* out_scale, cudaStream_t st);
+
+cudaError_t launch_dispatch_expand(const Shape& s, const void* x, const int32_t* topk_idx,
+                                   const int32_t* send_idx, const int32_t* put_offset,
+                                   const int64_t* rank_recv_base, void* expand_x,
+                                   float* dyn_scale, int64_t capacity_rows,
+                                   int32_t* dev_status, cudaStream_t st);
 
 cudaError_t launch_codes_to_bf16(const void* src, int64_t rows, int64_t stride, int K,
                                  void* dst, cudaStream_t st);

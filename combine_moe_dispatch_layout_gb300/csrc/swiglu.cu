@@ -72,10 +72,14 @@ struct ScaleSrc {
   int64_t ts_stride;          // bytes
 };
 
-template <int kCpt>
+// BF16OUT: the codes go out as bf16 values (exact; 2I bytes per row, the
+// next GEMM's operand) and 1/scale to out_scale[m]; otherwise the INT8 row
+// image of row_bytes bytes.
+template <int kCpt, bool BF16OUT>
 __global__ void __launch_bounds__(kMaxThreads)
 swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc sc,
-                    unsigned char* __restrict__ out, int64_t row_bytes) {
+                    unsigned char* __restrict__ out, int64_t row_bytes,
+                    float* __restrict__ out_scale) {
   __shared__ float s_wmax[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nwarps = nthreads / 32;
@@ -155,34 +159,50 @@ swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc 
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           b[j] = __float_as_uint(__fadd_rn(__fmul_rn(h[i][j], scale), kRoundMagic));
-        const uint32_t w0 = __byte_perm(__byte_perm(b[0], b[1], 0x0040),
-                                        __byte_perm(b[2], b[3], 0x0040), 0x5410);
-        const uint32_t w1 = __byte_perm(__byte_perm(b[4], b[5], 0x0040),
-                                        __byte_perm(b[6], b[7], 0x0040), 0x5410);
-        *reinterpret_cast<uint2*>(dst + 8 * c) = make_uint2(w0, w1);
+        if (BF16OUT) {   // q itself (exact subtraction), then its bf16 bits (exact)
+          uint32_t w4[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float q0 = __fsub_rn(__uint_as_float(b[2 * j]), kRoundMagic);
+            const float q1 = __fsub_rn(__uint_as_float(b[2 * j + 1]), kRoundMagic);
+            w4[j] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632);
+          }
+          *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        } else {
+          const uint32_t w0 = __byte_perm(__byte_perm(b[0], b[1], 0x0040),
+                                          __byte_perm(b[2], b[3], 0x0040), 0x5410);
+          const uint32_t w1 = __byte_perm(__byte_perm(b[4], b[5], 0x0040),
+                                          __byte_perm(b[6], b[7], 0x0040), 0x5410);
+          *reinterpret_cast<uint2*>(dst + 8 * c) = make_uint2(w0, w1);
+        }
       }
     }
-    if (tid < ntail)
+    if (BF16OUT) {
+      if (tid == 0) out_scale[m] = inv;
+    } else if (tid < ntail) {
       *reinterpret_cast<uint2*>(dst + I + 8 * tid) =
           make_uint2(tid == inv_word ? __float_as_uint(inv) : 0u, 0u);
+    }
     __syncthreads();   // s_wmax is rewritten for the next row
   }
 }
 
-template <int kCpt>
+template <int kCpt, bool BF16OUT>
 cudaError_t launch_t(const int32_t* acc, int64_t M, int I, const ScaleSrc& sc, void* out,
-                     cudaStream_t st) {
+                     float* out_scale, cudaStream_t st) {
   const int nch = I / 8;
   const int threads = std::max(32, std::min(kMaxThreads, ((nch + kCpt - 1) / kCpt + 31) / 32 * 32));
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, swiglu_quant_kernel<kCpt>, threads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, swiglu_quant_kernel<kCpt, BF16OUT>, threads, 0);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(M, int64_t(std::max(1, per_sm)) * sms);
-  swiglu_quant_kernel<kCpt><<<static_cast<unsigned>(grid), threads, 0, st>>>(
-      acc, M, I, sc, static_cast<unsigned char*>(out), align_up(I, 32) + 32);
+  swiglu_quant_kernel<kCpt, BF16OUT><<<static_cast<unsigned>(grid), threads, 0, st>>>(
+      acc, M, I, sc, static_cast<unsigned char*>(out),
+      BF16OUT ? int64_t(I) * 2 : align_up(I, 32) + 32, out_scale);
   return cudaGetLastError();
 }
 
@@ -194,20 +214,23 @@ cudaError_t launch_swiglu_quant(const int32_t* acc, int64_t M, int I,
   if (M == 0) return cudaSuccess;
   const ScaleSrc sc{weight_scale, nullptr, 1,
                     reinterpret_cast<const unsigned char*>(token_scale), 4};
-  return I / 8 <= 2 * kMaxThreads ? launch_t<2>(acc, M, I, sc, out, st)
-                                  : launch_t<4>(acc, M, I, sc, out, st);
+  return I / 8 <= 2 * kMaxThreads ? launch_t<2, false>(acc, M, I, sc, out, nullptr, st)
+                                  : launch_t<4, false>(acc, M, I, sc, out, nullptr, st);
 }
 
 cudaError_t launch_swiglu_quant_grouped(const int32_t* acc, int64_t M, int I,
                                         const float* weight_scale, const int64_t* group_off,
                                         int G, const void* token_scale,
                                         int64_t token_scale_stride, void* out,
-                                        cudaStream_t st) {
+                                        float* out_scale, cudaStream_t st) {
   if (M == 0) return cudaSuccess;
   const ScaleSrc sc{weight_scale, group_off, G,
                     static_cast<const unsigned char*>(token_scale), token_scale_stride};
-  return I / 8 <= 2 * kMaxThreads ? launch_t<2>(acc, M, I, sc, out, st)
-                                  : launch_t<4>(acc, M, I, sc, out, st);
+  if (out_scale)
+    return I / 8 <= 2 * kMaxThreads ? launch_t<2, true>(acc, M, I, sc, out, out_scale, st)
+                                    : launch_t<4, true>(acc, M, I, sc, out, out_scale, st);
+  return I / 8 <= 2 * kMaxThreads ? launch_t<2, false>(acc, M, I, sc, out, nullptr, st)
+                                  : launch_t<4, false>(acc, M, I, sc, out, nullptr, st);
 }
 
 }  // namespace moe_ep

@@ -11,9 +11,10 @@ import torch
 
 from . import (fused_workspace_bytes, make_shape, layout_workspace_bytes,
                moe_codes_to_bf16, moe_combine, moe_combine_f32, moe_combine_quant,
-               moe_dispatch, moe_dispatch_fused, moe_dispatch_layout,
-               moe_group_offsets, moe_grouped_gemm_i8, moe_grouped_gemm_i8_dequant,
-               moe_notify_dispatch, moe_swiglu_quant_grouped, recv_row_bytes)
+               moe_dispatch, moe_dispatch_expand, moe_dispatch_fused,
+               moe_dispatch_layout, moe_group_offsets, moe_grouped_gemm_i8,
+               moe_grouped_gemm_i8_dequant, moe_notify_dispatch,
+               moe_swiglu_quant_grouped_bf16, recv_row_bytes)
 
 
 class PipelineBuffers:
@@ -126,43 +127,45 @@ class DeepMoeWeights:
 
 
 class DeepMoeBuffers(PipelineBuffers):
-    """PipelineBuffers (INT8 dispatch) plus the deep MoE's intermediates,
-    all sized for T*k rows: bf16 GEMM operands, GMM1's int32 accumulators,
-    the GMM1 epilogue's INT8 row images, GMM2's dequantised fp32 outputs and
-    the expert row offsets."""
+    """PipelineBuffers plus the deep MoE's intermediates, all sized for T*k
+    rows: the dispatched codes as bf16 (expand_x) and their 1/scale, GMM1's
+    int32 accumulators, the requantised codes as bf16 and their 1/scale,
+    GMM2's dequantised fp32 outputs, and the expert row offsets."""
 
     def __init__(self, R, bs, k, epr, H, I, dtype, device="cuda"):
         super().__init__(R, bs, k, epr, H, dtype, True, device)
         P = R * bs * k
         self.I = I
+        f32 = dict(dtype=torch.float32, device=device)
         self.group_off = torch.empty((R * epr + 1,), dtype=torch.int64, device=device)
         self.a1 = torch.empty((P, H), dtype=torch.bfloat16, device=device)
+        self.ts1 = torch.empty((P,), **f32)
         self.acc1 = torch.empty((P, 2 * I), dtype=torch.int32, device=device)
-        self.row2 = _align32(I) + 32
-        self.x2 = torch.empty((P, self.row2), dtype=torch.uint8, device=device)
         self.a2 = torch.empty((P, I), dtype=torch.bfloat16, device=device)
-        self.y2 = torch.empty((P, H), dtype=torch.float32, device=device)
+        self.ts2 = torch.empty((P,), **f32)
+        self.y2 = torch.empty((P, H), **f32)
+
+
+def run_dispatch_expand(b, x, topk_idx, stream=None):
+    """Stage 1: INT8 quantisation into bf16-valued codes and packed 1/scale."""
+    moe_dispatch_expand(b.shape, x, topk_idx, b.send_idx, b.put_offset, b.rank_recv_base,
+                        b.a1, b.ts1, b.capacity, b.dev_status, stream)
 
 
 def run_deep_moe_experts(b, wts, stream=None):
-    """From the dispatched INT8 rows in ``b.recv`` to the dequantised expert
-    outputs ``b.y2`` (GMM1, DeqSwigluQuant, GMM2 with its dequantising
-    epilogue)."""
-    P, H, I = b.capacity, b.shape.H, b.I
+    """Stages 2-3 up to the dequantised expert outputs ``b.y2``: GMM1,
+    DeqSwigluQuant (per-expert scales, the dispatched rows' 1/scale), GMM2
+    with its dequantising epilogue."""
     moe_group_offsets(b.recv_per_expert, b.group_off, b.dev_status, stream)
-    moe_codes_to_bf16(b.recv, P, b.row_bytes, H, b.a1, stream)
     moe_grouped_gemm_i8(b.a1, wts.w1, b.recv_per_expert, b.acc1, b.dev_status, stream)
-    moe_swiglu_quant_grouped(b.acc1, wts.ws1, b.group_off,
-                             (b.recv, _align32(H), b.row_bytes), b.x2, b.dev_status,
-                             stream)
-    moe_codes_to_bf16(b.x2, P, b.row2, I, b.a2, stream)
-    moe_grouped_gemm_i8_dequant(b.a2, wts.w2, b.recv_per_expert, wts.ws2,
-                                (b.x2, _align32(I), b.row2), b.y2, b.dev_status, stream)
+    moe_swiglu_quant_grouped_bf16(b.acc1, wts.ws1, b.group_off, (b.ts1, 0, 4), b.a2,
+                                  b.ts2, b.dev_status, stream)
+    moe_grouped_gemm_i8_dequant(b.a2, wts.w2, b.recv_per_expert, wts.ws2, (b.ts2, 0, 4),
+                                b.y2, b.dev_status, stream)
 
 
-def run_deq_combine(b, wts, topk_idx, topk_weights, stream=None):
+def run_deep_combine(b, topk_idx, topk_weights, stream=None):
     """DeqCombine's remaining step: the weighted sum over the fp32 rows."""
-    del wts
     moe_combine_f32(b.shape, b.y2, topk_idx, topk_weights, b.send_idx, b.put_offset,
                     b.rank_recv_base, b.out, b.dev_status, stream)
 
@@ -170,6 +173,6 @@ def run_deq_combine(b, wts, topk_idx, topk_weights, stream=None):
 def run_deep_moe(b, wts, x, topk_idx, topk_weights, stream=None):
     """The whole deep MoE on one stream; the result is ``b.out``."""
     run_layout_notify(b, topk_idx, stream)
-    run_dispatch(b, x, topk_idx, stream)
+    run_dispatch_expand(b, x, topk_idx, stream)
     run_deep_moe_experts(b, wts, stream)
-    run_deq_combine(b, wts, topk_idx, topk_weights, stream)
+    run_deep_combine(b, topk_idx, topk_weights, stream)

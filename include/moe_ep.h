@@ -328,6 +328,31 @@ moe_status moe_grouped_gemm_i8(const void* a, int64_t a_rows, int32_t K, const v
                                int32_t G, int32_t N, const int32_t* group_rows, int32_t* c,
                                int32_t* dev_status, void* stream);
 
+/* Stage 1 of the fused deep MoE (section 4.3: "expand_x [M, h] (INT8)",
+ * "dynamic_scale [M]"): moe_dispatch's dynamic INT8 quantisation with the two
+ * outputs as separate arrays laid out for the tensor-core GEMM: the codes of
+ * each (token, k) pair's row written as bf16 values (exactly the int8 codes
+ * moe_dispatch writes, -127..127), and that row's 1/scale into
+ * dynamic_scale[row].  Row addressing, capacity and status as moe_dispatch.
+ *   expand_x       bf16 [capacity_rows][H], 16-byte aligned
+ *   dynamic_scale  fp32 [capacity_rows]
+ * One launch. */
+moe_status moe_dispatch_expand(const moe_shape* shape, const void* x,
+                               const int32_t* topk_idx, const int32_t* send_idx,
+                               const int32_t* put_offset, const int64_t* rank_recv_base,
+                               void* expand_x, float* dynamic_scale,
+                               int64_t capacity_rows, int32_t* dev_status, void* stream);
+
+/* moe_swiglu_quant_grouped with the requantised codes written as bf16 values
+ * (codes [M][I], exact) and each row's 1/scale to inv_scale[m], ready for the
+ * GMM2 GEMM; the values are those of the INT8 row images.  One launch. */
+moe_status moe_swiglu_quant_grouped_bf16(const int32_t* acc, int64_t M, int32_t I,
+                                         const float* weight_scale, const int64_t* group_off,
+                                         int32_t G, const void* token_scale,
+                                         int64_t token_scale_stride, void* codes,
+                                         float* inv_scale, int32_t* dev_status,
+                                         void* stream);
+
 /* moe_grouped_gemm_i8 with the GMM2 dequantisation of section 4.3 stage 3
  * ("Read INT32 -> Cast FP32 -> x weight_scale -> x per_token_scale") done
  * in the GEMM's epilogue registers: for row m of group g,

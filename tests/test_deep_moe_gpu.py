@@ -181,8 +181,14 @@ DEEP_CASES = [
 ]
 
 
+def _codes_bf16(images, K):
+    """bf16 bit patterns of the INT8 codes of row images (exact)."""
+    q = images[:, :K].view(np.int8).astype(np.float32)
+    return (q.view(np.uint32) >> 16).astype(np.uint16)
+
+
 @pytest.mark.parametrize("w", DEEP_CASES, ids=lambda w: w.name)
-def test_deep_moe_pipeline(oracle_mod, pl, w):
+def test_deep_moe_pipeline(oracle_mod, ep, pl, w):
     I = 136 if w.H > 512 else 128
     idx, wt, x, (w1, ws1, w2, ws2) = _deep_inputs(w, I, w.seed)
     ref = oracle_mod.deep_moe(W.bits(x), idx.numpy(), wt.numpy(), w.R, w.epr, w.dtype,
@@ -190,30 +196,46 @@ def test_deep_moe_pipeline(oracle_mod, pl, w):
     dev = torch.device("cuda")
     b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype)
     wts = pl.DeepMoeWeights(w1.to(dev), ws1.to(dev), w2.to(dev), ws2.to(dev))
-    idx_d, wt_d = idx.to(dev), wt.to(dev)
+    idx_d, wt_d, x_d = idx.to(dev), wt.to(dev), x.to(dev)
     pl.run_layout_notify(b, idx_d)
-    pl.run_dispatch(b, x.to(dev), idx_d)
+    pl.run_dispatch_expand(b, x_d, idx_d)
     assert b.status() == 0, "dispatch"
     L = oracle_mod.layout(idx.numpy(), w.R, w.epr)
     N = oracle_mod.notify(L["count"], w.R, w.bs, w.epr)
     recv, _ = oracle_mod.dispatch(W.bits(x), idx.numpy(), L["send_idx"], N["put_offset"],
                                   N["rank_recv_base"], w.R, w.epr, w.dtype, True)
-    _eq("recv", b.recv, recv)
+    _eq("expand_x", b.a1.view(torch.int16).cpu().numpy().view(np.uint16),
+        _codes_bf16(recv, w.H))
+    _eq("dynamic_scale", b.ts1.view(torch.int32), oracle_mod.row_inv_scale(recv, w.H).view(np.int32))
     pl.run_deep_moe_experts(b, wts)
     assert b.status() == 0, "experts"
-    pl.run_deq_combine(b, wts, idx_d, wt_d)
-    assert b.status() == 0, "deq_combine"
+    pl.run_deep_combine(b, idx_d, wt_d)
+    assert b.status() == 0, "combine"
     _eq("group_off", b.group_off, ref["group_off"])
     _eq("acc1", b.acc1, ref["acc1"])
-    _eq("x2", b.x2, ref["x2"])
+    _eq("a2 codes", b.a2.view(torch.int16).cpu().numpy().view(np.uint16),
+        _codes_bf16(ref["x2"], I))
+    _eq("a2 1/scale", b.ts2.view(torch.int32), oracle_mod.row_inv_scale(ref["x2"], I).view(np.int32))
     _eq("y2", b.y2.view(torch.int32), _dequant_bits(oracle_mod, ref, ws2.numpy(), I))
     _eq("out", b.out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"])
-    # DeqCombine on the int32 accumulators gives the same output
-    acc2 = torch.from_numpy(ref["acc2"]).to(dev)
+
+    # the INT8-row-image route gives the same intermediates and output
+    pl.run_dispatch(b, x_d, idx_d)                                 # b.recv: INT8 rows
+    _eq("recv", b.recv, recv)
+    a1 = torch.empty_like(b.a1)
+    ep.moe_codes_to_bf16(b.recv, b.capacity, b.row_bytes, w.H, a1)
+    _eq("codes_to_bf16(recv)", a1.view(torch.int16), b.a1.view(torch.int16).cpu().numpy())
+    row2 = (I + 31) // 32 * 32 + 32
+    x2 = torch.zeros((b.capacity, row2), dtype=torch.uint8, device=dev)
+    ep.moe_swiglu_quant_grouped(b.acc1, wts.ws1, b.group_off,
+                                (b.recv, (w.H + 31) // 32 * 32, b.row_bytes), x2, b.dev_status)
+    _eq("x2 images", x2, ref["x2"])
+    acc2 = torch.empty((b.capacity, w.H), dtype=torch.int32, device=dev)
+    ep.moe_grouped_gemm_i8(b.a2, wts.w2, b.recv_per_expert, acc2, b.dev_status)
+    _eq("acc2", acc2, ref["acc2"])
     b.out.zero_()
-    from combine_moe_dispatch_layout_gb300 import moe_deq_combine
-    moe_deq_combine(b.shape, acc2, ws2.to(dev), (b.x2, (I + 31) // 32 * 32, b.row2), idx_d,
-                    wt_d, b.send_idx, b.put_offset, b.rank_recv_base, b.out, b.dev_status)
+    ep.moe_deq_combine(b.shape, acc2, wts.ws2, (x2, (I + 31) // 32 * 32, row2), idx_d, wt_d,
+                       b.send_idx, b.put_offset, b.rank_recv_base, b.out, b.dev_status)
     assert b.status() == 0
     _eq("out(int32 DeqCombine)", b.out.view(torch.int16).cpu().numpy().view(np.uint16),
         ref["out"])
@@ -256,7 +278,11 @@ def test_deep_moe_dsv3_size_sampled(oracle_mod, pl):
         _eq("acc1 row", b.acc1[int(row_ids[t, kk])], a1[0])
         ts = oracle_mod.row_inv_scale(img, w.H)
         x2[i] = oracle_mod.swiglu_quant(a1, ws1[e].cpu().numpy(), ts)[0]
-        _eq("x2 row", b.x2[int(row_ids[t, kk])], x2[i])
+        r = int(row_ids[t, kk])
+        _eq("a2 row", b.a2[r].view(torch.int16).cpu().numpy().view(np.uint16),
+            _codes_bf16(x2[i:i + 1], I)[0])
+        _eq("ts2 row", b.ts2[r:r + 1].view(torch.int32),
+            oracle_mod.row_inv_scale(x2[i:i + 1], I).view(np.int32))
         acc2[i] = oracle_mod.grouped_gemm(x2[i:i + 1], one, w2[e].cpu().numpy()[None])[0]
         y = (acc2[i].astype(np.float32) * ws2_h[e]) * oracle_mod.row_inv_scale(x2[i:i + 1], I)[0]
         _eq("y2 row", b.y2[int(row_ids[t, kk])].view(torch.int32),
