@@ -293,3 +293,41 @@ def test_deep_moe_dsv3_size_sampled(oracle_mod, pl):
     assert st == 0
     _eq("out rows", b.out[torch.from_numpy(toks).to(dev)].view(torch.int16).cpu().numpy()
         .view(np.uint16), out)
+
+
+def test_deep_moe_graph_replay(oracle_mod, pl):
+    """The deep MoE's calls enqueue only kernels on the caller's stream (tensor
+    maps are encoded on the host into the launch), so the whole pipeline can
+    be captured once and replayed on new inputs."""
+    w = W.Workload("deep_graph", R=2, epr=4, bs=80, H=384, k=3, seed=41)
+    I = 192
+    dev = torch.device("cuda")
+    _, _, _, (w1, ws1, w2, ws2) = _deep_inputs(w, I, w.seed)
+    b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype)
+    wts = pl.DeepMoeWeights(w1.to(dev), ws1.to(dev), w2.to(dev), ws2.to(dev))
+    idx_d = torch.zeros((w.T, w.k), dtype=torch.int32, device=dev)
+    idx_d[:, 1] = 1
+    idx_d[:, 2] = 2
+    wt_d = torch.zeros((w.T, w.k), dtype=torch.float32, device=dev)
+    x_d = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pl.run_deep_moe(b, wts, x_d, idx_d, wt_d, s)      # warm-up outside the capture
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pl.run_deep_moe(b, wts, x_d, idx_d, wt_d, s)
+    for seed in (42, 43):
+        ww = w.with_(seed=seed)
+        idx, wt = W.routing(ww)
+        x = W.tokens(ww)
+        idx_d.copy_(idx)
+        wt_d.copy_(wt)
+        x_d.copy_(x)
+        b.dev_status.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert b.status() == 0
+        ref = oracle_mod.deep_moe(W.bits(x), idx.numpy(), wt.numpy(), w.R, w.epr, w.dtype,
+                                  w1.numpy(), ws1.numpy(), w2.numpy(), ws2.numpy())
+        _eq("out(graph)", b.out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"])
