@@ -488,7 +488,7 @@ def run_deep_moe_bench(args, w, ep, pl, x, idx, wt, stream, dev, flush):
     grouped GEMMs are reported against the dense bf16 tensor peak."""
     I = SWIGLU_INTERMEDIATE
     w1, ws1, w2, ws2 = W.moe_weights(w.E, w.H, I, seed=31, device=dev)
-    wts = pl.DeepMoeWeights(w1, ws1, w2, ws2, stream)
+    wts = pl.DeepMoeWeights(w1, ws1, w2, ws2, stream, interleaved=False)
     torch.cuda.synchronize()
     del w1, w2
     b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype, device=dev)
@@ -578,17 +578,30 @@ def run_gemm_only(args):
     gr = torch.full((G,), rows, dtype=torch.int32, device=dev)
     c = torch.empty((M, N), dtype=torch.int32, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
+    cs = torch.rand((G, N), generator=g, device=dev) * 1e-4 + 1e-4
+    rs = torch.rand((M,), generator=g, device=dev) * 0.01 + 0.01
+    mode = args.gemm_epilogue
+    h = torch.empty((M, N // 2), dtype=torch.float32, device=dev) if mode == "swiglu" else None
+
+    def gemm():
+        if mode == "int32":
+            ep.moe_grouped_gemm_i8(a, w, gr, c, st, stream)
+        elif mode == "dequant":
+            ep.moe_grouped_gemm_i8_dequant(a, w, gr, cs, (rs, 0, 4), c.view(torch.float32), st,
+                                           stream)
+        else:
+            ep.moe_grouped_gemm_i8_swiglu(a, w, gr, cs, (rs, 0, 4), h, st, stream)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     for _ in range(max(3, args.warmup)):
-        ep.moe_grouped_gemm_i8(a, w, gr, c, st, stream)
+        gemm()
     evs = []
     for i in range(args.steps):
         flush.fill_(i & 0xff)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        ep.moe_grouped_gemm_i8(a, w, gr, c, st, stream)
+        gemm()
         e1.record(stream)
         evs.append((e0, e1))
     torch.cuda.synchronize()
@@ -597,7 +610,8 @@ def run_gemm_only(args):
     us = float(np.mean([x.elapsed_time(y) for x, y in evs])) * 1e3
     burst, sustained, src = measured_bf16_tflops()
     tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
-    print(json.dumps({"kernel": "grouped_gemm_i8", "groups": G, "rows_per_group": rows,
+    print(json.dumps({"kernel": "grouped_gemm_i8", "epilogue": mode, "groups": G,
+                      "rows_per_group": rows,
                       "N": N, "K": K, "us": us, "tflops": tf, "frac_of_burst": tf / burst,
                       "peak_source": src, "steps": args.steps}))
 
@@ -778,6 +792,8 @@ def parse_args(argv=None):
                    help="skip the fused deep MoE section")
     p.add_argument("--gemm", default=None, metavar="G,ROWS,N,K",
                    help="time the grouped GEMM alone and exit")
+    p.add_argument("--gemm-epilogue", default="int32", choices=["int32", "dequant", "swiglu"],
+                   help="epilogue of the --gemm benchmark")
     p.add_argument("--ref-tokens", type=int, default=32)
     p.add_argument("--bs", type=int, default=None,
                    help="override tokens per rank (small profiling cases)")

@@ -84,6 +84,12 @@ def _load():
                                               ctypes.c_int32, vp, vp, vp, i64, vp, vp, vp]
     L.moe_combine_f32.argtypes = [sp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_dispatch_expand.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, i64, vp, vp]
+    L.moe_grouped_gemm_i8_swiglu.argtypes = [vp, i64, ctypes.c_int32, vp, ctypes.c_int32,
+                                             ctypes.c_int32, vp, vp, vp, i64, vp, vp, vp]
+    L.moe_interleave_gate_up.argtypes = [vp, vp, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, vp, vp, vp]
+    L.moe_quant_rows_bf16.argtypes = [vp, i64, ctypes.c_int32, vp, ctypes.c_int32, vp, vp,
+                                      vp]
     L.moe_swiglu_quant_grouped_bf16.argtypes = [vp, i64, ctypes.c_int32, vp, vp,
                                                 ctypes.c_int32, vp, i64, vp, vp, vp, vp]
     for name in ("moe_dispatch_layout", "moe_notify_dispatch", "moe_dispatch",
@@ -92,7 +98,9 @@ def _load():
                  "moe_codes_to_bf16", "moe_grouped_gemm_i8",
                  "moe_swiglu_quant_grouped", "moe_deq_combine",
                  "moe_grouped_gemm_i8_dequant", "moe_combine_f32",
-                 "moe_dispatch_expand", "moe_swiglu_quant_grouped_bf16"):
+                 "moe_dispatch_expand", "moe_swiglu_quant_grouped_bf16",
+                 "moe_grouped_gemm_i8_swiglu", "moe_interleave_gate_up",
+                 "moe_quant_rows_bf16"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -370,6 +378,8 @@ def moe_grouped_gemm_i8(a, w, group_rows, c, dev_status, stream=None):
     G, N = w.shape[0], w.shape[1]
     if group_rows.numel() != G:
         raise ValueError("group_rows must have G entries")
+    if rows == 0:
+        return MOE_OK
     st = _lib.moe_grouped_gemm_i8(
         _ptr(a, torch.bfloat16, rows * K, "a"), int(rows), int(K),
         _ptr(w, torch.bfloat16, G * N * K, "w"), int(G), int(N),
@@ -434,6 +444,8 @@ def moe_grouped_gemm_i8_dequant(a, w, group_rows, col_scale, row_scale, y, dev_s
     G, N = w.shape[0], w.shape[1]
     if group_rows.numel() != G:
         raise ValueError("group_rows must have G entries")
+    if rows == 0:
+        return MOE_OK
     rp, rstride = _strided(row_scale, rows, "row_scale")
     st = _lib.moe_grouped_gemm_i8_dequant(
         _ptr(a, torch.bfloat16, rows * K, "a"), int(rows), int(K),
@@ -501,3 +513,52 @@ def moe_swiglu_quant_grouped_bf16(acc, weight_scale, group_off, token_scale, cod
         _ptr(inv_scale, torch.float32, M, "inv_scale"),
         _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
     return _check(st, "moe_swiglu_quant_grouped_bf16")
+
+
+def moe_interleave_gate_up(w1, ws1, w1_interleaved, ws1_interleaved, stream=None):
+    """w1 int8 [G, 2I, K] -> bf16 with gate/up rows interleaved; ws1 likewise."""
+    G, N1, K = w1.shape
+    I = N1 // 2
+    st = _lib.moe_interleave_gate_up(
+        _ptr(w1, (torch.int8, torch.uint8), G * N1 * K, "w1"),
+        _ptr(ws1, torch.float32, G * N1, "ws1"), int(G), int(I), int(K),
+        _ptr(w1_interleaved, torch.bfloat16, G * N1 * K, "w1_interleaved"),
+        _ptr(ws1_interleaved, torch.float32, G * N1, "ws1_interleaved"), _stream(stream))
+    return _check(st, "moe_interleave_gate_up")
+
+
+def moe_grouped_gemm_i8_swiglu(a, w_interleaved, group_rows, col_scale_interleaved,
+                               row_scale, h, dev_status, stream=None):
+    """h [a_rows, I] fp32 = SwiGLU of the dequantised GMM1 (gate/up
+    interleaved weights [G, 2I, K]); row_scale is (tensor, byte_offset,
+    byte_stride)."""
+    if a.dim() != 2 or w_interleaved.dim() != 3 or w_interleaved.shape[2] != a.shape[1]:
+        raise ValueError("a must be [rows, K] and w [G, 2I, K]")
+    rows, K = a.shape
+    G, N = w_interleaved.shape[0], w_interleaved.shape[1]
+    I = N // 2
+    if group_rows.numel() != G:
+        raise ValueError("group_rows must have G entries")
+    if rows == 0:
+        return MOE_OK
+    rp, rstride = _strided(row_scale, rows, "row_scale")
+    st = _lib.moe_grouped_gemm_i8_swiglu(
+        _ptr(a, torch.bfloat16, rows * K, "a"), int(rows), int(K),
+        _ptr(w_interleaved, torch.bfloat16, G * N * K, "w_interleaved"), int(G), int(I),
+        _ptr(group_rows, torch.int32, G, "group_rows"),
+        _ptr(col_scale_interleaved, torch.float32, G * N, "col_scale_interleaved"), rp,
+        rstride, _ptr(h, torch.float32, rows * I, "h"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_grouped_gemm_i8_swiglu")
+
+
+def moe_quant_rows_bf16(h, group_off, codes, inv_scale, stream=None):
+    """Requantise fp32 rows h [M, I] into bf16-valued codes and 1/scale."""
+    M, I = h.shape
+    G = 0 if group_off is None else group_off.numel() - 1
+    st = _lib.moe_quant_rows_bf16(
+        _ptr(h, torch.float32, M * I, "h"), int(M), int(I),
+        None if group_off is None else _ptr(group_off, torch.int64, G + 1, "group_off"),
+        int(G), _ptr(codes, torch.bfloat16, M * I, "codes"),
+        _ptr(inv_scale, torch.float32, M, "inv_scale"), _stream(stream))
+    return _check(st, "moe_quant_rows_bf16")

@@ -311,17 +311,18 @@ moe_status moe_grouped_gemm_i8(const void* a, int64_t a_rows, int32_t K, const v
                                int32_t G, int32_t N, const int32_t* group_rows, int32_t* c,
                                int32_t* dev_status, void* stream) {
   const int64_t bn = moe_ep::gmm_block_n();
-  if (a_rows < 1 || a_rows > INT32_MAX || K < 8 || K > MOE_EP_MAX_HIDDEN || K % 8 != 0 ||
+  if (a_rows < 0 || a_rows > INT32_MAX || K < 8 || K > MOE_EP_MAX_HIDDEN || K % 8 != 0 ||
       G < 1 || G > MOE_EP_MAX_EXPERTS || N < 8 || N > MOE_EP_MAX_HIDDEN || N % 8 != 0 ||
       !dev_status)
     return MOE_ERR_INVALID_ARG;
+  if (a_rows == 0) return MOE_OK;   // no rows: nothing to compute
   if ((a_rows / 128 + G) * ((N + bn - 1) / bn) > INT32_MAX) return MOE_ERR_INVALID_ARG;
   if (!a || !w || !group_rows || !c) return MOE_ERR_INVALID_ARG;
   if (!aligned(a, 16) || !aligned(w, 16) || !aligned(group_rows, 4) || !aligned(c, 16) ||
       !aligned(dev_status, 4))
     return MOE_ERR_INVALID_ARG;
-  return from_cuda(moe_ep::launch_grouped_gemm(a, a_rows, K, w, G, N, group_rows, c, nullptr,
-                                               nullptr, 0, dev_status,
+  return from_cuda(moe_ep::launch_grouped_gemm(a, a_rows, K, w, G, N, group_rows, c, 0,
+                                               nullptr, nullptr, 0, dev_status,
                                                static_cast<cudaStream_t>(stream)));
 }
 
@@ -331,20 +332,73 @@ moe_status moe_grouped_gemm_i8_dequant(const void* a, int64_t a_rows, int32_t K,
                                        const void* row_scale, int64_t row_scale_stride,
                                        float* y, int32_t* dev_status, void* stream) {
   const int64_t bn = moe_ep::gmm_block_n();
-  if (a_rows < 1 || a_rows > INT32_MAX || K < 8 || K > MOE_EP_MAX_HIDDEN || K % 8 != 0 ||
+  if (a_rows < 0 || a_rows > INT32_MAX || K < 8 || K > MOE_EP_MAX_HIDDEN || K % 8 != 0 ||
       G < 1 || G > MOE_EP_MAX_EXPERTS || N < 8 || N > MOE_EP_MAX_HIDDEN || N % 8 != 0 ||
       row_scale_stride < 4 || row_scale_stride % 4 != 0 || !dev_status)
     return MOE_ERR_INVALID_ARG;
+  if (a_rows == 0) return MOE_OK;
   if ((a_rows / 128 + G) * ((N + bn - 1) / bn) > INT32_MAX) return MOE_ERR_INVALID_ARG;
   if (!a || !w || !group_rows || !col_scale || !row_scale || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned(a, 16) || !aligned(w, 16) || !aligned(group_rows, 4) ||
       !aligned(col_scale, 16) || !aligned(row_scale, 4) || !aligned(y, 16) ||
       !aligned(dev_status, 4))
     return MOE_ERR_INVALID_ARG;
-  return from_cuda(moe_ep::launch_grouped_gemm(a, a_rows, K, w, G, N, group_rows, y,
+  return from_cuda(moe_ep::launch_grouped_gemm(a, a_rows, K, w, G, N, group_rows, y, 1,
                                                col_scale, row_scale, row_scale_stride,
                                                dev_status,
                                                static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_grouped_gemm_i8_swiglu(const void* a, int64_t a_rows, int32_t K,
+                                      const void* w_interleaved, int32_t G, int32_t I,
+                                      const int32_t* group_rows,
+                                      const float* col_scale_interleaved,
+                                      const void* row_scale, int64_t row_scale_stride,
+                                      float* h, int32_t* dev_status, void* stream) {
+  const int64_t bn = moe_ep::gmm_block_n();
+  const int64_t N = 2 * int64_t(I);
+  if (a_rows < 0 || a_rows > INT32_MAX || K < 8 || K > MOE_EP_MAX_HIDDEN || K % 8 != 0 ||
+      G < 1 || G > MOE_EP_MAX_EXPERTS || I < 8 || N > MOE_EP_MAX_HIDDEN || I % 8 != 0 ||
+      row_scale_stride < 4 || row_scale_stride % 4 != 0 || !dev_status)
+    return MOE_ERR_INVALID_ARG;
+  if (a_rows == 0) return MOE_OK;
+  if ((a_rows / 128 + G) * ((N + bn - 1) / bn) > INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if (!a || !w_interleaved || !group_rows || !col_scale_interleaved || !row_scale || !h)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(a, 16) || !aligned(w_interleaved, 16) || !aligned(group_rows, 4) ||
+      !aligned(col_scale_interleaved, 16) || !aligned(row_scale, 4) || !aligned(h, 16) ||
+      !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_grouped_gemm(
+      a, a_rows, K, w_interleaved, G, static_cast<int>(N), group_rows, h, 2,
+      col_scale_interleaved, row_scale, row_scale_stride, dev_status,
+      static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_interleave_gate_up(const void* w1, const float* ws1, int32_t G, int32_t I,
+                                  int32_t K, void* w1_interleaved,
+                                  float* ws1_interleaved, void* stream) {
+  if (G < 1 || G > MOE_EP_MAX_EXPERTS || I < 8 || 2 * int64_t(I) > MOE_EP_MAX_HIDDEN ||
+      I % 8 != 0 || K < 8 || K > MOE_EP_MAX_HIDDEN || K % 8 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (!w1 || !ws1 || !w1_interleaved || !ws1_interleaved || !aligned(w1, 8) ||
+      !aligned(ws1, 4) || !aligned(w1_interleaved, 16) || !aligned(ws1_interleaved, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_interleave_gate_up(w1, ws1, G, I, K, w1_interleaved,
+                                                     ws1_interleaved,
+                                                     static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_quant_rows_bf16(const float* h, int64_t M, int32_t I, const int64_t* group_off,
+                               int32_t G, void* codes, float* inv_scale, void* stream) {
+  if (M < 0 || I < 8 || I > 16384 || I % 8 != 0 || (group_off && (G < 1 || G > MOE_EP_MAX_EXPERTS)))
+    return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  if (!h || !codes || !inv_scale || !aligned(h, 16) || !aligned(codes, 16) ||
+      !aligned(inv_scale, 4) || !aligned(group_off, 8))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_quant_rows_bf16(h, M, I, group_off, G, codes, inv_scale,
+                                                  static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_combine_f32(const moe_shape* shape, const float* expert_out,

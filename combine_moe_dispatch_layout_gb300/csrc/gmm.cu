@@ -128,6 +128,10 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
@@ -182,18 +186,26 @@ __device__ __forceinline__ Tile decode_tile(int64_t t, const int64_t* goff,
   return tl;
 }
 
-// Optional dequantising epilogue (the page's "Cast FP32 -> x weight_scale ->
-// x per_token_scale" after GMM2): out = (fp32(c) * col_scale[g][n]) * the fp32
-// at row_scale + m * row_scale_stride, each product rounded to nearest even.
+// Epilogue modes.  kOutInt32: c itself.  kOutDequant (the page's "Cast FP32
+// -> x weight_scale -> x per_token_scale" after GMM2): y = (fp32(c) *
+// col_scale[g][n]) * ts(m), ts(m) the fp32 at row_scale + m *
+// row_scale_stride.  kOutSwiGLU (GMM1 with its DeqSwiglu epilogue, section
+// 4.8.1; the weights' gate and up rows interleaved, column 2j = gate j,
+// 2j + 1 = up j): h[m][j] = swiglu(dequant(c[m][2j]), dequant(c[m][2j+1])),
+// N/2 fp32 outputs per row.  Every operation rounds to nearest even.
+enum { kOutInt32 = 0, kOutDequant = 1, kOutSwiGLU = 2 };
 struct Dequant {
-  const float* col_scale;            // [G][N]; nullptr: int32 output
+  int mode;
+  const float* col_scale;            // [G][N]
   const unsigned char* row_scale;
   int64_t row_scale_stride;          // bytes
 };
 
 // One CTA per SM; registers are allocated per SM sub-partition (16 K each),
 // and 10 warps put 3 on some of them, so at most 168 registers per thread.
-template <int STAGES>
+// MODE (kOut*) is a template parameter so each epilogue gets its own
+// register allocation.
+template <int STAGES, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -367,6 +379,22 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t chunk_ctr = 0;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
       const Tile tl = decode_tile(t, goff, tpre, G, ntn);
+      const int r = q * 32 + lane;
+      const int col0 = tl.n0 + half * kEpiCols;
+      const int ncols = N - col0;            // a ragged last column tile
+      // scales of the dequantising epilogues: pulled into L1 now (no
+      // registers held across the chunks), read after the last chunk; lane l
+      // reads columns 4l .. 4l+3 of this thread's half
+      const float* cs_ptr = MODE != kOutInt32
+                                ? dq.col_scale + int64_t(tl.g) * N + col0 + 4 * lane : nullptr;
+      const float* ts_ptr = MODE != kOutInt32
+                                ? reinterpret_cast<const float*>(
+                                      dq.row_scale + (tl.row0 + r) * dq.row_scale_stride)
+                                : nullptr;
+      if (MODE != kOutInt32) {
+        if (4 * lane < ncols) prefetch_l1(cs_ptr);
+        if (r < tl.rows) prefetch_l1(ts_ptr);
+      }
       int32_t acc[kEpiCols];
 #pragma unroll
       for (int j = 0; j < kEpiCols; ++j) acc[j] = 0;
@@ -396,23 +424,33 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         *abort_flag = 1;
         break;
       }
-      const int r = q * 32 + lane;
-      const int col0 = tl.n0 + half * kEpiCols;
-      const int ncols = N - col0;            // a ragged last column tile
-      if (dq.col_scale) {                    // dequantise in registers
-        const float ts = r < tl.rows ? __ldg(reinterpret_cast<const float*>(
-                                           dq.row_scale + (tl.row0 + r) * dq.row_scale_stride))
-                                     : 0.0f;
-        const float* cs = dq.col_scale + int64_t(tl.g) * N + col0;
+      constexpr bool swiglu = MODE == kOutSwiGLU;
+      const int nout = swiglu ? N / 2 : N;   // output columns of the matrix
+      const int ocol0 = swiglu ? col0 / 2 : col0;
+      const int ocols = nout - ocol0;
+      constexpr int nvals = swiglu ? kEpiCols / 2 : kEpiCols;   // outputs held per thread
+      if (MODE != kOutInt32) {               // dequantise (and SwiGLU) in registers
+        const float4 csv = 4 * lane < ncols ? __ldg(reinterpret_cast<const float4*>(cs_ptr))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float ts = r < tl.rows ? __ldg(ts_ptr) : 0.0f;
 #pragma unroll
         for (int j = 0; j < kEpiCols / 4; ++j) {
+          const float cv[4] = {__shfl_sync(0xffffffffu, csv.x, j),
+                               __shfl_sync(0xffffffffu, csv.y, j),
+                               __shfl_sync(0xffffffffu, csv.z, j),
+                               __shfl_sync(0xffffffffu, csv.w, j)};
           if (4 * j < ncols) {
-            const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs + 4 * j));
-            const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+            float y[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              acc[4 * j + i] = __float_as_int(
-                  __fmul_rn(__fmul_rn(__int2float_rn(acc[4 * j + i]), cv[i]), ts));
+              y[i] = __fmul_rn(__fmul_rn(__int2float_rn(acc[4 * j + i]), cv[i]), ts);
+            if (swiglu) {                    // (gate, up) pairs -> h, packed to the front
+              acc[2 * j] = __float_as_int(swiglu_rn(y[0], y[1]));
+              acc[2 * j + 1] = __float_as_int(swiglu_rn(y[2], y[3]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) acc[4 * j + i] = __float_as_int(y[i]);
+            }
           }
         }
       }
@@ -422,7 +460,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const uint32_t sw = (lane >> 1) & 3u;             // 64-byte swizzle of row `lane`
 #pragma unroll
         for (int blk = 0; blk < kEpiCols / kStoreCols; ++blk) {
-          if (blk * kStoreCols < ncols) {
+          if (blk * kStoreCols < nvals && blk * kStoreCols < ocols) {
             if (lane == 0) bulk_wait_read<0>();           // the buffer's last store has read it
             __syncwarp();
 #pragma unroll
@@ -433,17 +471,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmC, smem_addr(stg), col0 + blk * kStoreCols,
+              tma_store_2d(&tmC, smem_addr(stg), ocol0 + blk * kStoreCols,
                            static_cast<int>(tl.row0 + q * 32));
               bulk_commit();
             }
           }
         }
       } else if (r < tl.rows) {              // the group's last rows: plain stores
-        int4* dst = reinterpret_cast<int4*>(C + (tl.row0 + r) * int64_t(N) + col0);
+        int4* dst = reinterpret_cast<int4*>(C + (tl.row0 + r) * int64_t(nout) + ocol0);
 #pragma unroll
         for (int j = 0; j < kEpiCols / 4; ++j)
-          if (4 * j < ncols)
+          if (4 * j < nvals && 4 * j < ocols)
             dst[j] = make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
       }
     }
@@ -482,6 +520,37 @@ __global__ void codes_to_bf16_kernel(const uint8_t* __restrict__ src, int64_t ro
       o[j] = narrow_rn<MOE_BF16>(lo) | (narrow_rn<MOE_BF16>(hi) << 16);   // exact
     }
     reinterpret_cast<uint4*>(dst + r * int64_t(K))[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Gate/up interleave of GMM1's weights for the SwiGLU epilogue: output row
+// (g, 2j) = input row (g, j) (gate), (g, 2j + 1) = input row (g, I + j) (up),
+// converted to bf16; the column scales are permuted the same way.
+__global__ void interleave_gate_up_kernel(const uint8_t* __restrict__ w, const float* __restrict__ ws,
+                                          int G, int I, int K, uint16_t* __restrict__ wi,
+                                          float* __restrict__ wsi) {
+  const int per_row = K / 8;
+  const int64_t rows = int64_t(G) * 2 * I;
+  const int64_t n = rows * per_row;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / per_row;
+    const int c = static_cast<int>(i - r * per_row);
+    const int64_t g = r / (2 * I);
+    const int local = static_cast<int>(r - g * 2 * I);
+    const int64_t src = g * 2 * I + ((local & 1) ? I + (local >> 1) : (local >> 1));
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(w + src * K + 8 * c));
+    const uint32_t b[2] = {v.x, v.y};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t word = b[j >> 1] >> (16 * (j & 1));
+      const float lo = static_cast<float>(static_cast<int8_t>(word & 0xffu));
+      const float hi = static_cast<float>(static_cast<int8_t>((word >> 8) & 0xffu));
+      o[j] = narrow_rn<MOE_BF16>(lo) | (narrow_rn<MOE_BF16>(hi) << 16);   // exact
+    }
+    reinterpret_cast<uint4*>(wi + r * int64_t(K))[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    if (c == 0) wsi[r] = __ldg(ws + src);
   }
 }
 
@@ -554,32 +623,62 @@ int gmm_block_n() { return BN; }
 
 namespace {
 
+template <int STAGES, int MODE>
+cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                        const int32_t* group_rows, int G, int64_t a_rows, int K, int N,
+                        int32_t* c, const Dequant& dq, int32_t* dev_status, int sms,
+                        cudaStream_t st) {
+  const size_t smem = SmemLayout<STAGES>::bytes(G);
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<STAGES, MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  grouped_gemm_kernel<STAGES, MODE><<<sms, kThreads, smem, st>>>(ma, mb, mc, group_rows, G,
+                                                                 a_rows, K, N, c, dq,
+                                                                 dev_status);
+  return cudaGetLastError();
+}
+
 template <int STAGES>
 cudaError_t launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                           const int32_t* group_rows, int G, int64_t a_rows, int K, int N,
                           int32_t* c, const Dequant& dq, int32_t* dev_status, int sms,
                           cudaStream_t st) {
-  const size_t smem = SmemLayout<STAGES>::bytes(G);
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<STAGES>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  grouped_gemm_kernel<STAGES><<<sms, kThreads, smem, st>>>(ma, mb, mc, group_rows, G, a_rows, K,
-                                                           N, c, dq, dev_status);
-  return cudaGetLastError();
+  if (dq.mode == kOutDequant)
+    return launch_mode<STAGES, kOutDequant>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
+                                            dev_status, sms, st);
+  if (dq.mode == kOutSwiGLU)
+    return launch_mode<STAGES, kOutSwiGLU>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
+                                           dev_status, sms, st);
+  return launch_mode<STAGES, kOutInt32>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
+                                        dev_status, sms, st);
 }
 
 }  // namespace
 
+cudaError_t launch_interleave_gate_up(const void* w, const float* ws, int G, int I, int K,
+                                     void* wi, float* wsi, cudaStream_t st) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int64_t n = int64_t(G) * 2 * I * (K / 8);
+  const int threads = 256;
+  const int64_t grid = std::min<int64_t>((n + threads - 1) / threads, int64_t(sms) * 8);
+  interleave_gate_up_kernel<<<static_cast<unsigned>(grid), threads, 0, st>>>(
+      static_cast<const uint8_t*>(w), ws, G, I, K, static_cast<uint16_t*>(wi), wsi);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void* b, int G,
-                                int N, const int32_t* group_rows, void* c,
+                                int N, const int32_t* group_rows, void* c, int mode,
                                 const float* col_scale, const void* row_scale,
                                 int64_t row_scale_stride, int32_t* dev_status,
                                 cudaStream_t st) {
   CUtensorMap ma, mb, mc;
   cudaError_t e = encode_kmajor(&ma, a, a_rows, K, BM);
   if (e == cudaSuccess) e = encode_kmajor(&mb, b, int64_t(G) * N, K, BN);
-  if (e == cudaSuccess) e = encode_out(&mc, c, a_rows, N);
+  if (e == cudaSuccess) e = encode_out(&mc, c, a_rows, mode == kOutSwiGLU ? N / 2 : N);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0, optin = 0;
   e = cudaGetDevice(&dev);
@@ -587,7 +686,8 @@ cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  const Dequant dq{col_scale, static_cast<const unsigned char*>(row_scale), row_scale_stride};
+  const Dequant dq{mode, col_scale, static_cast<const unsigned char*>(row_scale),
+                   row_scale_stride};
   int32_t* out = static_cast<int32_t*>(c);
   // four stages unless the group tables (12 bytes per group) crowd them out
   if (SmemLayout<4>::bytes(G) <= size_t(optin))

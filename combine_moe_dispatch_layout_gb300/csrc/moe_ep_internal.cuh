@@ -174,6 +174,49 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// ---- the SwiGLU step of the GMM1 epilogue (UMDK/CAM deep analysis v2,
+// section 4.8.1: Muls(-1), Exp, Adds(1), Div on the gate, times the up value)
+// shared by the standalone epilogue kernel and the GEMM's fused epilogue, so
+// both evaluate exactly the same operations.
+
+// 1.5 * 2^23: adding it to a float of magnitude below 2^22 rounds that float
+// to an integer (ties to even), which then sits in the low mantissa bits.
+constexpr float kRoundMagic = 12582912.0f;
+
+// exp by Cody and Waite's two-constant range reduction, x = n ln 2 + r with
+// |r| <= ln 2 / 2 (ln 2 = C1 + C2, C1 = 0.693359375 so n*C1 is exact), and
+// the degree-7 Taylor polynomial of e^r in Horner form, times 2^n; input
+// clamped to [-87, 88].  Every step is one fp32 operation rounded to nearest
+// even; the reduction and Horner steps are fused multiply-adds.
+__device__ __forceinline__ float exp_cody_waite(float x) {
+  if (x > 88.0f) x = 88.0f;
+  if (x < -87.0f) x = -87.0f;
+  const float t = __fmul_rn(x, 1.44269504f);                 // x / ln 2
+  const float s = __fadd_rn(t, kRoundMagic);                 // rint(t) in the low bits
+  const float n = __fsub_rn(s, kRoundMagic);                 // rint(t), exactly
+  float r = __fmaf_rn(-n, 0.693359375f, x);                  // x - n*C1
+  r = __fmaf_rn(-n, -2.12194440e-4f, r);                     // - n*C2
+  float p = 1.98412698e-4f;                                  // 1/7!
+  p = __fmaf_rn(p, r, 1.38888889e-3f);                       // 1/6!
+  p = __fmaf_rn(p, r, 8.33333333e-3f);                       // 1/5!
+  p = __fmaf_rn(p, r, 4.16666667e-2f);                       // 1/4!
+  p = __fmaf_rn(p, r, 1.66666667e-1f);                       // 1/3!
+  p = __fmaf_rn(p, r, 0.5f);                                 // 1/2!
+  p = __fmaf_rn(p, r, 1.0f);                                 // 1/1!
+  p = __fmaf_rn(p, r, 1.0f);                                 // 1/0!
+  // n is in -126 .. 127: the low 9 bits of s hold n (two's complement), so
+  // (s + 127) << 23 is the bit pattern of 2^n.
+  return __fmul_rn(p, __uint_as_float((__float_as_uint(s) + 127u) << 23));
+}
+
+// h = (gate / (1 + exp(-gate))) * up, one rounding per operation.
+__device__ __forceinline__ float swiglu_rn(float gate, float up) {
+  const float e = exp_cody_waite(-gate);
+  const float d = __fadd_rn(e, 1.0f);
+  const float sg = __fdiv_rn(gate, d);
+  return __fmul_rn(sg, up);
+}
+
 // Combine: resolve the receive rows and gate weights of token g into the
 // shared tables rows[k], w[k] (one warp; lane kk handles pair kk).  A bad
 // expert id or a row outside [0, y_rows) gives row -1 and a status code.
@@ -254,11 +297,18 @@ cudaError_t launch_codes_to_bf16(const void* src, int64_t rows, int64_t stride, 
 
 int gmm_block_n();
 
+// mode: 0 int32 c, 1 dequantised fp32, 2 SwiGLU of interleaved gate/up pairs
 cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void* b, int G,
-                                int N, const int32_t* group_rows, void* c,
+                                int N, const int32_t* group_rows, void* c, int mode,
                                 const float* col_scale, const void* row_scale,
                                 int64_t row_scale_stride, int32_t* dev_status,
                                 cudaStream_t st);
+
+cudaError_t launch_interleave_gate_up(const void* w, const float* ws, int G, int I, int K,
+                                     void* wi, float* wsi, cudaStream_t st);
+
+cudaError_t launch_quant_rows_bf16(const float* h, int64_t M, int I, const int64_t* group_off,
+                                   int G, void* codes, float* inv_scale, cudaStream_t st);
 
 cudaError_t launch_group_offsets(const int32_t* counts, int G, int64_t* off,
                                  int32_t* dev_status, cudaStream_t st);

@@ -33,31 +33,6 @@ constexpr int kMaxThreads = 512;
 // 8-output chunks per thread: 2 while that fits 512 threads (I <= 8192; more
 // warps per SM, measured fastest at I = 2048), else 4 (I <= 16384).
 
-// 1.5 * 2^23: adding it to a float of magnitude below 2^22 rounds that float
-// to an integer (ties to even), which then sits in the low mantissa bits.
-constexpr float kRoundMagic = 12582912.0f;
-
-__device__ __forceinline__ float exp_cody_waite(float x) {
-  if (x > 88.0f) x = 88.0f;
-  if (x < -87.0f) x = -87.0f;
-  const float t = __fmul_rn(x, 1.44269504f);                 // x / ln 2
-  const float s = __fadd_rn(t, kRoundMagic);                 // rint(t) in the low bits
-  const float n = __fsub_rn(s, kRoundMagic);                 // rint(t), exactly
-  float r = __fmaf_rn(-n, 0.693359375f, x);                  // x - n*C1 (ln 2, high part)
-  r = __fmaf_rn(-n, -2.12194440e-4f, r);                     // - n*C2 (ln 2, low part)
-  float p = 1.98412698e-4f;                                  // 1/7!
-  p = __fmaf_rn(p, r, 1.38888889e-3f);                       // 1/6!
-  p = __fmaf_rn(p, r, 8.33333333e-3f);                       // 1/5!
-  p = __fmaf_rn(p, r, 4.16666667e-2f);                       // 1/4!
-  p = __fmaf_rn(p, r, 1.66666667e-1f);                       // 1/3!
-  p = __fmaf_rn(p, r, 0.5f);                                 // 1/2!
-  p = __fmaf_rn(p, r, 1.0f);                                 // 1/1!
-  p = __fmaf_rn(p, r, 1.0f);                                 // 1/0!
-  // n is in -126 .. 127: the low 9 bits of s hold n (two's complement), so
-  // (s + 127) << 23 is the bit pattern of 2^n.
-  return __fmul_rn(p, __uint_as_float((__float_as_uint(s) + 127u) << 23));
-}
-
 // Where a row's scales come from.  Plain: one weight-scale vector for all
 // rows, token scales packed fp32.  Grouped (fused deep MoE): row m belongs to
 // the expert g with group_off[g] <= m < group_off[g + 1] and uses
@@ -132,10 +107,7 @@ swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc 
           float up = __int2float_rn(ui[j]);
           up = __fmul_rn(up, wu[j]);
           up = __fmul_rn(up, ts);
-          const float e = exp_cody_waite(-gate);
-          const float d = __fadd_rn(e, 1.0f);
-          const float sg = __fdiv_rn(gate, d);
-          h[i][j] = __fmul_rn(sg, up);
+          h[i][j] = swiglu_rn(gate, up);
           amax = fmaxf(amax, fabsf(h[i][j]));
         }
       }
@@ -206,7 +178,100 @@ cudaError_t launch_t(const int32_t* acc, int64_t M, int I, const ScaleSrc& sc, v
   return cudaGetLastError();
 }
 
+// Dynamic INT8 quantisation of fp32 rows (the requant half of the GMM1
+// epilogue when the GEMM's own epilogue has produced h): per row, amax =
+// max |h|, scale = 127/(amax + 1e-12f), q = rint(h * scale); the codes go out
+// as bf16 values (exact) and 1/scale to inv_scale[m].  Rows at or past
+// group_off[G] (when given) are not written.
+template <int kCpt>
+__global__ void __launch_bounds__(kMaxThreads)
+quant_rows_bf16_kernel(const float* __restrict__ h, int64_t M, int I,
+                       const int64_t* __restrict__ group_off, int G,
+                       uint16_t* __restrict__ codes, float* __restrict__ inv_scale) {
+  __shared__ float s_wmax[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, nwarps = nthreads / 32;
+  const int nch = I / 8;
+  if (group_off) {
+    const int64_t rows = __ldg(group_off + G);
+    if (rows < M) M = rows;
+  }
+  const int64_t per_cta = (M + gridDim.x - 1) / gridDim.x;
+  const int64_t m_end = (blockIdx.x + 1) * per_cta < M ? (blockIdx.x + 1) * per_cta : M;
+  for (int64_t m = blockIdx.x * per_cta; m < m_end; ++m) {
+    const float* row = h + m * int64_t(I);
+    float v[kCpt][8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kCpt; ++i) {
+      const int c = tid + i * nthreads;
+      if (c < nch) {
+        const uint4 a = ld_stream_16(row + 8 * c), b = ld_stream_16(row + 8 * c + 4);
+        const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[i][j] = __uint_as_float(u[j]);
+          amax = fmaxf(amax, fabsf(v[i][j]));
+        }
+      }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    if (lane == 0) s_wmax[warp] = amax;
+    __syncthreads();
+    amax = s_wmax[0];
+    for (int w = 1; w < nwarps; ++w) amax = fmaxf(amax, s_wmax[w]);
+    const float scale = __fdiv_rn(127.0f, __fadd_rn(amax, 1e-12f));
+    const float inv = __fdiv_rn(1.0f, scale);
+#pragma unroll
+    for (int i = 0; i < kCpt; ++i) {
+      const int c = tid + i * nthreads;
+      if (c < nch) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {   // q = rint(h * scale) exactly, then its bf16 bits
+          const float q0 = __fsub_rn(__fadd_rn(__fmul_rn(v[i][2 * j], scale), kRoundMagic),
+                                     kRoundMagic);
+          const float q1 = __fsub_rn(__fadd_rn(__fmul_rn(v[i][2 * j + 1], scale), kRoundMagic),
+                                     kRoundMagic);
+          w4[j] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632);
+        }
+        *reinterpret_cast<uint4*>(codes + m * int64_t(I) + 8 * c) =
+            make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+    }
+    if (tid == 0) inv_scale[m] = inv;
+    __syncthreads();   // s_wmax is rewritten for the next row
+  }
+}
+
+template <int kCpt>
+cudaError_t launch_quant_rows_t(const float* h, int64_t M, int I, const int64_t* group_off,
+                                int G, void* codes, float* inv_scale, cudaStream_t st) {
+  const int nch = I / 8;
+  const int threads = std::max(32, std::min(kMaxThreads, ((nch + kCpt - 1) / kCpt + 31) / 32 * 32));
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_rows_bf16_kernel<kCpt>,
+                                                      threads, 0);
+  if (e != cudaSuccess) return e;
+  const int64_t grid = std::min<int64_t>(M, int64_t(std::max(1, per_sm)) * sms);
+  quant_rows_bf16_kernel<kCpt><<<static_cast<unsigned>(grid), threads, 0, st>>>(
+      h, M, I, group_off, G, static_cast<uint16_t*>(codes), inv_scale);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_quant_rows_bf16(const float* h, int64_t M, int I, const int64_t* group_off,
+                                   int G, void* codes, float* inv_scale, cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  return I / 8 <= 2 * kMaxThreads
+             ? launch_quant_rows_t<2>(h, M, I, group_off, G, codes, inv_scale, st)
+             : launch_quant_rows_t<4>(h, M, I, group_off, G, codes, inv_scale, st);
+}
 
 cudaError_t launch_swiglu_quant(const int32_t* acc, int64_t M, int I,
                                 const float* weight_scale, const float* token_scale,

@@ -13,7 +13,8 @@ from . import (fused_workspace_bytes, make_shape, layout_workspace_bytes,
                moe_codes_to_bf16, moe_combine, moe_combine_f32, moe_combine_quant,
                moe_dispatch, moe_dispatch_expand, moe_dispatch_fused,
                moe_dispatch_layout, moe_group_offsets, moe_grouped_gemm_i8,
-               moe_grouped_gemm_i8_dequant, moe_notify_dispatch,
+               moe_grouped_gemm_i8_dequant, moe_grouped_gemm_i8_swiglu,
+               moe_interleave_gate_up, moe_notify_dispatch, moe_quant_rows_bf16,
                moe_swiglu_quant_grouped_bf16, recv_row_bytes)
 
 
@@ -113,17 +114,26 @@ class DeepMoeWeights:
     (exact) for the tensor-core GEMMs, plus fp32 per-column scales.
     w1 int8 [E, 2I, H], ws1 [E, 2I], w2 int8 [E, H, I], ws2 [E, H]."""
 
-    def __init__(self, w1, ws1, w2, ws2, stream=None):
+    def __init__(self, w1, ws1, w2, ws2, stream=None, plain=True, interleaved=True):
         E, N1, H = w1.shape
         I = N1 // 2
         assert w2.shape == (E, H, I)
         self.E, self.H, self.I = E, H, I
-        self.w1 = torch.empty((E, N1, H), dtype=torch.bfloat16, device=w1.device)
-        self.w2 = torch.empty((E, H, I), dtype=torch.bfloat16, device=w2.device)
-        moe_codes_to_bf16(w1, E * N1, H, H, self.w1, stream)
-        moe_codes_to_bf16(w2, E * H, I, I, self.w2, stream)
+        dev = w1.device
         self.ws1 = ws1.contiguous()
         self.ws2 = ws2.contiguous()
+        # plain copy for GMM1 with int32 output (the standalone epilogue)
+        self.w1 = self.w1i = self.ws1i = None
+        if plain:
+            self.w1 = torch.empty((E, N1, H), dtype=torch.bfloat16, device=dev)
+            moe_codes_to_bf16(w1, E * N1, H, H, self.w1, stream)
+        # gate/up interleaved copy for GMM1 with the SwiGLU epilogue
+        if interleaved:
+            self.w1i = torch.empty((E, N1, H), dtype=torch.bfloat16, device=dev)
+            self.ws1i = torch.empty((E, N1), dtype=torch.float32, device=dev)
+            moe_interleave_gate_up(w1, self.ws1, self.w1i, self.ws1i, stream)
+        self.w2 = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev)
+        moe_codes_to_bf16(w2, E * H, I, I, self.w2, stream)
 
 
 class DeepMoeBuffers(PipelineBuffers):
@@ -141,6 +151,7 @@ class DeepMoeBuffers(PipelineBuffers):
         self.a1 = torch.empty((P, H), dtype=torch.bfloat16, device=device)
         self.ts1 = torch.empty((P,), **f32)
         self.acc1 = torch.empty((P, 2 * I), dtype=torch.int32, device=device)
+        self.h = torch.empty((P, I), **f32)
         self.a2 = torch.empty((P, I), dtype=torch.bfloat16, device=device)
         self.ts2 = torch.empty((P,), **f32)
         self.y2 = torch.empty((P, H), **f32)
@@ -152,14 +163,21 @@ def run_dispatch_expand(b, x, topk_idx, stream=None):
                         b.a1, b.ts1, b.capacity, b.dev_status, stream)
 
 
-def run_deep_moe_experts(b, wts, stream=None):
-    """Stages 2-3 up to the dequantised expert outputs ``b.y2``: GMM1,
-    DeqSwigluQuant (per-expert scales, the dispatched rows' 1/scale), GMM2
-    with its dequantising epilogue."""
+def run_deep_moe_experts(b, wts, stream=None, fused_swiglu=False):
+    """Stages 2-3 up to the dequantised expert outputs ``b.y2``.  GMM1 to
+    int32 + the standalone DeqSwigluQuant kernel (the faster route at the
+    DeepSeek-V3 size), or with ``fused_swiglu`` GMM1 with DeqSwiglu in its
+    epilogue (fp32 h, half the intermediate bytes) + the requantisation
+    pass; then GMM2 with its dequantising epilogue."""
     moe_group_offsets(b.recv_per_expert, b.group_off, b.dev_status, stream)
-    moe_grouped_gemm_i8(b.a1, wts.w1, b.recv_per_expert, b.acc1, b.dev_status, stream)
-    moe_swiglu_quant_grouped_bf16(b.acc1, wts.ws1, b.group_off, (b.ts1, 0, 4), b.a2,
-                                  b.ts2, b.dev_status, stream)
+    if fused_swiglu:
+        moe_grouped_gemm_i8_swiglu(b.a1, wts.w1i, b.recv_per_expert, wts.ws1i,
+                                   (b.ts1, 0, 4), b.h, b.dev_status, stream)
+        moe_quant_rows_bf16(b.h, b.group_off, b.a2, b.ts2, stream)
+    else:
+        moe_grouped_gemm_i8(b.a1, wts.w1, b.recv_per_expert, b.acc1, b.dev_status, stream)
+        moe_swiglu_quant_grouped_bf16(b.acc1, wts.ws1, b.group_off, (b.ts1, 0, 4), b.a2,
+                                      b.ts2, b.dev_status, stream)
     moe_grouped_gemm_i8_dequant(b.a2, wts.w2, b.recv_per_expert, wts.ws2, (b.ts2, 0, 4),
                                 b.y2, b.dev_status, stream)
 

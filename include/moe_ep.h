@@ -313,7 +313,7 @@ int32_t moe_gmm_block_n(void);
  * GB300's tensor cores have no INT8 MMA, and with values of this range the
  * bf16 MMA with fp32 accumulation over K chunks of 1024 is exact, so c is
  * the integer GEMM bit for bit.
- *   a           bf16 [a_rows][K], 16-byte aligned; a_rows <= 2^31 - 1
+ *   a           bf16 [a_rows][K], 16-byte aligned; a_rows <= 2^31 - 1 (0: no-op)
  *   w           bf16 [G][N][K] (K-major), 16-byte aligned
  *   group_rows  int32 [G] device (e.g. recv_per_expert of moe_notify_dispatch)
  *   c           int32 [a_rows][N], 16-byte aligned; rows past the groups'
@@ -370,6 +370,40 @@ moe_status moe_grouped_gemm_i8_dequant(const void* a, int64_t a_rows, int32_t K,
                                        const int32_t* group_rows, const float* col_scale,
                                        const void* row_scale, int64_t row_scale_stride,
                                        float* y, int32_t* dev_status, void* stream);
+
+/* GMM1 with its DeqSwiglu epilogue in the GEMM (section 4.3 stage 2; section
+ * 4.8.1's Cast, x weight_scale, x per_token_scale, SwiGLU): the weights' gate
+ * and up rows are interleaved (moe_interleave_gate_up: row 2j = gate j,
+ * 2j + 1 = up j, column scales likewise), so every output tile holds whole
+ * (gate, up) pairs, and for row m of group g
+ *   gate = (fp32(c[m][2j]) * cs[g][2j]) * ts(m),  up likewise at 2j + 1,
+ *   h[m][j] = (gate / (1 + exp(-gate))) * up
+ * with the same operations as moe_swiglu_quant (exp: Cody-Waite + Taylor).
+ * h (fp32 [a_rows][I], 16-byte aligned) then goes through
+ * moe_quant_rows_bf16 for the requantisation, which needs whole rows.
+ * Other arguments and limits as moe_grouped_gemm_i8 with N = 2I.  One launch. */
+moe_status moe_grouped_gemm_i8_swiglu(const void* a, int64_t a_rows, int32_t K,
+                                      const void* w_interleaved, int32_t G, int32_t I,
+                                      const int32_t* group_rows,
+                                      const float* col_scale_interleaved,
+                                      const void* row_scale, int64_t row_scale_stride,
+                                      float* h, int32_t* dev_status, void* stream);
+
+/* Weight preparation for moe_grouped_gemm_i8_swiglu: w1 int8 [G][2I][K]
+ * (rows 0..I-1 gate, I..2I-1 up) -> bf16 [G][2I][K] with row 2j = gate j and
+ * row 2j + 1 = up j (exact); ws1 fp32 [G][2I] permuted the same way.  One
+ * launch. */
+moe_status moe_interleave_gate_up(const void* w1, const float* ws1, int32_t G, int32_t I,
+                                  int32_t K, void* w1_interleaved,
+                                  float* ws1_interleaved, void* stream);
+
+/* The requantisation of the GMM1 epilogue on fp32 rows h [M][I]: per row,
+ * scale = 127 / (max|h| + 1e-12f), codes = round half to even of h * scale
+ * written as bf16 values [M][I] (exact), 1/scale to inv_scale[m].  With
+ * group_off (int64 [G+1]) rows at or past group_off[G] are not written;
+ * group_off may be NULL.  8 <= I <= 16384, I % 8 == 0.  One launch. */
+moe_status moe_quant_rows_bf16(const float* h, int64_t M, int32_t I, const int64_t* group_off,
+                               int32_t G, void* codes, float* inv_scale, void* stream);
 
 /* Combine over fp32 expert outputs [expert_out_rows][H] (e.g. the output of
  * moe_grouped_gemm_i8_dequant): acc = acc + (y * w), k in order, acc from 0,

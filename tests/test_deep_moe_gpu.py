@@ -176,9 +176,22 @@ def _deep_inputs(w, I, seed, device="cpu"):
 
 DEEP_CASES = [
     W.Workload("deep_small", R=2, epr=4, bs=96, H=256, k=4, seed=21),
+    W.Workload("deep_fp16", R=2, epr=3, bs=50, H=264, k=2, dtype=W.FP16, x_dist="uniform",
+               x_scale=4.0, seed=23),
     W.Workload("deep_ragged", R=3, epr=3, bs=70, H=1096, k=3, routing="zipf",
                weights="sigmoid", x_scale=2.0, seed=22),
 ]
+
+
+def _swiglu_bits(oracle, acc1, group_off, rows, ws1, ts, I):
+    """h of the GMM1 epilogue as int32 bit patterns, restated with numpy
+    float32 operations (one rounding each) and the oracle's exp."""
+    grp = np.searchsorted(group_off, rows, side="right") - 1
+    v = (acc1.astype(np.float32) * ws1[grp]) * ts[:, None].astype(np.float32)
+    gate, up = v[:, :I], v[:, I:]
+    e = oracle.exp_f32(-gate)
+    h = (gate / (e + np.float32(1.0))) * up
+    return h.astype(np.float32).view(np.int32)
 
 
 def _codes_bf16(images, K):
@@ -207,17 +220,27 @@ def test_deep_moe_pipeline(oracle_mod, ep, pl, w):
     _eq("expand_x", b.a1.view(torch.int16).cpu().numpy().view(np.uint16),
         _codes_bf16(recv, w.H))
     _eq("dynamic_scale", b.ts1.view(torch.int32), oracle_mod.row_inv_scale(recv, w.H).view(np.int32))
-    pl.run_deep_moe_experts(b, wts)
-    assert b.status() == 0, "experts"
-    pl.run_deep_combine(b, idx_d, wt_d)
-    assert b.status() == 0, "combine"
-    _eq("group_off", b.group_off, ref["group_off"])
-    _eq("acc1", b.acc1, ref["acc1"])
-    _eq("a2 codes", b.a2.view(torch.int16).cpu().numpy().view(np.uint16),
-        _codes_bf16(ref["x2"], I))
-    _eq("a2 1/scale", b.ts2.view(torch.int32), oracle_mod.row_inv_scale(ref["x2"], I).view(np.int32))
-    _eq("y2", b.y2.view(torch.int32), _dequant_bits(oracle_mod, ref, ws2.numpy(), I))
-    _eq("out", b.out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"])
+    for fused in (True, False):      # SwiGLU in GMM1's epilogue, or the standalone kernel
+        for t in (b.a2, b.ts2, b.y2, b.out):
+            t.zero_()
+        pl.run_deep_moe_experts(b, wts, fused_swiglu=fused)
+        assert b.status() == 0, "experts"
+        pl.run_deep_combine(b, idx_d, wt_d)
+        assert b.status() == 0, "combine"
+        tag = "(fused)" if fused else "(int32 + epilogue kernel)"
+        _eq("group_off", b.group_off, ref["group_off"])
+        if fused:
+            _eq("h" + tag, b.h.view(torch.int32),
+                _swiglu_bits(oracle_mod, ref["acc1"], ref["group_off"], ref["rows"],
+                             ws1.numpy(), oracle_mod.row_inv_scale(recv, w.H), I))
+        else:
+            _eq("acc1" + tag, b.acc1, ref["acc1"])
+        _eq("a2 codes" + tag, b.a2.view(torch.int16).cpu().numpy().view(np.uint16),
+            _codes_bf16(ref["x2"], I))
+        _eq("a2 1/scale" + tag, b.ts2.view(torch.int32),
+            oracle_mod.row_inv_scale(ref["x2"], I).view(np.int32))
+        _eq("y2" + tag, b.y2.view(torch.int32), _dequant_bits(oracle_mod, ref, ws2.numpy(), I))
+        _eq("out" + tag, b.out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"])
 
     # the INT8-row-image route gives the same intermediates and output
     pl.run_dispatch(b, x_d, idx_d)                                 # b.recv: INT8 rows
@@ -331,3 +354,17 @@ def test_deep_moe_graph_replay(oracle_mod, pl):
         ref = oracle_mod.deep_moe(W.bits(x), idx.numpy(), wt.numpy(), w.R, w.epr, w.dtype,
                                   w1.numpy(), ws1.numpy(), w2.numpy(), ws2.numpy())
         _eq("out(graph)", b.out.view(torch.int16).cpu().numpy().view(np.uint16), ref["out"])
+
+
+def test_deep_moe_empty_batch(pl):
+    w = W.Workload("deep_empty", R=2, epr=2, bs=0, H=128, k=2)
+    dev = torch.device("cuda")
+    _, _, _, (w1, ws1, w2, ws2) = _deep_inputs(w, 64, 3)
+    b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, 64, w.dtype)
+    wts = pl.DeepMoeWeights(w1.to(dev), ws1.to(dev), w2.to(dev), ws2.to(dev))
+    e = torch.zeros((0, w.k), device=dev)
+    pl.run_deep_moe(b, wts, torch.zeros((0, w.H), dtype=torch.bfloat16, device=dev),
+                    e.to(torch.int32), e)
+    torch.cuda.synchronize()
+    assert b.status() == 0
+    assert int(b.group_off[-1].item()) == 0
