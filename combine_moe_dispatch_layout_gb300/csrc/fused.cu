@@ -20,6 +20,12 @@
 //      rank_recv_base and maxBs) and dispatches tokens: rows resolved by one
 //      warp, max|x| by a block reduction, codes and 1/scale exactly as
 //      moe_dispatch (scale = 127/(amax + 1e-12f), round half to even).
+//      When the rows fit (STAGED), the CTA's first two x rows are requested
+//      with cp.async.bulk at kernel start, so they arrive while phases A-C
+//      run; each token's row image (or x itself, verbatim) is built in
+//      shared memory and written to its k rows with k bulk stores, and the
+//      token two steps ahead is loaded into the freed stage, as moe_dispatch
+//      does.  Otherwise threads store the image with 8-byte stores.
 //
 // The grid barrier is a generation counter in the workspace; a wait that
 // exceeds its bound (about a second) sets MOE_ERR_TIMEOUT and the CTA goes
@@ -88,7 +94,26 @@ struct Params {
   int32_t* dev_status;
 };
 
-template <int DT, bool QUANT>
+// Dynamic shared memory: warp counters, partition bases, then (STAGED) two
+// x stages, two image stages (QUANT) and two mbarriers.
+struct FusedSmem {
+  int64_t xs, os, bar, bytes;   // byte offsets of the x stages, images, barriers; total
+  int64_t x_stride, o_stride;
+};
+__host__ __device__ inline FusedSmem fused_smem(int R, int E, int H, int64_t row_bytes,
+                                                bool staged, bool quant) {
+  FusedSmem L;
+  const int64_t head = align_up(2 * kWarps * int64_t(E), 16) + 8 * int64_t(R + 1);
+  L.x_stride = staged ? align_up(int64_t(H) * 2, 128) : 0;
+  L.o_stride = staged && quant ? align_up(row_bytes, 128) : 0;
+  L.xs = align_up(head, 128);
+  L.os = L.xs + 2 * L.x_stride;
+  L.bar = L.os + 2 * L.o_stride;
+  L.bytes = staged ? L.bar + 16 : head;
+  return L;
+}
+
+template <int DT, bool QUANT, bool STAGED>
 __global__ void __launch_bounds__(kThreads)
 fused_dispatch_kernel(Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -104,8 +129,32 @@ fused_dispatch_kernel(Params p) {
 
   uint16_t* wcnt = reinterpret_cast<uint16_t*>(smem);                      // [8][E]
   int64_t* s_base = reinterpret_cast<int64_t*>(smem + align_up(2 * kWarps * E, 16));  // [R+1]
-  __shared__ int64_t s_rows[MOE_EP_MAX_TOPK];
+  __shared__ int64_t s_rows2[2][MOE_EP_MAX_TOPK];
+  int64_t* s_rows = s_rows2[0];
   __shared__ float s_wmax[kWarps];
+  __shared__ int s_abort;
+
+  const FusedSmem SL = fused_smem(R, E, H, p.row_bytes, STAGED, QUANT);
+  unsigned char* xs = smem + SL.xs;
+  unsigned char* os = smem + SL.os;
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + SL.bar);
+  const int64_t T = int64_t(R) * p.bs;
+  const uint32_t xbytes = static_cast<uint32_t>(H) * 2u;
+  int pend[2] = {-1, -1};   // thread 0: completion parity of the x load in flight per stage
+  if (STAGED && tid == 0) {  // this CTA's first two x rows arrive during phases A-C
+    mbar_init(&mbar[0], 1);
+    mbar_init(&mbar[1], 1);
+    fence_mbar_init();
+    for (int st = 0; st < 2; ++st) {
+      const int64_t gs = blockIdx.x + int64_t(st) * G;
+      if (gs < T) {
+        mbar_arrive_expect_tx(&mbar[st], xbytes);
+        bulk_load(xs + st * SL.x_stride, p.x + gs * xbytes, xbytes, &mbar[st]);
+        pend[st] = 0;
+      }
+    }
+  }
+  if (tid == 0) s_abort = 0;
 
   // ---- A: layout tiles -------------------------------------------------------
   for (int tile = blockIdx.x; tile < p.num_tiles; tile += G) {
@@ -253,12 +302,13 @@ fused_dispatch_kernel(Params p) {
     if (tid == 0) p.max_bs[0] = p.bs;
   }
   const int nch = H / 8;
-  const int64_t T = int64_t(R) * p.bs;
   const int h_align = static_cast<int>(align_up(H, 32));
   const int ntail = static_cast<int>((p.row_bytes - H) / 8);
   const int inv_word = (h_align - H) / 8;
-  for (int64_t g = blockIdx.x; g < T; g += G) {
+  int it = 0;
+  for (int64_t g = blockIdx.x; g < T; g += G, ++it) {
     const int s = static_cast<int>(g / p.bs);
+    if (STAGED) s_rows = s_rows2[it & 1];   // the previous token's stores may still read the other
     if (warp == 0) {
       for (int kk = lane; kk < k; kk += 32) {
         const int64_t q = g * k + kk;
@@ -275,6 +325,71 @@ fused_dispatch_kernel(Params p) {
         s_rows[kk] = row;
       }
     }
+    if constexpr (STAGED) {
+      const int b = it & 1;
+      const unsigned char* xsb = xs + b * SL.x_stride;
+      unsigned char* osb = os + b * SL.o_stride;
+      if (tid == 0 && QUANT) bulk_wait_read<1>();   // image b: iteration it-2's stores read it
+      if (!mbar_wait_bounded(&mbar[b], static_cast<uint32_t>(it >> 1) & 1u, kBarrierSpin)) {
+        set_status(p.dev_status, MOE_ERR_TIMEOUT);
+        s_abort = 1;
+      }
+      if constexpr (QUANT) {
+        float amax = 0.0f;
+        for (int c = tid; c < nch; c += kThreads) {
+          float f[8];
+          unpack8<DT>(*reinterpret_cast<const uint4*>(xsb + c * 16), f);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1)
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+        if (lane == 0) s_wmax[warp] = amax;
+      }
+      __syncthreads();   // (A) maxima, rows and the abort flag visible
+      if (s_abort) break;
+      if (tid == 0) pend[b] = -1;
+      if constexpr (QUANT) {
+        float amax = s_wmax[0];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, s_wmax[w]);
+        const float scale = __fdiv_rn(127.0f, __fadd_rn(amax, 1e-12f));
+        const float inv = __fdiv_rn(1.0f, scale);
+        for (int c = tid; c < nch; c += kThreads) {
+          float f[8];
+          unpack8<DT>(*reinterpret_cast<const uint4*>(xsb + c * 16), f);
+          uint32_t w2[2] = {0u, 0u};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int qv = __float2int_rn(__fmul_rn(f[j], scale));
+            w2[j >> 2] |= (static_cast<uint32_t>(qv) & 0xffu) << (8 * (j & 3));
+          }
+          *reinterpret_cast<uint2*>(osb + c * 8) = make_uint2(w2[0], w2[1]);
+        }
+        if (tid < ntail)
+          *reinterpret_cast<uint2*>(osb + H + 8 * tid) =
+              make_uint2(tid == inv_word ? __float_as_uint(inv) : 0u, 0u);
+        fence_proxy_async_smem();
+        __syncthreads();   // (B) the image is complete; x stage b is free
+      }
+      if (tid == 0) {
+        const unsigned char* src = QUANT ? osb : xsb;
+        for (int kk = 0; kk < k; ++kk)
+          if (s_rows[kk] >= 0)
+            bulk_store(p.recv + s_rows[kk] * p.row_bytes, src,
+                       static_cast<uint32_t>(p.row_bytes));
+        bulk_commit();
+        if (!QUANT) bulk_wait_read<0>();   // the stores read x stage b; refill it
+        const int64_t g2 = g + 2 * int64_t(G);
+        if (g2 < T) {
+          mbar_arrive_expect_tx(&mbar[b], xbytes);
+          bulk_load(const_cast<unsigned char*>(xsb), p.x + g2 * xbytes, xbytes, &mbar[b]);
+          pend[b] = ((it + 2) >> 1) & 1;
+        }
+      }
+      continue;
+    } else {
     const uint4* xrow = reinterpret_cast<const uint4*>(p.x + g * int64_t(H) * 2);
     if constexpr (QUANT) {
       float amax = 0.0f;
@@ -326,22 +441,29 @@ fused_dispatch_kernel(Params p) {
         }
       }
     }
+    }
     __syncthreads();   // s_rows and s_wmax are reused by the next token
   }
-}
-
-size_t smem_bytes(int R, int E) {
-  return static_cast<size_t>(align_up(2 * kWarps * int64_t(E), 16) + 8 * int64_t(R + 1));
+  if (STAGED && tid == 0) {
+    bulk_wait_all<0>();   // stores done before shared memory goes away
+    for (int st = 0; st < 2; ++st)   // only after an abort: loads still in flight
+      if (pend[st] >= 0 &&
+          !mbar_wait_bounded(&mbar[st], static_cast<uint32_t>(pend[st]), kBarrierSpin))
+        set_status(p.dev_status, MOE_ERR_TIMEOUT);
+  }
 }
 
 int tiles_per_rank_of(const Shape& s) {
   return static_cast<int>((int64_t(s.bs) * s.k + kTile - 1) / kTile);
 }
 
-template <int DT, bool QUANT>
+constexpr int64_t kStagedSmemMax = 110 * 1024;   // two CTAs per SM still fit
+
+template <int DT, bool QUANT, bool STAGED>
 cudaError_t launch_t(const Shape& s, Params p, cudaStream_t st) {
-  auto kernel = fused_dispatch_kernel<DT, QUANT>;
-  const size_t smem = smem_bytes(s.R, s.E());
+  auto kernel = fused_dispatch_kernel<DT, QUANT, STAGED>;
+  const size_t smem = static_cast<size_t>(
+      fused_smem(s.R, s.E(), s.H, p.row_bytes, STAGED, QUANT).bytes);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   int dev = 0, sms = 0, per_sm = 0;
@@ -396,9 +518,20 @@ cudaError_t launch_fused_dispatch(const Shape& s, const void* x, const int32_t* 
   p.capacity = capacity;
   p.workspace = workspace;
   p.dev_status = dev_status;
-  if (s.dtype == MOE_BF16)
-    return quant ? launch_t<MOE_BF16, true>(s, p, st) : launch_t<MOE_BF16, false>(s, p, st);
-  return quant ? launch_t<MOE_FP16, true>(s, p, st) : launch_t<MOE_FP16, false>(s, p, st);
+  const bool staged =
+      fused_smem(s.R, s.E(), s.H, row_bytes, true, quant).bytes <= kStagedSmemMax;
+  if (s.dtype == MOE_BF16) {
+    if (quant)
+      return staged ? launch_t<MOE_BF16, true, true>(s, p, st)
+                    : launch_t<MOE_BF16, true, false>(s, p, st);
+    return staged ? launch_t<MOE_BF16, false, true>(s, p, st)
+                  : launch_t<MOE_BF16, false, false>(s, p, st);
+  }
+  if (quant)
+    return staged ? launch_t<MOE_FP16, true, true>(s, p, st)
+                  : launch_t<MOE_FP16, true, false>(s, p, st);
+  return staged ? launch_t<MOE_FP16, false, true>(s, p, st)
+                : launch_t<MOE_FP16, false, false>(s, p, st);
 }
 
 }  // namespace moe_ep
