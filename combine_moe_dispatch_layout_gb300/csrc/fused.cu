@@ -94,8 +94,13 @@ struct Params {
   int32_t* dev_status;
 };
 
-// Dynamic shared memory: warp counters, partition bases, then (STAGED) two
-// x stages, two image stages (QUANT) and two mbarriers.
+// x stages of the token phase: two with the INT8 image (the block computes
+// each token), four on the verbatim path (one warp copies, stages refilled
+// three tokens ahead).
+constexpr int kQuantStages = 2, kCopyStages = 4;
+
+// Dynamic shared memory: warp counters, partition bases, then (STAGED) the x
+// stages, two image stages (QUANT) and one mbarrier per x stage.
 struct FusedSmem {
   int64_t xs, os, bar, bytes;   // byte offsets of the x stages, images, barriers; total
   int64_t x_stride, o_stride;
@@ -103,13 +108,14 @@ struct FusedSmem {
 __host__ __device__ inline FusedSmem fused_smem(int R, int E, int H, int64_t row_bytes,
                                                 bool staged, bool quant) {
   FusedSmem L;
+  const int nst = quant ? kQuantStages : kCopyStages;
   const int64_t head = align_up(2 * kWarps * int64_t(E), 16) + 8 * int64_t(R + 1);
   L.x_stride = staged ? align_up(int64_t(H) * 2, 128) : 0;
   L.o_stride = staged && quant ? align_up(row_bytes, 128) : 0;
   L.xs = align_up(head, 128);
-  L.os = L.xs + 2 * L.x_stride;
+  L.os = L.xs + nst * L.x_stride;
   L.bar = L.os + 2 * L.o_stride;
-  L.bytes = staged ? L.bar + 16 : head;
+  L.bytes = staged ? L.bar + 8 * nst : head;
   return L;
 }
 
@@ -140,12 +146,14 @@ fused_dispatch_kernel(Params p) {
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + SL.bar);
   const int64_t T = int64_t(R) * p.bs;
   const uint32_t xbytes = static_cast<uint32_t>(H) * 2u;
-  int pend[2] = {-1, -1};   // thread 0: completion parity of the x load in flight per stage
-  if (STAGED && tid == 0) {  // this CTA's first two x rows arrive during phases A-C
-    mbar_init(&mbar[0], 1);
-    mbar_init(&mbar[1], 1);
+  constexpr int kNst = QUANT ? kQuantStages : kCopyStages;
+  int pend[kNst];           // thread 0: completion parity of the x load in flight per stage
+#pragma unroll
+  for (int st = 0; st < kNst; ++st) pend[st] = -1;
+  if (STAGED && tid == 0) {  // this CTA's first x rows arrive during phases A-C
+    for (int st = 0; st < kNst; ++st) mbar_init(&mbar[st], 1);
     fence_mbar_init();
-    for (int st = 0; st < 2; ++st) {
+    for (int st = 0; st < kNst; ++st) {
       const int64_t gs = blockIdx.x + int64_t(st) * G;
       if (gs < T) {
         mbar_arrive_expect_tx(&mbar[st], xbytes);
@@ -305,6 +313,60 @@ fused_dispatch_kernel(Params p) {
   const int h_align = static_cast<int>(align_up(H, 32));
   const int ntail = static_cast<int>((p.row_bytes - H) / 8);
   const int inv_word = (h_align - H) / 8;
+  if constexpr (STAGED && !QUANT) {
+    // verbatim: warp 0 alone; lane 0 waits for a token's x row, stores it to
+    // the k rows and refills the previous token's stage (its stores have read
+    // it once at most one group -- this token's -- is still reading)
+    if (warp == 0) {
+      int it = 0;
+      for (int64_t g = blockIdx.x; g < T; g += G, ++it) {
+        int64_t* rows = s_rows2[it & 1];
+        const int s = static_cast<int>(g / p.bs);
+        for (int kk = lane; kk < k; kk += 32) {
+          const int64_t q = g * k + kk;
+          const int e = __ldg(p.topk_idx + q);
+          int64_t row = -1;
+          if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
+            row = s_base[e / epr] + __ldcg(p.put_offset + int64_t(e) * R + s) +
+                  __ldcg(p.send_idx + q);
+            if (row < 0 || row >= p.capacity) {
+              set_status(p.dev_status, MOE_ERR_CAPACITY);
+              row = -1;
+            }
+          }
+          rows[kk] = row;
+        }
+        __syncwarp();
+        int ab = 0;
+        if (lane == 0) {
+          const int b = it % kNst;
+          if (!mbar_wait_bounded(&mbar[b], static_cast<uint32_t>(it / kNst) & 1u,
+                                 kBarrierSpin)) {
+            set_status(p.dev_status, MOE_ERR_TIMEOUT);
+            ab = 1;
+          } else {
+            pend[b] = -1;
+            for (int kk = 0; kk < k; ++kk)
+              if (rows[kk] >= 0)
+                bulk_store(p.recv + rows[kk] * p.row_bytes, xs + b * SL.x_stride,
+                           static_cast<uint32_t>(p.row_bytes));
+            bulk_commit();
+            if (it >= 1) {
+              bulk_wait_read<1>();
+              const int pb = (it - 1) % kNst;
+              const int64_t gn = g + int64_t(kNst - 1) * G;   // iteration it - 1 + kNst
+              if (gn < T) {
+                mbar_arrive_expect_tx(&mbar[pb], xbytes);
+                bulk_load(xs + pb * SL.x_stride, p.x + gn * xbytes, xbytes, &mbar[pb]);
+                pend[pb] = ((it - 1 + kNst) / kNst) & 1;
+              }
+            }
+          }
+        }
+        if (__shfl_sync(0xffffffffu, ab, 0)) break;
+      }
+    }
+  } else {
   int it = 0;
   for (int64_t g = blockIdx.x; g < T; g += G, ++it) {
     const int s = static_cast<int>(g / p.bs);
@@ -325,7 +387,7 @@ fused_dispatch_kernel(Params p) {
         s_rows[kk] = row;
       }
     }
-    if constexpr (STAGED) {
+    if constexpr (STAGED) {   // QUANT here: the verbatim path runs above
       const int b = it & 1;
       const unsigned char* xsb = xs + b * SL.x_stride;
       unsigned char* osb = os + b * SL.o_stride;
@@ -444,9 +506,10 @@ fused_dispatch_kernel(Params p) {
     }
     __syncthreads();   // s_rows and s_wmax are reused by the next token
   }
+  }
   if (STAGED && tid == 0) {
     bulk_wait_all<0>();   // stores done before shared memory goes away
-    for (int st = 0; st < 2; ++st)   // only after an abort: loads still in flight
+    for (int st = 0; st < kNst; ++st)   // only after an abort: loads still in flight
       if (pend[st] >= 0 &&
           !mbar_wait_bounded(&mbar[st], static_cast<uint32_t>(pend[st]), kBarrierSpin))
         set_status(p.dev_status, MOE_ERR_TIMEOUT);
