@@ -16,8 +16,8 @@
 // Kernel: persistent CTAs (one per SM) walk 128 x 256 output tiles (the last
 // column tile may be ragged: its B rows past the expert are computed from
 // the next expert's rows, or zero-filled by TMA, and never stored; tiles of
-// one expert together, m fastest, so the expert's weights and rows are
-// reused from L2).  Warp 0 streams 128 x 64 (A) and 256 x 64 (B) bf16 tiles
+// one expert together, in blocks of 8 row tiles with the row tile fastest,
+// so the expert's weights and rows are reused from L2).  Warp 0 streams 128 x 64 (A) and 256 x 64 (B) bf16 tiles
 // into a 4-stage shared-memory ring with TMA (cp.async.bulk.tensor, 128-byte
 // swizzle; 192 KB in flight per SM, which the L2 latency needs); warp 1
 // allocates all 512 TMEM columns and one elected lane issues tcgen05.mma
@@ -38,6 +38,7 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;   // BK bf16 = one 128-byte swizzle row
 constexpr int kChunkBlocks = 16;             // 16 x 64 = 1024: exact fp32 partial sums
+constexpr int kRasterM = 8;                  // row tiles per raster block (L2 reuse of A)
 constexpr uint32_t kTmemCols = 2 * BN;       // two chunk accumulators (all of TMEM)
 constexpr int kEpiWarps = 8;                 // 4 TMEM lane quarters x 2 column halves
 constexpr int kThreads = 64 + 32 * kEpiWarps;   // TMA warp, MMA warp, epilogue
@@ -176,7 +177,24 @@ __device__ __forceinline__ Tile decode_tile(int64_t t, const int64_t* goff,
   const int64_t cnt = goff[g + 1] - goff[g];
   const int mt = static_cast<int>((cnt + BM - 1) / BM);
   const int local = static_cast<int>(t - tpre[g]);
-  const int m = local % mt, n = local / mt;
+  // blocks of row tiles: inside a block m is fastest, then n, so the tiles
+  // in flight together touch a bounded number of A's row tiles however large
+  // the expert is; all blocks have kRasterM row tiles except the last, which
+  // takes the remainder too (kRasterM .. 2*kRasterM - 1; an expert of fewer
+  // than 2*kRasterM row tiles is one block), so no short block re-reads B
+  const int nblk = mt / kRasterM > 0 ? mt / kRasterM : 1;
+  const int full = nblk - 1, per_full = kRasterM * ntn;
+  const int blk = local / per_full;
+  int m, n;
+  if (blk < full) {
+    const int r = local - blk * per_full;
+    m = blk * kRasterM + r % kRasterM;
+    n = r / kRasterM;
+  } else {
+    const int rem = mt - full * kRasterM, r = local - full * per_full;
+    m = full * kRasterM + r % rem;
+    n = r / rem;
+  }
   Tile tl;
   tl.g = g;
   tl.row0 = goff[g] + int64_t(m) * BM;
