@@ -11,6 +11,14 @@
  * its BarrierAll / magic-counter protocol (section 2.7) is replaced by
  * stream order between the four calls.
  *
+ * Entry points, in groups: the four stages (moe_dispatch_layout,
+ * moe_notify_dispatch, moe_dispatch, moe_combine) and their size queries;
+ * variants of them (moe_dispatch_layout_static, moe_dispatch_fused -- layout,
+ * notify and dispatch in one launch -- and moe_combine_quant,
+ * moe_token_layout); and the fused deep MoE of section 4 (moe_dispatch_expand,
+ * moe_group_offsets, the grouped INT8 GEMMs on the tensor cores, the GMM1
+ * epilogue moe_swiglu_quant*, moe_combine_f32 / moe_deq_combine).
+ *
  * Notation: R ranks, epr experts per rank, E = R*epr experts, bs tokens per
  * rank, T = R*bs tokens, k experts per token, P = T*k (token, k) pairs,
  * H hidden size.  Token g = s*bs + t belongs to source rank s; expert e
