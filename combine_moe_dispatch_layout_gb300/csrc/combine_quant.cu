@@ -4,13 +4,20 @@
 // ReadBufferAndWeightedSum.
 //
 // Each expert-output row is a dispatched-style INT8 row image (codes, fp32
-// 1/scale at align32(H)).  Same persistent producer/compute structure as
-// combine.cu: the producer warp resolves the next token's rows and weights
-// and also fetches each row's 1/scale; compute threads load 16 codes per
-// 16-byte load (8 rows in flight) and dequantise every element as
-// float(q) * (1/scale) (one rounding) before the same multiply-then-add
-// (__fmul_rn / __fadd_rn, k in order), then round to the token dtype.
-// Rows are half the bytes of bf16 rows.
+// 1/scale at align32(H)).  Every element is dequantised as float(q) *
+// (1/scale) (one rounding) before the combine's multiply-then-add
+// (__fmul_rn / __fadd_rn, k in order), then rounded to the token dtype.
+//
+// Work is split per warp, with no block barrier: a work item is one token,
+// or a contiguous part of its hidden dimension when that evens out the last
+// round over the grid's warps.  The warp resolves the item's k rows, weights
+// and 1/scales into its own shared-memory table, then each lane walks
+// 8-code chunks of the item (one 8-byte load per row, 8 rows per batch),
+// issuing the next (chunk, batch)'s loads before it computes the current
+// one.  Per element: a sign-extending byte permute, an int-to-float
+// conversion, two multiplies and an add -- the arithmetic is about as long
+// as the HBM time, so keeping loads in flight across the compute is what
+// matters.  Rows are half the bytes of bf16 rows.
 #include <algorithm>
 
 #include "moe_ep_internal.cuh"
@@ -19,9 +26,7 @@ namespace moe_ep {
 
 namespace {
 
-constexpr int kBatch = 8;          // expert rows loaded before accumulating
-
-constexpr int kQuantMaxThreads = 512;
+constexpr int kCqWarps = 8;   // warps per CTA, each on its own work item
 
 __device__ __forceinline__ uint2 ld_stream_8(const void* p) {
   uint2 v;
@@ -31,129 +36,223 @@ __device__ __forceinline__ uint2 ld_stream_8(const void* p) {
   return v;
 }
 
-// The i-th signed byte of a 32-bit word, as float (exact).
-__device__ __forceinline__ float code_f(uint32_t w, int i) {
-  return static_cast<float>(static_cast<int32_t>(w << (24 - 8 * i)) >> 24);
+// Byte i of w, sign-extended (byte permute), converted to float (exact).
+template <int I>
+__device__ __forceinline__ float code_f(uint32_t w) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(w), "n"(0x8880 | (I * 0x1111)));
+  return __int2float_rn(static_cast<int32_t>(r));
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kQuantMaxThreads)
+// One row of the warp's table: the row's first byte (nullptr for padding or
+// a rejected pair), its weight and its 1/scale (both 0 then).
+struct __align__(16) RowRef {
+  const unsigned char* p;
+  float w;
+  float inv;
+};
+
+// KB: rows per batch.  MULTI = false: KB == k (one batch, no padding).
+// MULTI = true: KB = 8, k > 8 split into batches, the last one padded.
+template <int DT, int KB, bool MULTI>
+__global__ void __launch_bounds__(kCqWarps * 32, 3)
 combine_quant_kernel(const unsigned char* __restrict__ yq, int64_t y_rows,
                      int64_t row_bytes, const int32_t* __restrict__ topk_idx,
                      const float* __restrict__ weights,
                      const int32_t* __restrict__ send_idx,
                      const int32_t* __restrict__ put_offset,
                      const int64_t* __restrict__ rank_recv_base, int R, int bs,
-                     int k, int epr, int H, int64_t T, uint4* __restrict__ out,
-                     int32_t* dev_status) {
-  __shared__ int64_t s_rows[2][MOE_EP_MAX_TOPK];
-  __shared__ float s_w[2][MOE_EP_MAX_TOPK];
-  __shared__ float s_inv[2][MOE_EP_MAX_TOPK];
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int ncomp = blockDim.x - 32;
-  const bool producer = tid >= ncomp;
-  const int nq = (H + 15) / 16;                 // 16-code chunks (last may be 8)
+                     int k, int epr, int H, int64_t T, int parts,
+                     uint4* __restrict__ out, int32_t* dev_status) {
+  __shared__ RowRef s_ref[kCqWarps][MOE_EP_MAX_TOPK];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  RowRef* ref = s_ref[warp];
+  const int E = R * epr;
+  const int nch = H / 8;                         // 8-code chunks per row
   const int64_t h_align = align_up(H, 32);
-  const int nch8 = H / 8;                       // uint4 outputs per row
+  const int nb = MULTI ? (k + KB - 1) / KB : 1;
+  const int64_t items = T * parts;
+  const int64_t nwarps = int64_t(gridDim.x) * kCqWarps;
 
-  auto resolve = [&](int64_t gt, int b) {
-    resolve_token(gt, topk_idx, weights, send_idx, put_offset, rank_recv_base, R, bs,
-                  k, epr, y_rows, s_rows[b], s_w[b], dev_status, lane);
-    __syncwarp();
-    for (int kk = lane; kk < k; kk += 32) {
-      const int64_t row = s_rows[b][kk];
-      s_inv[b][kk] = row >= 0 ? __ldg(reinterpret_cast<const float*>(
-                                    yq + row * row_bytes + h_align))
-                              : 0.0f;
+  for (int64_t item = int64_t(blockIdx.x) * kCqWarps + warp; item < items; item += nwarps) {
+    const int64_t g = item / parts;
+    const int part = static_cast<int>(item - g * parts);
+    const int c0 = static_cast<int>(int64_t(nch) * part / parts);
+    const int c1 = static_cast<int>(int64_t(nch) * (part + 1) / parts);
+    __syncwarp();                                 // the last item's readers are done
+    const int s = static_cast<int>(g / bs);
+    for (int kk = lane; kk < nb * KB; kk += 32) {
+      RowRef r{nullptr, 0.0f, 0.0f};
+      if (kk < k) {
+        const int64_t pair = g * k + kk;
+        const int e = __ldg(topk_idx + pair);
+        const int32_t sidx = __ldg(send_idx + pair);
+        const float wt = __ldg(weights + pair);
+        if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
+          set_status(dev_status, MOE_ERR_EXPERT_ID);
+        } else {
+          const int64_t row =
+              __ldg(rank_recv_base + e / epr) + __ldg(put_offset + int64_t(e) * R + s) + sidx;
+          if (row < 0 || row >= y_rows) {
+            set_status(dev_status, MOE_ERR_CAPACITY);
+          } else {
+            r.p = yq + row * row_bytes;
+            r.w = wt;
+            r.inv = __ldg(reinterpret_cast<const float*>(r.p + h_align));
+          }
+        }
+      }
+      ref[kk] = r;
     }
-  };
+    __syncwarp();
 
-  int64_t g = blockIdx.x;
-  if (producer) resolve(g, 0);
-  __syncthreads();
-
-  for (int it = 0; g < T; ++it, g += gridDim.x) {
-    const int buf = it & 1;
-    if (producer) {
-      __syncwarp();
-      const int64_t gn = g + gridDim.x;
-      if (gn < T) resolve(gn, buf ^ 1);
+    // A rejected row (p == nullptr) is not loaded; its register keeps older
+    // codes, which contribute (q * 0) * 0 = +-0 and leave acc unchanged (acc
+    // is never -0: it starts at +0 and a round-to-nearest sum is -0 only
+    // when both terms are).
+    auto load = [&](int c, int b, uint2 (&v)[KB]) {
+#pragma unroll
+      for (int j = 0; j < KB; ++j) {
+        const unsigned char* p = ref[b * KB + j].p;
+        if (p != nullptr) v[j] = ld_stream_8(p + 8 * int64_t(c));
+      }
+    };
+    auto accumulate = [&](int b, const uint2 (&v)[KB], float (&acc)[8]) {
+#pragma unroll
+      for (int j = 0; j < KB; ++j) {
+        if (!MULTI || b * KB + j < k) {           // warp-uniform: padding rows skipped
+          const float2 wi = *reinterpret_cast<const float2*>(&ref[b * KB + j].w);
+          const float wk = wi.x, sk = wi.y;
+          const uint32_t lo = v[j].x, hi = v[j].y;
+          const float q[8] = {code_f<0>(lo), code_f<1>(lo), code_f<2>(lo), code_f<3>(lo),
+                              code_f<0>(hi), code_f<1>(hi), code_f<2>(hi), code_f<3>(hi)};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float t = __fmul_rn(q[e], sk);                 // dequantise
+            acc[e] = __fadd_rn(acc[e], __fmul_rn(t, wk));        // Muls, Add
+          }
+        }
+      }
+    };
+    uint2 va[KB], vb[KB];
+#pragma unroll
+    for (int j = 0; j < KB; ++j) va[j] = vb[j] = make_uint2(0u, 0u);
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    int c = c0 + lane;
+    if (!MULTI) {
+      // One batch per chunk; two register sets alternate (chunk c + 32 loads
+      // while chunk c computes).
+      auto finish = [&](int cc) {
+        out[g * nch + cc] = pack8<DT>(acc);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+      };
+      if (c < c1) load(c, 0, va);
+      while (c < c1) {
+        if (c + 32 < c1) load(c + 32, 0, vb);
+        accumulate(0, va, acc);
+        finish(c);
+        c += 32;
+        if (c >= c1) break;
+        if (c + 32 < c1) load(c + 32, 0, va);
+        accumulate(0, vb, acc);
+        finish(c);
+        c += 32;
+      }
     } else {
-      const int64_t* rows = s_rows[buf];
-      const float* w = s_w[buf];
-      const float* inv = s_inv[buf];
-      for (int c = tid; c < nq; c += ncomp) {
-        const bool half = 16 * c + 8 >= H;      // only 8 codes left
-        float acc[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-        for (int k0 = 0; k0 < k; k0 += kBatch) {
-          uint4 v[kBatch];
-#pragma unroll
-          for (int b = 0; b < kBatch; ++b) {
-            const int kk = k0 + b;
-            const int64_t row = kk < k ? rows[kk] : -1;
-            v[b] = make_uint4(0u, 0u, 0u, 0u);
-            if (row >= 0) {
-              const unsigned char* src = yq + row * row_bytes + 16 * c;
-              if (half) {
-                const uint2 h2 = ld_stream_8(src);
-                v[b].x = h2.x;
-                v[b].y = h2.y;
-              } else {
-                v[b] = ld_stream_16(src);
-              }
-            }
-          }
-#pragma unroll
-          for (int b = 0; b < kBatch; ++b) {
-            const int kk = k0 + b;
-            if (kk < k && rows[kk] >= 0) {
-              const float wk = w[kk], sk = inv[kk];
-              const uint32_t wd[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float t = __fmul_rn(code_f(wd[j >> 2], j & 3), sk);   // dequantise
-                acc[j] = __fadd_rn(acc[j], __fmul_rn(t, wk));              // Muls, Add
-              }
-            }
-          }
+      // (chunk, batch) positions in order: batch fastest, chunks lane-strided.
+      int b = 0;
+      if (c < c1) load(c, b, va);
+      while (c < c1) {
+        int cn = c, bn = b + 1;
+        if (bn == nb) {
+          bn = 0;
+          cn = c + 32;
         }
-        float lo[8], hi[8];
+        if (cn < c1) load(cn, bn, vb);
+        accumulate(b, va, acc);
+        if (bn == 0) {
+          out[g * nch + c] = pack8<DT>(acc);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          lo[j] = acc[j];
-          hi[j] = acc[8 + j];
+          for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
         }
-        out[g * nch8 + 2 * c] = pack8<DT>(lo);
-        if (!half) out[g * nch8 + 2 * c + 1] = pack8<DT>(hi);
+        c = cn;
+        b = bn;
+#pragma unroll
+        for (int j = 0; j < KB; ++j) va[j] = vb[j];
       }
     }
-    __syncthreads();
   }
 }
 
-template <int DT>
+// Parts per token: the smallest split (1, 2, 4 or 8; each part at least 32
+// chunks) whose last round over the grid's warps is at least 97% full, else
+// the fullest.
+int parts_for(int64_t T, int nch, int64_t warps) {
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= 8; s *= 2) {
+    if (s > 1 && nch / s < 32) break;
+    const int64_t n = T * s;
+    const int64_t rounds = (n + warps - 1) / warps;
+    const double eff = double(n) / double(rounds * warps);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+    if (eff >= 0.97) break;
+  }
+  return best;
+}
+
+template <int DT, int KB, bool MULTI>
 cudaError_t launch_quant_t(const Shape& s, const void* yq, int64_t y_rows,
                            const int32_t* topk_idx, const float* weights,
                            const int32_t* send_idx, const int32_t* put_offset,
                            const int64_t* rank_recv_base, void* out,
                            int32_t* dev_status, cudaStream_t st) {
-  const int nq = (s.H + 15) / 16;
-  const int ncomp = std::max(32, std::min(kQuantMaxThreads - 32, ((nq + 3) / 4 + 31) / 32 * 32));
-  const int threads = ncomp + 32;
+  constexpr int threads = kCqWarps * 32;
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_quant_kernel<DT>, threads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, combine_quant_kernel<DT, KB, MULTI>, threads, 0);
   if (e != cudaSuccess) return e;
-  const int64_t grid = std::min<int64_t>(s.T(), int64_t(std::max(1, per_sm)) * sms);
-  combine_quant_kernel<DT><<<static_cast<unsigned>(grid), threads, 0, st>>>(
+  const int64_t max_ctas = int64_t(std::max(1, per_sm)) * sms;
+  const int parts = parts_for(s.T(), s.H / 8, max_ctas * kCqWarps);
+  const int64_t items = s.T() * parts;
+  const int64_t grid = std::min<int64_t>((items + kCqWarps - 1) / kCqWarps, max_ctas);
+  combine_quant_kernel<DT, KB, MULTI><<<static_cast<unsigned>(grid), threads, 0, st>>>(
       static_cast<const unsigned char*>(yq), y_rows, align_up(s.H, 32) + 32, topk_idx,
-      weights, send_idx, put_offset, rank_recv_base, s.R, s.bs, s.k, s.epr, s.H, s.T(),
+      weights, send_idx, put_offset, rank_recv_base, s.R, s.bs, s.k, s.epr, s.H, s.T(), parts,
       static_cast<uint4*>(out), dev_status);
   return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_quant_dt(const Shape& s, const void* yq, int64_t y_rows,
+                            const int32_t* topk_idx, const float* weights,
+                            const int32_t* send_idx, const int32_t* put_offset,
+                            const int64_t* rank_recv_base, void* out, int32_t* dev_status,
+                            cudaStream_t st) {
+#define MOE_CQ_LAUNCH(KB_, MULTI_)                                                           \
+  return launch_quant_t<DT, KB_, MULTI_>(s, yq, y_rows, topk_idx, weights, send_idx,       \
+                                         put_offset, rank_recv_base, out, dev_status, st)
+  switch (s.k) {
+    case 1: MOE_CQ_LAUNCH(1, false);
+    case 2: MOE_CQ_LAUNCH(2, false);
+    case 3: MOE_CQ_LAUNCH(3, false);
+    case 4: MOE_CQ_LAUNCH(4, false);
+    case 5: MOE_CQ_LAUNCH(5, false);
+    case 6: MOE_CQ_LAUNCH(6, false);
+    case 7: MOE_CQ_LAUNCH(7, false);
+    case 8: MOE_CQ_LAUNCH(8, false);
+    default: MOE_CQ_LAUNCH(8, true);
+  }
+#undef MOE_CQ_LAUNCH
 }
 
 }  // namespace
@@ -165,10 +264,10 @@ cudaError_t launch_combine_quant(const Shape& s, const void* yq, int64_t y_rows,
                                  int32_t* dev_status, cudaStream_t st) {
   if (s.T() == 0) return cudaSuccess;
   if (s.dtype == MOE_BF16)
-    return launch_quant_t<MOE_BF16>(s, yq, y_rows, topk_idx, weights, send_idx,
-                                    put_offset, rank_recv_base, out, dev_status, st);
-  return launch_quant_t<MOE_FP16>(s, yq, y_rows, topk_idx, weights, send_idx,
-                                  put_offset, rank_recv_base, out, dev_status, st);
+    return launch_quant_dt<MOE_BF16>(s, yq, y_rows, topk_idx, weights, send_idx,
+                                     put_offset, rank_recv_base, out, dev_status, st);
+  return launch_quant_dt<MOE_FP16>(s, yq, y_rows, topk_idx, weights, send_idx,
+                                   put_offset, rank_recv_base, out, dev_status, st);
 }
 
 }  // namespace moe_ep

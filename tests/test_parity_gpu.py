@@ -356,6 +356,8 @@ def test_combine_quant_full_size(oracle_mod, pl, name):
     dict(R=5, epr=3, bs=400, k=4, H=136, dtype=W.FP16),    # fp16 out, half chunk
     dict(R=4, epr=2, bs=300, k=1, H=64),                   # k = 1
     dict(R=2, epr=4, bs=50, k=8, H=65536),                 # widest rows
+    dict(R=4, epr=8, bs=200, k=13, H=520),                 # two row batches, 8-code tail
+    dict(R=8, epr=8, bs=64, k=64, H=256),                  # largest k
 ], ids=lambda c: "-".join("%s%s" % kv for kv in c.items()))
 def test_combine_quant_mid(oracle_mod, pl, case):
     _check_combine_quant(oracle_mod, pl, W.Workload("cq", **case))
