@@ -159,6 +159,164 @@ swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc 
   }
 }
 
+// Warp-per-row-block form (I <= kWarpMaxI): each warp takes a contiguous
+// block of rows and walks them in 8-output chunks (lane-strided), with the
+// next (row, chunk)'s accumulators loaded while the current chunk computes.
+// h goes to the warp's shared buffer [I]; max|h| is a warp reduction (no
+// block barrier); a second pass over the buffer quantises and stores.
+constexpr int kWarpMaxI = 4096;
+constexpr int kWarpSmemBudget = 64 * 1024;   // h buffers per CTA
+
+template <bool BF16OUT>
+__global__ void __launch_bounds__(256, 3)
+swiglu_quant_warp_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc sc,
+                         unsigned char* __restrict__ out, int64_t row_bytes,
+                         float* __restrict__ out_scale) {
+  extern __shared__ float4 s_hbuf[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
+  float* hb = reinterpret_cast<float*>(s_hbuf) + int64_t(warp) * I;
+  const int nch = I / 8;
+  const int i_align = static_cast<int>(align_up(I, 32));
+  const int ntail = static_cast<int>((row_bytes - I) / 8);
+  const int inv_word = (i_align - I) / 8;
+  if (sc.group_off) {
+    const int64_t rows = __ldg(sc.group_off + sc.G);
+    if (rows < M) M = rows;
+  }
+  const int64_t nw = int64_t(gridDim.x) * W;
+  const int64_t per = (M + nw - 1) / nw;
+  const int64_t m0 = (int64_t(blockIdx.x) * W + warp) * per;
+  const int64_t m1 = m0 + per < M ? m0 + per : M;
+  if (m0 >= m1) return;                       // no block-level synchronisation below
+
+  // Accumulators of chunk c of row m: gate words g0, g1, up words u0, u1.
+  struct Acc { uint4 g0, g1, u0, u1; };
+  auto load = [&](int64_t m, int c, Acc& a) {
+    const int32_t* row = acc + m * 2 * int64_t(I);
+    a.g0 = ld_stream_16(row + 8 * c);
+    a.g1 = ld_stream_16(row + 8 * c + 4);
+    a.u0 = ld_stream_16(row + I + 8 * c);
+    a.u1 = ld_stream_16(row + I + 8 * c + 4);
+  };
+
+  int grp = 0;
+  int64_t pm = m0;                             // position of `cur`
+  int pc = lane;
+  Acc cur{}, nxt{};
+  if (pc < nch) load(pm, pc, cur);
+  for (int64_t m = m0; m < m1; ++m) {
+    const float ts = __ldg(reinterpret_cast<const float*>(sc.ts_base + m * sc.ts_stride));
+    const float* weight_scale = sc.weight_scale;
+    if (sc.group_off) {                        // largest g with group_off[g] <= m
+      while (grp + 1 < sc.G && __ldg(sc.group_off + grp + 1) <= m) ++grp;
+      weight_scale += int64_t(grp) * 2 * I;
+    }
+    float amax = 0.0f;
+    for (int c = lane; c < nch; c += 32) {
+      // Prefetch the lane's next position: the next chunk of this row, else
+      // its first chunk of the next row.
+      int64_t qm = pm;
+      int qc = pc + 32;
+      if (qc >= nch) {
+        qc = lane;
+        ++qm;
+      }
+      if (qm < m1) load(qm, qc, nxt);
+      const int32_t gi[8] = {int32_t(cur.g0.x), int32_t(cur.g0.y), int32_t(cur.g0.z),
+                             int32_t(cur.g0.w), int32_t(cur.g1.x), int32_t(cur.g1.y),
+                             int32_t(cur.g1.z), int32_t(cur.g1.w)};
+      const int32_t ui[8] = {int32_t(cur.u0.x), int32_t(cur.u0.y), int32_t(cur.u0.z),
+                             int32_t(cur.u0.w), int32_t(cur.u1.x), int32_t(cur.u1.y),
+                             int32_t(cur.u1.z), int32_t(cur.u1.w)};
+      const float4 wg0 = __ldg(reinterpret_cast<const float4*>(weight_scale + 8 * c));
+      const float4 wg1 = __ldg(reinterpret_cast<const float4*>(weight_scale + 8 * c + 4));
+      const float4 wu0 = __ldg(reinterpret_cast<const float4*>(weight_scale + I + 8 * c));
+      const float4 wu1 = __ldg(reinterpret_cast<const float4*>(weight_scale + I + 8 * c + 4));
+      const float wg[8] = {wg0.x, wg0.y, wg0.z, wg0.w, wg1.x, wg1.y, wg1.z, wg1.w};
+      const float wu[8] = {wu0.x, wu0.y, wu0.z, wu0.w, wu1.x, wu1.y, wu1.z, wu1.w};
+      float h[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float gate = __int2float_rn(gi[j]);
+        gate = __fmul_rn(gate, wg[j]);
+        gate = __fmul_rn(gate, ts);
+        float up = __int2float_rn(ui[j]);
+        up = __fmul_rn(up, wu[j]);
+        up = __fmul_rn(up, ts);
+        h[j] = swiglu_rn(gate, up);
+        amax = fmaxf(amax, fabsf(h[j]));
+      }
+      *reinterpret_cast<float4*>(hb + 8 * c) = make_float4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<float4*>(hb + 8 * c + 4) = make_float4(h[4], h[5], h[6], h[7]);
+      pm = qm;
+      pc = qc;
+      cur = nxt;
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+    const float scale = __fdiv_rn(127.0f, __fadd_rn(amax, 1e-12f));
+    const float inv = __fdiv_rn(1.0f, scale);
+    unsigned char* dst = out + m * row_bytes;
+    for (int c = lane; c < nch; c += 32) {
+      const float4 h0 = *reinterpret_cast<const float4*>(hb + 8 * c);
+      const float4 h1 = *reinterpret_cast<const float4*>(hb + 8 * c + 4);
+      const float h[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      // q = rint(h * scale) in [-127, 127]; after adding kRoundMagic the low
+      // byte of the float's bits is q as an int8.
+      uint32_t b[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        b[j] = __float_as_uint(__fadd_rn(__fmul_rn(h[j], scale), kRoundMagic));
+      if (BF16OUT) {   // q itself (exact subtraction), then its bf16 bits (exact)
+        uint32_t w4[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float q0 = __fsub_rn(__uint_as_float(b[2 * j]), kRoundMagic);
+          const float q1 = __fsub_rn(__uint_as_float(b[2 * j + 1]), kRoundMagic);
+          w4[j] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632);
+        }
+        *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      } else {
+        const uint32_t w0 = __byte_perm(__byte_perm(b[0], b[1], 0x0040),
+                                        __byte_perm(b[2], b[3], 0x0040), 0x5410);
+        const uint32_t w1 = __byte_perm(__byte_perm(b[4], b[5], 0x0040),
+                                        __byte_perm(b[6], b[7], 0x0040), 0x5410);
+        *reinterpret_cast<uint2*>(dst + 8 * c) = make_uint2(w0, w1);
+      }
+    }
+    if (BF16OUT) {
+      if (lane == 0) out_scale[m] = inv;
+    } else if (lane < ntail) {
+      *reinterpret_cast<uint2*>(dst + I + 8 * lane) =
+          make_uint2(lane == inv_word ? __float_as_uint(inv) : 0u, 0u);
+    }
+    __syncwarp();                              // hb is rewritten for the next row
+  }
+}
+
+template <bool BF16OUT>
+cudaError_t launch_warp_t(const int32_t* acc, int64_t M, int I, const ScaleSrc& sc, void* out,
+                          float* out_scale, cudaStream_t st) {
+  const int W = std::max(1, std::min(8, kWarpSmemBudget / (4 * I)));
+  const int threads = 32 * W;
+  const size_t smem = size_t(W) * I * sizeof(float);
+  auto kernel = swiglu_quant_warp_kernel<BF16OUT>;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  const int64_t grid =
+      std::min<int64_t>((M + W - 1) / W, int64_t(std::max(1, per_sm)) * sms);
+  kernel<<<static_cast<unsigned>(grid), threads, smem, st>>>(
+      acc, M, I, sc, static_cast<unsigned char*>(out),
+      BF16OUT ? int64_t(I) * 2 : align_up(I, 32) + 32, out_scale);
+  return cudaGetLastError();
+}
+
 template <int kCpt, bool BF16OUT>
 cudaError_t launch_t(const int32_t* acc, int64_t M, int I, const ScaleSrc& sc, void* out,
                      float* out_scale, cudaStream_t st) {
@@ -279,6 +437,7 @@ cudaError_t launch_swiglu_quant(const int32_t* acc, int64_t M, int I,
   if (M == 0) return cudaSuccess;
   const ScaleSrc sc{weight_scale, nullptr, 1,
                     reinterpret_cast<const unsigned char*>(token_scale), 4};
+  if (I <= kWarpMaxI) return launch_warp_t<false>(acc, M, I, sc, out, nullptr, st);
   return I / 8 <= 2 * kMaxThreads ? launch_t<2, false>(acc, M, I, sc, out, nullptr, st)
                                   : launch_t<4, false>(acc, M, I, sc, out, nullptr, st);
 }
@@ -291,9 +450,12 @@ cudaError_t launch_swiglu_quant_grouped(const int32_t* acc, int64_t M, int I,
   if (M == 0) return cudaSuccess;
   const ScaleSrc sc{weight_scale, group_off, G,
                     static_cast<const unsigned char*>(token_scale), token_scale_stride};
-  if (out_scale)
+  if (out_scale) {
+    if (I <= kWarpMaxI) return launch_warp_t<true>(acc, M, I, sc, out, out_scale, st);
     return I / 8 <= 2 * kMaxThreads ? launch_t<2, true>(acc, M, I, sc, out, out_scale, st)
                                     : launch_t<4, true>(acc, M, I, sc, out, out_scale, st);
+  }
+  if (I <= kWarpMaxI) return launch_warp_t<false>(acc, M, I, sc, out, nullptr, st);
   return I / 8 <= 2 * kMaxThreads ? launch_t<2, false>(acc, M, I, sc, out, nullptr, st)
                                   : launch_t<4, false>(acc, M, I, sc, out, nullptr, st);
 }
