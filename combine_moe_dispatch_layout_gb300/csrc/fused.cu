@@ -43,7 +43,9 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kRounds = 8;
 constexpr int kTile = kWarps * kRounds * 32;     // 2048 pairs
 constexpr uint32_t kBarrierSpin = 1u << 20;
-constexpr int kMaxCtasPerSm = 2;                 // bounds the barrier's fan-in
+// CTAs per SM (CPS, a template parameter: the register cap that lets them
+// all be resident): 2 when x rows are 12 KB or wider, else 4 on the INT8
+// path and 3 on the verbatim path (measured fastest per shape).
 
 struct BarrierWs {
   uint32_t count;
@@ -119,8 +121,8 @@ __host__ __device__ inline FusedSmem fused_smem(int R, int E, int H, int64_t row
   return L;
 }
 
-template <int DT, bool QUANT, bool STAGED>
-__global__ void __launch_bounds__(kThreads)
+template <int DT, bool QUANT, bool STAGED, int CPS>
+__global__ void __launch_bounds__(kThreads, CPS)
 fused_dispatch_kernel(Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int R = p.R, epr = p.epr, k = p.k, H = p.H, E = R * epr;
@@ -522,9 +524,9 @@ int tiles_per_rank_of(const Shape& s) {
 
 constexpr int64_t kStagedSmemMax = 110 * 1024;   // two CTAs per SM still fit
 
-template <int DT, bool QUANT, bool STAGED>
+template <int DT, bool QUANT, bool STAGED, int CPS>
 cudaError_t launch_t(const Shape& s, Params p, cudaStream_t st) {
-  auto kernel = fused_dispatch_kernel<DT, QUANT, STAGED>;
+  auto kernel = fused_dispatch_kernel<DT, QUANT, STAGED, CPS>;
   const size_t smem = static_cast<size_t>(
       fused_smem(s.R, s.E(), s.H, p.row_bytes, STAGED, QUANT).bytes);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -539,10 +541,21 @@ cudaError_t launch_t(const Shape& s, Params p, cudaStream_t st) {
   // a CTA per token (or tile), few enough for a cheap barrier; all co-resident
   const int64_t want = std::max<int64_t>(p.num_tiles, s.T());
   const int grid = static_cast<int>(std::max<int64_t>(
-      1, std::min<int64_t>(want, int64_t(std::min(per_sm, kMaxCtasPerSm)) * sms)));
+      1, std::min<int64_t>(want, int64_t(std::min(per_sm, CPS)) * sms)));
   void* args[] = {&p};
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kernel), dim3(grid),
                                      dim3(kThreads), args, smem, st);
+}
+
+template <int DT>
+cudaError_t launch_dt(const Shape& s, Params p, bool quant, bool staged, bool wide,
+                      cudaStream_t st) {
+  if (quant) {
+    if (!staged) return launch_t<DT, true, false, 2>(s, p, st);
+    return wide ? launch_t<DT, true, true, 2>(s, p, st) : launch_t<DT, true, true, 4>(s, p, st);
+  }
+  if (!staged) return launch_t<DT, false, false, 2>(s, p, st);
+  return wide ? launch_t<DT, false, true, 2>(s, p, st) : launch_t<DT, false, true, 3>(s, p, st);
 }
 
 }  // namespace
@@ -583,18 +596,9 @@ cudaError_t launch_fused_dispatch(const Shape& s, const void* x, const int32_t* 
   p.dev_status = dev_status;
   const bool staged =
       fused_smem(s.R, s.E(), s.H, row_bytes, true, quant).bytes <= kStagedSmemMax;
-  if (s.dtype == MOE_BF16) {
-    if (quant)
-      return staged ? launch_t<MOE_BF16, true, true>(s, p, st)
-                    : launch_t<MOE_BF16, true, false>(s, p, st);
-    return staged ? launch_t<MOE_BF16, false, true>(s, p, st)
-                  : launch_t<MOE_BF16, false, false>(s, p, st);
-  }
-  if (quant)
-    return staged ? launch_t<MOE_FP16, true, true>(s, p, st)
-                  : launch_t<MOE_FP16, true, false>(s, p, st);
-  return staged ? launch_t<MOE_FP16, false, true>(s, p, st)
-                : launch_t<MOE_FP16, false, false>(s, p, st);
+  const bool wide = int64_t(s.H) * 2 >= 12 * 1024;
+  return s.dtype == MOE_BF16 ? launch_dt<MOE_BF16>(s, p, quant, staged, wide, st)
+                             : launch_dt<MOE_FP16>(s, p, quant, staged, wide, st);
 }
 
 }  // namespace moe_ep
