@@ -357,6 +357,8 @@ def test_combine_quant_full_size(oracle_mod, pl, name):
     dict(R=4, epr=2, bs=300, k=1, H=64),                   # k = 1
     dict(R=2, epr=4, bs=50, k=8, H=65536),                 # widest rows
     dict(R=4, epr=8, bs=200, k=13, H=520),                 # two row batches, 8-code tail
+    dict(R=3, epr=2, bs=500, k=3, H=1032),                 # k = 3
+    dict(R=2, epr=5, bs=333, k=5, H=264, dtype=W.FP16),    # k = 5, fp16 out
     dict(R=8, epr=8, bs=64, k=64, H=256),                  # largest k
 ], ids=lambda c: "-".join("%s%s" % kv for kv in c.items()))
 def test_combine_quant_mid(oracle_mod, pl, case):
@@ -496,7 +498,7 @@ def _check_swiglu(oracle, ep, M, I, sample=None):
 
 
 @pytest.mark.parametrize("M,I", [(3000, 2048), (500, 40), (257, 16384), (0, 64),
-                                 (1, 8)])
+                                 (1, 8), (777, 4096), (300, 4104)])
 def test_swiglu_quant_full(oracle_mod, ep, M, I):
     _check_swiglu(oracle_mod, ep, M, I)
 
