@@ -19,6 +19,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -707,6 +708,25 @@ def _oracle_tokens_per_s(w, t_ln, t_dc, n):
     return w.T / (t_ln + t_dc * w.T / n)
 
 
+def host_cpu():
+    """The host CPU's model string and usable core count (for the CPU baseline)."""
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    try:
+        avail = len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        avail = os.cpu_count() or 1
+    return model, avail
+
+
 def cpu_baseline(w, idx_h, wt_h, x_h, y_h, seconds):
     import oracle as o
     idx_np, wt_np = idx_h.numpy(), wt_h.numpy()
@@ -718,8 +738,9 @@ def cpu_baseline(w, idx_h, wt_h, x_h, y_h, seconds):
     n = int(min(w.T, max(64, (seconds - t_ln) / max(per_tok, 1e-9))))
     tokens = np.sort(rng.choice(w.T, size=n, replace=False))
     t_ln, t_dc = _oracle_step(o, w, idx_np, wt_np, x_bits, y_bits, tokens)
+    model, avail = host_cpu()
     return {"value": _oracle_tokens_per_s(w, t_ln, t_dc, n), "unit": "tokens/s",
-            "cores": 1, "kind": "oracle",
+            "cores": 1, "kind": "oracle", "cpu": model, "host_cores_available": avail,
             "sample": "layout+notify on all %d tokens (%.3f s), dispatch+combine "
                       "on %d random tokens (%.2f s), scaled to the full batch"
                       % (w.T, t_ln, n, t_dc)}
@@ -767,7 +788,8 @@ def run_reference(args, w):
         "config": {"workload": workload_desc(w),
                    "step": "layout+notify+dispatch+combine (CPU oracle)"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1,
-                         "kind": "oracle",
+                         "kind": "oracle", "cpu": host_cpu()[0],
+                         "host_cores_available": host_cpu()[1],
                          "sample": "each step: layout+notify on all %d tokens, "
                                    "dispatch+combine on %d random tokens, "
                                    "scaled to the full batch" % (w.T, n)},
