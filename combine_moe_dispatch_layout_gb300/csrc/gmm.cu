@@ -27,6 +27,9 @@
 // per thread, and one half of the columns) into int32 registers while the
 // next chunk accumulates, then store the tile's rows.  Every mbarrier wait is
 // bounded: a timeout sets MOE_ERR_TIMEOUT and the CTA stops issuing work.
+// When the groups average at least four row tiles, CTAs run in clusters of
+// two on the two row tiles of a pair and multicast one half of the weight
+// tile each into both CTAs' stages (the CL form).
 #include <cuda.h>
 
 #include <algorithm>
