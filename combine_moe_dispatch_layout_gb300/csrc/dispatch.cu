@@ -9,7 +9,8 @@
 //   * a persistent grid walks the tokens; per CTA, x rows arrive in shared
 //     memory through cp.async.bulk loads issued one or two tokens ahead
 //     (double-buffered stages, mbarrier transaction counts);
-//   * INT8 path: compute warps reduce max|x| from shared memory (warp
+//   * INT8 path: compute threads (two 8-element chunks each, kept in
+//     registers between the passes) reduce max|x| from shared memory (warp
 //     shuffles + one shared step), quantise into a staging row image (codes,
 //     zero pad, fp32 1/scale, zero pad), fence the async proxy, and one
 //     thread issues the k cp.async.bulk stores of that image to the token's
@@ -90,7 +91,10 @@ __host__ __device__ inline SmemLayout smem_layout(int H, int64_t row_bytes, int 
 // ---------------------------------------------------------------------------
 // EXPAND: the codes go out as bf16 values (2H bytes per row) and 1/scale to
 // dyn_scale[row]; otherwise the INT8 row image of row_bytes bytes.
-template <int DT, int S, bool EXPAND>
+// CPT: 8-element chunks per compute thread, held in registers from the max|x|
+// pass to the quantising pass (chunks past CPT * compute threads, for very
+// wide rows, are read from shared memory again).
+template <int DT, int S, bool EXPAND, int CPT>
 __global__ void __launch_bounds__(kMaxThreads)
 dispatch_quant_kernel(const unsigned char* __restrict__ x,
                       const int32_t* __restrict__ topk_idx,
@@ -123,7 +127,9 @@ dispatch_quant_kernel(const unsigned char* __restrict__ x,
   const int inv_word = (h_align - H) / 8;
   const int64_t grid = gridDim.x;
 
-  int pend[2] = {-1, -1};   // issuer: parity of the load in flight per stage
+  int pend[S];               // issuer: parity of the load in flight per stage
+#pragma unroll
+  for (int s = 0; s < S; ++s) pend[s] = -1;
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&mbar[s], 1);
     fence_mbar_init();
@@ -147,6 +153,7 @@ dispatch_quant_kernel(const unsigned char* __restrict__ x,
   __syncthreads();
 
   int it = 0;
+  float xf[CPT][8];   // this thread's chunks of the current token's x
   for (int64_t g = blockIdx.x; g < T; ++it, g += grid) {
     const int b = it % S;
     const uint32_t parity = static_cast<uint32_t>(it / S) & 1u;
@@ -165,10 +172,18 @@ dispatch_quant_kernel(const unsigned char* __restrict__ x,
         s_abort = 1;
       }
       float amax = 0.0f;
-      for (int c = tid; c < nch; c += ncomp) {
-        const uint4 v = *reinterpret_cast<const uint4*>(xs + c * 16);
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) {
+        const int c = tid + i * ncomp;
+        if (c < nch) {
+          unpack8<DT>(*reinterpret_cast<const uint4*>(xs + c * 16), xf[i]);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(xf[i][j]));
+        }
+      }
+      for (int c = tid + CPT * ncomp; c < nch; c += ncomp) {
         float f[8];
-        unpack8<DT>(v, f);
+        unpack8<DT>(*reinterpret_cast<const uint4*>(xs + c * 16), f);
 #pragma unroll
         for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
       }
@@ -185,10 +200,7 @@ dispatch_quant_kernel(const unsigned char* __restrict__ x,
       for (int w = 1; w < ncw; ++w) amax = fmaxf(amax, s_wmax[w]);
       const float scale = __fdiv_rn(127.0f, __fadd_rn(amax, 1e-12f));
       const float inv = __fdiv_rn(1.0f, scale);
-      for (int c = tid; c < nch; c += ncomp) {
-        const uint4 v = *reinterpret_cast<const uint4*>(xs + c * 16);
-        float f[8];
-        unpack8<DT>(v, f);
+      auto quantise = [&](int c, const float (&f)[8]) {
         if (EXPAND) {   // q as bf16: exact (|q| <= 127 has at most 7 significant bits)
           uint32_t w4[4];
 #pragma unroll
@@ -207,6 +219,14 @@ dispatch_quant_kernel(const unsigned char* __restrict__ x,
           }
           *reinterpret_cast<uint2*>(os + c * 8) = make_uint2(w2[0], w2[1]);
         }
+      };
+#pragma unroll
+      for (int i = 0; i < CPT; ++i)
+        if (tid + i * ncomp < nch) quantise(tid + i * ncomp, xf[i]);
+      for (int c = tid + CPT * ncomp; c < nch; c += ncomp) {
+        float f[8];
+        unpack8<DT>(*reinterpret_cast<const uint4*>(xs + c * 16), f);
+        quantise(c, f);
       }
       if (EXPAND) {   // 1/scale of this token into each of its k rows' slots
         for (int kk = tid; kk < k; kk += ncomp) {
@@ -334,26 +354,33 @@ cudaError_t launch_persistent(Kernel kernel, int threads, int smem, int64_t T,
   return cudaSuccess;
 }
 
-template <int DT, int S, bool EXPAND>
+template <int DT, int S, bool EXPAND, int CPT>
 cudaError_t launch_quant(const Shape& s, const void* x, const int32_t* topk_idx,
                          const int32_t* send_idx, const int32_t* put_offset,
                          const int64_t* rank_recv_base, void* recv, int64_t row_bytes,
                          float* dyn_scale, int64_t capacity, int32_t* dev_status,
                          cudaStream_t st) {
   const int nch = s.H / 8;
-  const int ncomp = std::max(32, std::min(kMaxThreads - 32, ((nch + 3) / 4 + 31) / 32 * 32));
+  const int ncomp =
+      std::max(32, std::min(kMaxThreads - 32, ((nch + CPT - 1) / CPT + 31) / 32 * 32));
   const int threads = ncomp + 32;
   const int smem = smem_layout(s.H, row_bytes, S, true).bytes;
   int grid = 0;
-  cudaError_t e =
-      launch_persistent(dispatch_quant_kernel<DT, S, EXPAND>, threads, smem, s.T(), &grid);
+  cudaError_t e = launch_persistent(dispatch_quant_kernel<DT, S, EXPAND, CPT>, threads, smem,
+                                    s.T(), &grid);
   if (e != cudaSuccess) return e;
-  dispatch_quant_kernel<DT, S, EXPAND><<<grid, threads, smem, st>>>(
+  dispatch_quant_kernel<DT, S, EXPAND, CPT><<<grid, threads, smem, st>>>(
       static_cast<const unsigned char*>(x), topk_idx, send_idx, put_offset,
       rank_recv_base, s.R, s.bs, s.k, s.epr, s.H, s.T(),
       static_cast<unsigned char*>(recv), row_bytes, dyn_scale, capacity, dev_status);
   return cudaGetLastError();
 }
+
+// Two 8-element chunks per compute thread (so H/16 compute threads per
+// token, up to 992): measured against four, two was as fast or faster on every
+// shape (dsv3 398 -> 374, skew 186 -> 172, maxrank 600 -> 565 us) -- a token's
+// critical path (two passes, two block barriers) matters more than CTAs per SM.
+constexpr int kCpt = 2;
 
 template <int DT, bool EXPAND>
 cudaError_t launch_quant_stages(const Shape& s, const void* x, const int32_t* topk_idx,
@@ -363,10 +390,12 @@ cudaError_t launch_quant_stages(const Shape& s, const void* x, const int32_t* to
                                 int32_t* dev_status, cudaStream_t st) {
   // two stages (prefetch one token ahead) unless the rows are too wide
   if (smem_layout(s.H, row_bytes, 2, true).bytes <= kSmemBudget)
-    return launch_quant<DT, 2, EXPAND>(s, x, topk_idx, send_idx, put_offset, rank_recv_base,
-                                       recv, row_bytes, dyn_scale, capacity, dev_status, st);
-  return launch_quant<DT, 1, EXPAND>(s, x, topk_idx, send_idx, put_offset, rank_recv_base,
-                                     recv, row_bytes, dyn_scale, capacity, dev_status, st);
+    return launch_quant<DT, 2, EXPAND, kCpt>(s, x, topk_idx, send_idx, put_offset,
+                                             rank_recv_base, recv, row_bytes, dyn_scale,
+                                             capacity, dev_status, st);
+  return launch_quant<DT, 1, EXPAND, kCpt>(s, x, topk_idx, send_idx, put_offset,
+                                           rank_recv_base, recv, row_bytes, dyn_scale,
+                                           capacity, dev_status, st);
 }
 
 template <int S>

@@ -27,9 +27,6 @@
 // per thread, and one half of the columns) into int32 registers while the
 // next chunk accumulates, then store the tile's rows.  Every mbarrier wait is
 // bounded: a timeout sets MOE_ERR_TIMEOUT and the CTA stops issuing work.
-// When the groups average at least four row tiles, CTAs run in clusters of
-// two on the two row tiles of a pair and multicast one half of the weight
-// tile each into both CTAs' stages (the CL form).
 #include <cuda.h>
 
 #include <algorithm>
@@ -93,44 +90,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t ss
       : "memory");
 }
 
-// The same tile into this CTA's and the other cluster CTAs' shared memory
-// (same offset in each CTA of `mask`), each CTA's mbarrier at `bar`'s offset
-// counting the bytes it receives.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t sdst, const CUtensorMap* map, int x,
-                                               int y, uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(sdst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_id_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_count_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster (release / acquire).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Shared-memory matrix descriptor: K-major tile, rows of 128 bytes with the
 // 128-byte swizzle, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
@@ -160,16 +119,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_addr(bar))
-      : "memory");
-}
-
-// As mma_commit, arriving on the mbarrier at `bar`'s offset in every CTA of
-// `mask` in the cluster.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_addr(bar)),
-      "h"(mask)
       : "memory");
 }
 
@@ -213,12 +162,8 @@ struct Tile {
   int n0;         // first output column
 };
 
-// CL (clusters of two CTAs): a tile index names a pair of row tiles (2u,
-// 2u + 1) of one column tile; CTA `crank` of the cluster takes row tile
-// 2u + crank (0 rows when the expert has no such tile).
-template <bool CL>
 __device__ __forceinline__ Tile decode_tile(int64_t t, const int64_t* goff,
-                                            const int32_t* tpre, int G, int ntn, int crank) {
+                                            const int32_t* tpre, int G, int ntn) {
   int lo = 0, hi = G;                 // largest g with tpre[g] <= t
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -226,34 +171,31 @@ __device__ __forceinline__ Tile decode_tile(int64_t t, const int64_t* goff,
   }
   const int g = lo;
   const int64_t cnt = goff[g + 1] - goff[g];
-  const int mt0 = static_cast<int>((cnt + BM - 1) / BM);
-  const int mt = CL ? (mt0 + 1) / 2 : mt0;           // row units: tiles or pairs
-  constexpr int kRaster = CL ? kRasterM / 2 : kRasterM;
+  const int mt = static_cast<int>((cnt + BM - 1) / BM);
   const int local = static_cast<int>(t - tpre[g]);
   // blocks of row tiles: inside a block m is fastest, then n, so the tiles
   // in flight together touch a bounded number of A's row tiles however large
   // the expert is; all blocks have kRasterM row tiles except the last, which
   // takes the remainder too (kRasterM .. 2*kRasterM - 1; an expert of fewer
   // than 2*kRasterM row tiles is one block), so no short block re-reads B
-  const int nblk = mt / kRaster > 0 ? mt / kRaster : 1;
-  const int full = nblk - 1, per_full = kRaster * ntn;
+  const int nblk = mt / kRasterM > 0 ? mt / kRasterM : 1;
+  const int full = nblk - 1, per_full = kRasterM * ntn;
   const int blk = local / per_full;
   int m, n;
   if (blk < full) {
     const int r = local - blk * per_full;
-    m = blk * kRaster + r % kRaster;
-    n = r / kRaster;
+    m = blk * kRasterM + r % kRasterM;
+    n = r / kRasterM;
   } else {
-    const int rem = mt - full * kRaster, r = local - full * per_full;
-    m = full * kRaster + r % rem;
+    const int rem = mt - full * kRasterM, r = local - full * per_full;
+    m = full * kRasterM + r % rem;
     n = r / rem;
   }
-  if (CL) m = 2 * m + crank;
   Tile tl;
   tl.g = g;
   tl.row0 = goff[g] + int64_t(m) * BM;
   const int64_t left = cnt - int64_t(m) * BM;
-  tl.rows = left < BM ? (left > 0 ? left : 0) : BM;
+  tl.rows = left < BM ? left : BM;
   tl.n0 = n * BN;
   return tl;
 }
@@ -277,12 +219,7 @@ struct Dequant {
 // and 10 warps put 3 on some of them, so at most 168 registers per thread.
 // MODE (kOut*) is a template parameter so each epilogue gets its own
 // register allocation.
-// CL: launched in clusters of two CTAs that take the two row tiles of a pair
-// (same expert, same column tile); each CTA loads its own A tile and one
-// 128-row half of the weight tile, multicast into both CTAs' stages, so each
-// SM requests a third fewer operand bytes.  A stage is refilled once both
-// CTAs' MMAs have read it (empty barriers count an arrival from each).
-template <int STAGES, int MODE, bool CL>
+template <int STAGES, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -306,10 +243,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntn = (N + BN - 1) / BN;
-  const int crank = CL ? static_cast<int>(cluster_ctarank()) : 0;
-  const int64_t t_first = CL ? int64_t(cluster_id_x()) : int64_t(blockIdx.x);
-  const int64_t t_step = CL ? int64_t(cluster_count_x()) : int64_t(gridDim.x);
-  constexpr uint16_t kPair = 0x3;                 // both CTAs of the cluster
 
   // ---- group tables: row offsets and tile prefix (block scan over G) ----------
   {
@@ -320,8 +253,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int g = g0; g < g1; ++g) {
       const int64_t c = group_count(group_rows, g, dev_status);
       rsum += c;
-      const int32_t mt = static_cast<int32_t>((c + BM - 1) / BM);
-      tsum += (CL ? (mt + 1) / 2 : mt) * ntn;
+      tsum += static_cast<int32_t>((c + BM - 1) / BM) * ntn;
     }
     int64_t* s_r = reinterpret_cast<int64_t*>(smem + kOffA);            // [kThreads]
     int32_t* s_t = reinterpret_cast<int32_t*>(s_r + kThreads);           // [kThreads]
@@ -350,14 +282,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       tpre[g] = tt;
       const int64_t c = group_count(group_rows, g, nullptr);
       r += c;
-      const int32_t mt = static_cast<int32_t>((c + BM - 1) / BM);
-      tt += (CL ? (mt + 1) / 2 : mt) * ntn;
+      tt += static_cast<int32_t>((c + BM - 1) / BM) * ntn;
     }
   }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full + s, 1);
-      mbar_init(empty + s, CL ? 2 : 1);
+      mbar_init(empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull + b, 1);
@@ -376,7 +307,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   }
   tc_fence_before();
   __syncthreads();
-  if (CL) cluster_sync();   // both CTAs' barriers exist before any multicast
   tc_fence_after();
 
   const uint32_t tmem = *tmem_slot;
@@ -384,17 +314,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const int64_t tiles = tpre[G];
   const int nkb = (K + BK - 1) / BK;
   const int nchunks = (nkb + kChunkBlocks - 1) / kChunkBlocks;
-  if (CL && cluster_size() != 2u) {       // the pair protocol needs clusters of two
-    if (tid == 0) set_status(dev_status, MOE_ERR_INVALID_ARG);
-  } else if (total_rows > a_rows) {       // more rows than the A buffer holds
+  if (total_rows > a_rows) {              // more rows than the A buffer holds
     if (tid == 0) set_status(dev_status, MOE_ERR_CAPACITY);
   } else if (warp == 0) {
     // ---- TMA producer ---------------------------------------------------------
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int64_t t = t_first; t < tiles && !*abort_flag; t += t_step) {
-        const Tile tl = decode_tile<CL>(t, goff, tpre, G, ntn, crank);
+      for (int64_t t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+        const Tile tl = decode_tile(t, goff, tpre, G, ntn);
         const int brow = tl.g * N + tl.n0;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait_bounded(empty + stage, phase ^ 1u, kSpin)) {
@@ -405,13 +333,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           mbar_arrive_expect_tx(full + stage, kTileABytes + kTileBBytes);
           tma_load_2d(smem_addr(smem + kOffA + stage * kTileABytes), &tmA, kb * BK,
                       static_cast<int>(tl.row0), full + stage);
-          if (CL)   // this CTA's half of the weight tile, into both CTAs
-            tma_load_2d_mc(smem_addr(smem + kOffB + stage * kTileBBytes +
-                                     crank * (kTileBBytes / 2)),
-                           &tmB, kb * BK, brow + crank * (BN / 2), full + stage, kPair);
-          else
-            tma_load_2d(smem_addr(smem + kOffB + stage * kTileBBytes), &tmB, kb * BK, brow,
-                        full + stage);
+          tma_load_2d(smem_addr(smem + kOffB + stage * kTileBBytes), &tmB, kb * BK, brow,
+                      full + stage);
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -430,7 +353,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int stage = 0;
       uint32_t phase = 0, chunk_ctr = 0;
       bool ok = true;
-      for (int64_t t = t_first; ok && t < tiles; t += t_step) {
+      for (int64_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
         for (int c = 0; ok && c < nchunks; ++c, ++chunk_ctr) {
           const uint32_t b = chunk_ctr & 1u, use = (chunk_ctr >> 1) & 1u;
           if (!mbar_wait_bounded(tempty + b, use ^ 1u, kSpin) || *abort_flag) {
@@ -452,10 +375,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             for (int kk = 0; kk < BK / 16; ++kk)   // +32 bytes along K per step
               mma_bf16(d, ad + 2 * kk, bd + 2 * kk,
                        (kb != c * kChunkBlocks || kk != 0) ? 1u : 0u);
-            if (CL)
-              mma_commit_mc(empty + stage, kPair); // read here: one of the two arrivals
-            else
-              mma_commit(empty + stage);           // frees the stage when read
+            mma_commit(empty + stage);             // frees the stage when read
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
           }
           mma_commit(tfull + b);                   // the chunk's sums are final
@@ -471,8 +391,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const int q = warp & 3;                  // TMEM lanes 32q .. 32q+31
     const int half = (warp - 2) >> 2;        // columns half*128 .. half*128+127
     uint32_t chunk_ctr = 0;
-    for (int64_t t = t_first; t < tiles; t += t_step) {
-      const Tile tl = decode_tile<CL>(t, goff, tpre, G, ntn, crank);
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const Tile tl = decode_tile(t, goff, tpre, G, ntn);
       const int r = q * 32 + lane;
       const int col0 = tl.n0 + half * kEpiCols;
       const int ncols = N - col0;            // a ragged last column tile
@@ -591,9 +511,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                  "r"(kTmemCols)
                  : "memory");
   }
-  // neither CTA leaves while the other may still multicast into its stages
-  // or arrive on its barriers
-  if (CL) cluster_sync();
 }
 
 // ---- int8 codes -> bf16 ------------------------------------------------------------
@@ -720,56 +637,35 @@ int gmm_block_n() { return BN; }
 
 namespace {
 
-template <int STAGES, int MODE, bool CL>
+template <int STAGES, int MODE>
 cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                         const int32_t* group_rows, int G, int64_t a_rows, int K, int N,
                         int32_t* c, const Dequant& dq, int32_t* dev_status, int sms,
                         cudaStream_t st) {
-  auto kernel = grouped_gemm_kernel<STAGES, MODE, CL>;
   const size_t smem = SmemLayout<STAGES>::bytes(G);
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<STAGES, MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL ? static_cast<unsigned>(sms / 2 * 2) : static_cast<unsigned>(sms));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (CL) {
-    // as many pairs as can be resident at once (a GPC with an odd number of
-    // free SMs holds one fewer), so no pair waits for another to finish
-    int maxc = 0;
-    e = cudaOccupancyMaxActiveClusters(&maxc, kernel, &cfg);
-    if (e != cudaSuccess) return e;
-    if (maxc < 1) return cudaErrorNotSupported;   // the caller runs the plain form
-    cfg.gridDim = dim3(2u * static_cast<unsigned>(std::min(sms / 2, maxc)));
-  }
-  e = cudaLaunchKernelEx(&cfg, kernel, ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
-                         dev_status);
-  if (e != cudaSuccess) return e;
+  grouped_gemm_kernel<STAGES, MODE><<<sms, kThreads, smem, st>>>(ma, mb, mc, group_rows, G,
+                                                                 a_rows, K, N, c, dq,
+                                                                 dev_status);
   return cudaGetLastError();
 }
 
-template <int STAGES, bool CL>
+template <int STAGES>
 cudaError_t launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                           const int32_t* group_rows, int G, int64_t a_rows, int K, int N,
                           int32_t* c, const Dequant& dq, int32_t* dev_status, int sms,
                           cudaStream_t st) {
   if (dq.mode == kOutDequant)
-    return launch_mode<STAGES, kOutDequant, CL>(ma, mb, mc, group_rows, G, a_rows, K, N, c,
-                                                dq, dev_status, sms, st);
-  if (dq.mode == kOutSwiGLU)
-    return launch_mode<STAGES, kOutSwiGLU, CL>(ma, mb, mc, group_rows, G, a_rows, K, N, c,
-                                               dq, dev_status, sms, st);
-  return launch_mode<STAGES, kOutInt32, CL>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
+    return launch_mode<STAGES, kOutDequant>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
                                             dev_status, sms, st);
+  if (dq.mode == kOutSwiGLU)
+    return launch_mode<STAGES, kOutSwiGLU>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
+                                           dev_status, sms, st);
+  return launch_mode<STAGES, kOutInt32>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
+                                        dev_status, sms, st);
 }
 
 }  // namespace
@@ -793,37 +689,25 @@ cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void
                                 const float* col_scale, const void* row_scale,
                                 int64_t row_scale_stride, int32_t* dev_status,
                                 cudaStream_t st) {
+  CUtensorMap ma, mb, mc;
+  cudaError_t e = encode_kmajor(&ma, a, a_rows, K, BM);
+  if (e == cudaSuccess) e = encode_kmajor(&mb, b, int64_t(G) * N, K, BN);
+  if (e == cudaSuccess) e = encode_out(&mc, c, a_rows, mode == kOutSwiGLU ? N / 2 : N);
+  if (e != cudaSuccess) return e;
   int dev = 0, sms = 0, optin = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  // four stages unless the group tables (12 bytes per group) crowd them out;
-  // clusters of two when the buffer holds at least 4 row tiles per group on
-  // average (with fewer, many pairs would hold one real tile)
-  const bool four = SmemLayout<4>::bytes(G) <= size_t(optin);
-  const bool cl = four && sms >= 2 && a_rows >= int64_t(G) * 4 * BM;
-  CUtensorMap ma, mb, mc;
-  e = encode_kmajor(&ma, a, a_rows, K, BM);
-  if (e == cudaSuccess) e = encode_kmajor(&mb, b, int64_t(G) * N, K, cl ? BN / 2 : BN);
-  if (e == cudaSuccess) e = encode_out(&mc, c, a_rows, mode == kOutSwiGLU ? N / 2 : N);
-  if (e != cudaSuccess) return e;
   const Dequant dq{mode, col_scale, static_cast<const unsigned char*>(row_scale),
                    row_scale_stride};
   int32_t* out = static_cast<int32_t*>(c);
-  if (cl) {
-    e = launch_stages<4, true>(ma, mb, mc, group_rows, G, a_rows, K, N, out, dq, dev_status,
-                               sms, st);
-    if (e != cudaErrorNotSupported) return e;
-    e = encode_kmajor(&mb, b, int64_t(G) * N, K, BN);   // no pair fits: plain form
-    if (e != cudaSuccess) return e;
-  }
-  if (four)
-    return launch_stages<4, false>(ma, mb, mc, group_rows, G, a_rows, K, N, out, dq,
-                                   dev_status, sms, st);
-  return launch_stages<3, false>(ma, mb, mc, group_rows, G, a_rows, K, N, out, dq, dev_status,
-                                 sms, st);
+  // four stages unless the group tables (12 bytes per group) crowd them out
+  if (SmemLayout<4>::bytes(G) <= size_t(optin))
+    return launch_stages<4>(ma, mb, mc, group_rows, G, a_rows, K, N, out, dq, dev_status, sms,
+                            st);
+  return launch_stages<3>(ma, mb, mc, group_rows, G, a_rows, K, N, out, dq, dev_status, sms, st);
 }
 
 }  // namespace moe_ep

@@ -67,8 +67,8 @@ GEMM_CASES = [
     (3, 136, 520, (70, 0, 200)),          # a ragged last column tile
     (2, 8, 32, (3, 140)),                 # N and K below one tile
     (3000, 136, 72, tuple((7 * i) % 5 for i in range(3000))),   # many groups: 3 stages
-    # >= 512 rows per group on average: clusters of two CTAs share the weight
-    # tile; odd row-tile counts leave one CTA of a pair without rows
+    # large groups: odd row-tile counts, ragged tails, an empty group, a
+    # partial third K chunk
     (7, 136, 2112, (700, 1030, 128, 513, 900, 0, 2049)),
     (2, 512, 1024, (1, 1100)),
     (1, 256, 64, (640,)),
@@ -144,7 +144,7 @@ def _dequant_bits(oracle, ref, ws2, I):
 
 
 @pytest.mark.parametrize("case", [(3, 264, 200, (130, 0, 70)),
-                                  (3, 264, 1104, (600, 0, 1000))],   # clusters of two
+                                  (3, 264, 1104, (600, 0, 1000))],   # two K chunks
                          ids=lambda c: "G%d_N%d_K%d" % c[:3])
 def test_grouped_gemm_dequant_epilogue(oracle_mod, ep, case):
     rng = np.random.default_rng(9)
