@@ -710,7 +710,7 @@ def _oracle_tokens_per_s(w, t_ln, t_dc, n):
 
 def host_cpu():
     """The host CPU's model string and usable core count (for the CPU baseline)."""
-    model = platform.processor() or platform.machine()
+    model = None
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
@@ -720,6 +720,16 @@ def host_cpu():
                     break
     except OSError:
         pass
+    if not model:                       # Arm hosts: /proc/cpuinfo names no model
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    model = model or platform.processor() or platform.machine()
     try:
         avail = len(os.sched_getaffinity(0))
     except (AttributeError, OSError):
