@@ -12,9 +12,9 @@
 // or a contiguous part of its hidden dimension when that evens out the last
 // round over the grid's warps.  The warp resolves the item's k rows, weights
 // and 1/scales into its own shared-memory table, then each lane walks
-// 8-code chunks of the item (one 8-byte load per row, 8 rows per batch),
-// issuing the next (chunk, batch)'s loads before it computes the current
-// one.  Per element: a sign-extending byte permute, an int-to-float
+// 8-code chunks of the item (one 8-byte load per row; all k rows of a chunk
+// in one batch when k <= 8, batches of 8 rows otherwise), issuing the next
+// (chunk, batch)'s loads before it computes the current one.  Per element: a sign-extending byte permute, an int-to-float
 // conversion, two multiplies and an add -- the arithmetic is about as long
 // as the HBM time, so keeping loads in flight across the compute is what
 // matters.  Rows are half the bytes of bf16 rows.
