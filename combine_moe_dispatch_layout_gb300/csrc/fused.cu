@@ -149,10 +149,16 @@ fused_dispatch_kernel(Params p) {
   const int64_t T = int64_t(R) * p.bs;
   const uint32_t xbytes = static_cast<uint32_t>(H) * 2u;
   constexpr int kNst = QUANT ? kQuantStages : kCopyStages;
-  int pend[kNst];           // thread 0: completion parity of the x load in flight per stage
+  int pend[kNst];           // issuer: completion parity of the x load in flight per stage
 #pragma unroll
   for (int st = 0; st < kNst; ++st) pend[st] = -1;
-  if (STAGED && tid == 0) {  // this CTA's first x rows arrive during phases A-C
+  // The thread that issues the token phase's copies (and owns their bulk
+  // groups and pend[]): lane 0 of the last warp on the INT8 path -- its warp
+  // holds the fewest x chunks, so the copy duties do not delay a block barrier
+  // (thread 0, on the busiest warp, made every token ~4% slower) -- and thread
+  // 0 on the verbatim path, whose warp 0 runs the token loop alone.
+  const int issuer = QUANT ? kThreads - 32 : 0;
+  if (STAGED && tid == issuer) {  // this CTA's first x rows arrive during phases A-C
     for (int st = 0; st < kNst; ++st) mbar_init(&mbar[st], 1);
     fence_mbar_init();
     for (int st = 0; st < kNst; ++st) {
@@ -393,7 +399,7 @@ fused_dispatch_kernel(Params p) {
       const int b = it & 1;
       const unsigned char* xsb = xs + b * SL.x_stride;
       unsigned char* osb = os + b * SL.o_stride;
-      if (tid == 0 && QUANT) bulk_wait_read<1>();   // image b: iteration it-2's stores read it
+      if (tid == issuer && QUANT) bulk_wait_read<1>();   // image b: iteration it-2's stores read it
       if (!mbar_wait_bounded(&mbar[b], static_cast<uint32_t>(it >> 1) & 1u, kBarrierSpin)) {
         set_status(p.dev_status, MOE_ERR_TIMEOUT);
         s_abort = 1;
@@ -413,7 +419,7 @@ fused_dispatch_kernel(Params p) {
       }
       __syncthreads();   // (A) maxima, rows and the abort flag visible
       if (s_abort) break;
-      if (tid == 0) pend[b] = -1;
+      if (tid == issuer) pend[b] = -1;
       if constexpr (QUANT) {
         float amax = s_wmax[0];
 #pragma unroll
@@ -437,7 +443,7 @@ fused_dispatch_kernel(Params p) {
         fence_proxy_async_smem();
         __syncthreads();   // (B) the image is complete; x stage b is free
       }
-      if (tid == 0) {
+      if (tid == issuer) {
         const unsigned char* src = QUANT ? osb : xsb;
         for (int kk = 0; kk < k; ++kk)
           if (s_rows[kk] >= 0)
@@ -509,7 +515,7 @@ fused_dispatch_kernel(Params p) {
     __syncthreads();   // s_rows and s_wmax are reused by the next token
   }
   }
-  if (STAGED && tid == 0) {
+  if (STAGED && tid == issuer) {
     bulk_wait_all<0>();   // stores done before shared memory goes away
     for (int st = 0; st < kNst; ++st)   // only after an abort: loads still in flight
       if (pend[st] >= 0 &&
