@@ -18,6 +18,7 @@
 // the add (__fmul_rn / __fadd_rn; the unit is also built with -fmad=false),
 // k in order; out = round-to-nearest-even in the token dtype.
 #include <algorithm>
+#include <atomic>
 
 #include "moe_ep_internal.cuh"
 
@@ -92,11 +93,37 @@ combine_kernel(const uint4* __restrict__ y, int64_t y_rows,
   }
 }
 
-// Compute threads per CTA: about 4 chunks each, a multiple of 32, at most
+// Compute threads per CTA for `cpt` chunks each: a multiple of 32, at most
 // 992 (plus the producer warp).
-int compute_threads(int nch) {
-  int t = ((nch + 3) / 4 + 31) / 32 * 32;
+int compute_threads(int nch, int cpt) {
+  int t = ((nch + cpt - 1) / cpt + 31) / 32 * 32;
   return std::max(32, std::min(kMaxThreads - 32, t));
+}
+
+// Rows in flight per SM below which fewer, wider CTAs stop paying: a token's
+// k rows are in flight while its CTA gathers them.
+constexpr int64_t kInFlightBytes = 160 * 1024;
+
+// CTAs of combine_kernel<DT> per SM for a block size, queried once per device
+// and block size (the launcher asks for two sizes on every call; the query
+// costs host time that small, launch-bound calls would otherwise pay).
+template <int DT>
+cudaError_t blocks_per_sm(int dev, int threads, int* out) {
+  constexpr int kDevs = 16, kSizes = kMaxThreads / 32 + 1;
+  static std::atomic<int> cache[kDevs][kSizes];   // 0: not known yet
+  const bool cached = dev >= 0 && dev < kDevs && threads % 32 == 0 && threads <= kMaxThreads;
+  if (cached) {
+    const int v = cache[dev][threads / 32].load(std::memory_order_relaxed);
+    if (v > 0) {
+      *out = v;
+      return cudaSuccess;
+    }
+  }
+  const cudaError_t e =
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, combine_kernel<DT>, threads, 0);
+  if (e == cudaSuccess && cached && *out > 0)
+    cache[dev][threads / 32].store(*out, std::memory_order_relaxed);
+  return e;
 }
 
 template <int DT>
@@ -106,13 +133,22 @@ cudaError_t launch_t(const Shape& s, const void* y, int64_t y_rows,
                      const int64_t* rank_recv_base, void* out,
                      int32_t* dev_status, cudaStream_t st) {
   const int nch = s.H / 8;
-  const int threads = compute_threads(nch) + 32;
-  int dev = 0, sms = 0, per_sm = 0;
+  int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<DT>, threads, 0);
   if (e != cudaSuccess) return e;
+  // Two chunks per compute thread (a shorter gather per token) when the CTAs
+  // that fit still keep kInFlightBytes of rows in flight per SM, else four
+  // (more CTAs).  Measured: with two, dsv3 (2 CTAs x 112 KB per SM) 634 ->
+  // 625 us, fp16 (6 x 32 KB) 196 -> 188, maxrank 951 -> 937; skew (3 x 48 KB)
+  // 294 -> 301, so it keeps four.
+  int threads = 0, per_sm = 0;
+  for (int cpt = 2; cpt <= 4; cpt += 2) {
+    threads = compute_threads(nch, cpt) + 32;
+    e = blocks_per_sm<DT>(dev, threads, &per_sm);
+    if (e != cudaSuccess) return e;
+    if (int64_t(per_sm) * s.k * s.H * 2 >= kInFlightBytes) break;
+  }
   const int64_t grid = std::min<int64_t>(s.T(), int64_t(std::max(1, per_sm)) * sms);
   combine_kernel<DT><<<static_cast<unsigned>(grid), threads, 0, st>>>(
       static_cast<const uint4*>(y), y_rows, topk_idx, weights, send_idx,
