@@ -164,11 +164,9 @@ def aggregate_tokens_per_s(tokens_per_rank, world, max_seconds):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, path=None):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv") \
-            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else \
-            "/tmp/moe_ep_clocks_%d.csv" % os.getpid()
+        self.path = path or "/tmp/moe_ep_clocks_%d.csv" % os.getpid()
         self.gpu = gpu_index
 
     def start(self):
@@ -260,7 +258,7 @@ def run_gpu(args, w):
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
            for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clocks_csv)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
@@ -818,6 +816,9 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="dsv3", choices=W.ORDER)
     p.add_argument("--impl", default="moe_ep", choices=["moe_ep", "reference"])
     p.add_argument("--e2e-steps", type=int, default=30)
+    p.add_argument("--clocks-csv", default=None,
+                   help="where the nvidia-smi clock samples of the timed steps go "
+                        "(default: a file in /tmp)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-deep-moe", action="store_true",
