@@ -1,7 +1,9 @@
 """Property tests of the oracle over random shapes (hypothesis): the layout,
-notify and receive-row invariants, and the quantisation bounds, on shapes the
-fixed-seed pins do not reach (empty batches, one rank, k = E, repeated experts
-in a token).  CPU only; skipped where hypothesis is not installed."""
+notify and receive-row invariants, the quantisation bounds and the combine
+(one-hot weights give the token back; general weights within the rounding
+bound of the fp64 sum), on shapes the fixed-seed pins do not reach (empty
+batches, one rank, k = E, repeated experts in a token).  CPU only; skipped
+where hypothesis is not installed."""
 import numpy as np
 import pytest
 import torch
@@ -103,3 +105,45 @@ def test_quant_row_any_shape(oracle_mod, H8, dtype, scale, zeros, seed):
     ok = margin > 1e-4
     np.testing.assert_array_equal(q[ok], qe[ok])
     assert (np.abs(q * inv - x) <= (amax + 1e-12) / 254 * (1 + 2.0 ** -14)).all()
+
+
+@settings(**SETTINGS)
+@given(R=st.integers(1, 4), epr=st.integers(1, 4), bs=st.integers(1, 12),
+       kfrac=st.floats(0.0, 1.0), H8=st.integers(1, 12), dtype=st.sampled_from([0, 1]),
+       seed=st.integers(0, 10 ** 6))
+def test_combine_any_shape(oracle_mod, R, epr, bs, kfrac, H8, dtype, seed):
+    """Combine over the dispatched rows: all the weight on one k gives the token
+    back exactly; general weights stay within the bf16/fp16 rounding of the
+    fp64 sum plus k fp32 roundings."""
+    E = R * epr
+    k = 1 + int(kfrac * (min(E, 6) - 1))
+    H = 8 * H8
+    wl = P.W.Workload("prop", R=R, epr=epr, bs=bs, H=H, k=k, dtype=dtype, quant=False,
+                      seed=seed)
+    idx, wt = P.W.routing(wl)
+    idx, wt = idx.numpy(), wt.numpy()
+    x = P.W.tokens(wl)
+    L = oracle_mod.layout(idx, R, epr)
+    N = oracle_mod.notify(L["count"], R, bs, epr)
+    recv, stt = oracle_mod.dispatch(P.W.bits(x), idx, L["send_idx"], N["put_offset"],
+                                    N["rank_recv_base"], R, epr, dtype, 0)
+    assert stt == 0
+    y = recv.view(np.uint16)
+    rng = np.random.default_rng(seed)
+    w1 = np.zeros_like(wt)
+    w1[np.arange(wl.T), rng.integers(0, k, size=wl.T)] = 1.0
+    out, stt = oracle_mod.combine(y, idx, w1, L["send_idx"], N["put_offset"],
+                                  N["rank_recv_base"], R, epr, dtype)
+    assert stt == 0
+    np.testing.assert_array_equal(oracle_mod.to_f32(out, dtype), x.float().numpy())
+    out, stt = oracle_mod.combine(y, idx, wt, L["send_idx"], N["put_offset"],
+                                  N["rank_recv_base"], R, epr, dtype)
+    rows = oracle_mod.dst_rows(idx, L["send_idx"], N["put_offset"],
+                               N["rank_recv_base"], R, epr)
+    yf = oracle_mod.to_f32(y, dtype).astype(np.float64)
+    terms = yf[rows] * wt[..., None].astype(np.float64)
+    ref = terms.sum(axis=1)
+    got = oracle_mod.to_f32(out, dtype).astype(np.float64)
+    rel = 2.0 ** -8 if dtype == 0 else 2.0 ** -10
+    tol = rel * np.abs(ref) + (k + 1) * 2.0 ** -23 * np.abs(terms).sum(axis=1) + 2.0 ** -24
+    assert (np.abs(got - ref) <= tol).all()
