@@ -45,6 +45,15 @@ extern "C" moe_status moe_dispatch_layout_static(
     int32_t* rank_send, int32_t* send_idx, int32_t* dev_status, void* stream) {
   const size_t need = moe_layout_workspace_bytes(shape);   // 0: invalid shape
   if (need > MOE_EP_STATIC_LAYOUT_WS_BYTES) return MOE_ERR_INVALID_ARG;
+  // the regular entry point's pointer checks, before this one's own CUDA
+  // calls (host-checkable errors return before any CUDA call)
+  auto misaligned4 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 3u) != 0; };
+  if (!count || !rank_send || !dev_status || misaligned4(count) || misaligned4(rank_send) ||
+      misaligned4(dev_status))
+    return MOE_ERR_INVALID_ARG;
+  if (need > 0 && int64_t(shape->R) * shape->bs * shape->k > 0 &&
+      (!topk_idx || !send_idx || misaligned4(topk_idx) || misaligned4(send_idx)))
+    return MOE_ERR_INVALID_ARG;
   if (need == 0)   // let the regular entry point report the invalid shape
     return moe_dispatch_layout(shape, topk_idx, count, rank_send, send_idx,
                                nullptr, dev_status, stream);
