@@ -102,3 +102,10 @@ def test_bad_shape_rejected(lib, name, args):
     plausible: rejected by the shape check."""
     for bad in (Shape(0, 16, 2, 2, 64, 0), Shape(2, 16, 2, 2, 60, 0)):
         assert _call(lib, name, args, bad, lambda pn: 0x10000) == INVALID_ARG
+
+
+@pytest.mark.parametrize("name,args", DECLS, ids=[n for n, _ in DECLS])
+def test_all_null_pointers_rejected(lib, name, args):
+    """Every pointer NULL (sizes plausible): rejected before any CUDA call."""
+    shape = Shape(2, 16, 2, 2, 64, 0)
+    assert _call(lib, name, args, shape, lambda pn: None) == INVALID_ARG
