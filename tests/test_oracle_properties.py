@@ -147,3 +147,32 @@ def test_combine_any_shape(oracle_mod, R, epr, bs, kfrac, H8, dtype, seed):
     rel = 2.0 ** -8 if dtype == 0 else 2.0 ** -10
     tol = rel * np.abs(ref) + (k + 1) * 2.0 ** -23 * np.abs(terms).sum(axis=1) + 2.0 ** -24
     assert (np.abs(got - ref) <= tol).all()
+
+
+@settings(**SETTINGS)
+@given(R=st.integers(1, 4), epr=st.integers(1, 4), bs=st.integers(1, 10),
+       kfrac=st.floats(0.0, 1.0), H8=st.integers(1, 16),
+       inv_exp=st.integers(-12, 6), seed=st.integers(0, 10 ** 6))
+def test_combine_quant_exact_scales_any_shape(oracle_mod, R, epr, bs, kfrac, H8, inv_exp,
+                                              seed):
+    """With 1/scale an exact power of two the dequantised value q * 1/scale is
+    exact, so the INT8 combine equals the combine of those values as bf16 rows
+    (exact in bf16: |q| <= 127 has 7 significant bits), bit for bit; H % 32 != 0
+    also checks where 1/scale is read."""
+    E = R * epr
+    k = 1 + int(kfrac * (min(E, 6) - 1))
+    H = 8 * H8
+    wl = P.W.Workload("propq", R=R, epr=epr, bs=bs, H=H, k=k, seed=seed)
+    idx, wt = P.W.routing(wl)
+    idx, wt = idx.numpy(), wt.numpy()
+    L = oracle_mod.layout(idx, R, epr)
+    N = oracle_mod.notify(L["count"], R, bs, epr)
+    args = (idx, wt, L["send_idx"], N["put_offset"], N["rank_recv_base"], R, epr, 0)
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(-127, 128, size=(wl.P, H))
+    inv = 2.0 ** inv_exp
+    img = P._int8_images(codes, np.full(wl.P, inv), H)
+    got, stt = oracle_mod.combine_quant(img, *args, H=H)
+    assert stt == 0
+    ref, _ = oracle_mod.combine(P._bf16_bits((codes * inv).astype(np.float32)), *args)
+    np.testing.assert_array_equal(got, ref)
