@@ -722,6 +722,29 @@ MUTANTS = {
     "deq_combine_fused_multiply_add": ("acc[h] = acc[h] + prod;",
                                        "acc[h] = fmaf(y, w, acc[h]);", 2),
     "exp_horner_coefficient_order": ("p = fmaf(p, r, 4.16666667e-2f);", "p = fmaf(p, r, 8.33333333e-3f);"),
+    "rank_send_strided_experts": ("sum += cnt[r * epr + j];", "sum += cnt[j * R + r];"),
+    "invalid_id_send_index_zero": ("send_idx[p] = -1;", "send_idx[p] = 0;"),
+    "rank_recv_base_inclusive": ("rank_recv_base[r] = base;\n    base += total_recv[r];",
+                                 "base += total_recv[r];\n    rank_recv_base[r] = base;"),
+    "recv_per_expert_one_source": ("for (int s = 0; s < R; ++s) sum += count[(int64_t)s * E + e];",
+                                   "for (int s = 0; s < 1; ++s) sum += count[(int64_t)s * E + e];"),
+    "max_bs_counts_all_ranks": ("max_bs[0] = bs;", "max_bs[0] = bs * R;"),
+    "source_rank_by_modulo": ("const int64_t s = g / bs;", "const int64_t s = g % R;"),
+    "quant_pads_not_zeroed": ("memset(out, 0, (size_t)Sq);", "memset(out, 0x5a, (size_t)Sq);"),
+    "verbatim_drops_last_element": ("memcpy(image, xrow, (size_t)S);",
+                                    "memcpy(image, xrow, (size_t)S - 2); memset(image + S - 2, 0, 2);"),
+    "combine_weight_of_first_k": ("const float w = topk_weights[g * k + kk];",
+                                  "const float w = topk_weights[g * k];", 0),
+    "combine_quant_weight_of_first_k": ("const float w = topk_weights[g * k + kk];",
+                                        "const float w = topk_weights[g * k];", 1),
+    "f16_ties_toward_zero": ("_Float16 h = (_Float16)f;",
+                             "_Float16 h = (_Float16)nextafterf(f, 0.0f);"),
+    "swiglu_up_uses_gate_scale": ("up = up * weight_scale[I + j];", "up = up * weight_scale[j];"),
+    "gemm_drops_last_k": ("for (int kk = 0; kk < K; ++kk) acc +=",
+                          "for (int kk = 0; kk < K - 1; ++kk) acc +="),
+    "requant_scale_stored": ("const float inv = 1.0f / scale;\n    memcpy(img + i_align",
+                             "const float inv = scale;\n    memcpy(img + i_align"),
+    "deq_combine_weight_scale_by_row": ("y = y * ws[h];", "y = y * ws[0];"),
 }
 
 
