@@ -1,9 +1,13 @@
 """Property tests of the oracle over random shapes (hypothesis): the layout,
-notify and receive-row invariants, the quantisation bounds and the combine
+notify and receive-row invariants, the quantisation bounds, the combine
 (one-hot weights give the token back; general weights within the rounding
-bound of the fp64 sum), on shapes the fixed-seed pins do not reach (empty
-batches, one rank, k = E, repeated experts in a token).  CPU only; skipped
-where hypothesis is not installed."""
+bound of the fp64 sum), the INT8 combine and DeqCombine where they reduce
+exactly to the combine, verbatim dispatch and a short receive buffer, the
+token-level layout against Python sets, the grouped GEMM against numpy int64
+matmuls and the GMM1 epilogue against a float64 restatement, on shapes the
+fixed-seed pins do not reach (empty batches and groups, one rank, k = E,
+repeated experts in a token).  CPU only; skipped where hypothesis is not
+installed."""
 import numpy as np
 import pytest
 import torch
@@ -176,3 +180,139 @@ def test_combine_quant_exact_scales_any_shape(oracle_mod, R, epr, bs, kfrac, H8,
     assert stt == 0
     ref, _ = oracle_mod.combine(P._bf16_bits((codes * inv).astype(np.float32)), *args)
     np.testing.assert_array_equal(got, ref)
+
+
+@settings(**SETTINGS)
+@given(case=routings(), H8=st.integers(1, 12), dtype=st.sampled_from([0, 1]),
+       capfrac=st.floats(0.0, 1.0))
+def test_dispatch_verbatim_and_capacity_any_shape(oracle_mod, case, H8, dtype, capfrac):
+    """Verbatim dispatch puts the bytes of x[g] in each of g's k rows (the
+    receive rows being the closed-form order); with a shorter receive buffer
+    the rows inside it are unchanged and status 3 is set exactly when some
+    row falls outside."""
+    R, epr, bs, k, idx = case
+    H = 8 * H8
+    T = R * bs
+    rng = np.random.default_rng(H8 * 7919 + T)
+    xb = rng.integers(0, 1 << 16, size=(T, H), dtype=np.uint16)
+    L = oracle_mod.layout(idx, R, epr)
+    N = oracle_mod.notify(L["count"], R, bs, epr)
+    args = (xb, idx, L["send_idx"], N["put_offset"], N["rank_recv_base"], R, epr, dtype, 0)
+    recv, stt = oracle_mod.dispatch(*args)
+    assert stt == 0
+    rows = P.rows_by_sort(idx)
+    y = recv.view(np.uint16).reshape(-1, H)
+    for g in range(T):
+        for kk in range(k):
+            np.testing.assert_array_equal(y[rows[g, kk]], xb[g])
+    cap = int(capfrac * T * k)
+    short, stt = oracle_mod.dispatch(*args, capacity_rows=cap)
+    assert stt == (3 if cap < T * k else 0)
+    np.testing.assert_array_equal(short[:cap], recv[:cap])
+
+
+@settings(**SETTINGS)
+@given(case=routings())
+def test_token_layout_any_shape(oracle_mod, case):
+    """Membership = the set of destination ranks of a token's experts (Python
+    sets); tokens per rank = membership summed over the source rank's tokens,
+    never more than the pair counts."""
+    R, epr, bs, k, idx = case
+    TL = oracle_mod.token_layout(idx, R, epr)
+    assert TL["status"] == 0
+    exp_in = np.zeros((R * bs, R), np.uint8)
+    for g in range(R * bs):
+        for r in {int(e) // epr for e in idx[g]}:
+            exp_in[g, r] = 1
+    np.testing.assert_array_equal(TL["in_rank"], exp_in)
+    np.testing.assert_array_equal(TL["tokens_per_rank"], exp_in.reshape(R, bs, R).sum(axis=1))
+    assert (TL["tokens_per_rank"] <= oracle_mod.layout(idx, R, epr)["rank_send"]).all()
+
+
+@st.composite
+def gemm_problems(draw):
+    G = draw(st.integers(1, 6))
+    sizes = draw(st.lists(st.integers(0, 20), min_size=G, max_size=G))
+    K = draw(st.integers(1, 300))
+    N = draw(st.integers(1, 24))
+    pad = draw(st.integers(0, 16))
+    seed = draw(st.integers(0, 2 ** 31 - 1))
+    return G, sizes, K, N, pad, seed
+
+
+@settings(**SETTINGS)
+@given(prob=gemm_problems())
+def test_grouped_gemm_any_shape(oracle_mod, prob):
+    """Each group's rows times that group's weights, as numpy int64 matmuls,
+    over random group sizes (empty groups included), K, N and row strides;
+    a random subset of listed rows gives the same rows."""
+    G, sizes, K, N, pad, seed = prob
+    rng = np.random.default_rng(seed)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    M = int(off[-1])
+    a = rng.integers(-128, 128, (M, K + pad)).astype(np.int8)
+    b = rng.integers(-128, 128, (G, N, K)).astype(np.int8)
+    c = oracle_mod.grouped_gemm(a.view(np.uint8), off, b)
+    assert c.shape == (M, N)
+    for g in range(G):
+        ref = a[off[g]:off[g + 1], :K].astype(np.int64) @ b[g].T.astype(np.int64)
+        np.testing.assert_array_equal(c[off[g]:off[g + 1]], ref)
+    if M:
+        rows = rng.choice(M, size=min(M, 5), replace=False).astype(np.int64)
+        np.testing.assert_array_equal(
+            oracle_mod.grouped_gemm(a[rows].view(np.uint8), off, b, rows=rows), c[rows])
+
+
+@settings(**SETTINGS)
+@given(R=st.integers(1, 4), epr=st.integers(1, 4), bs=st.integers(1, 10),
+       kfrac=st.floats(0.0, 1.0), H8=st.integers(1, 8), dtype=st.sampled_from([0, 1]),
+       seed=st.integers(0, 10 ** 6))
+def test_deq_combine_unit_scales_any_shape(oracle_mod, R, epr, bs, kfrac, H8, dtype, seed):
+    """With unit weight and row scales and accumulators exact in the token
+    dtype (|acc| <= 256), DeqCombine is the combine of those values, bit for
+    bit, in bf16 and fp16."""
+    E = R * epr
+    k = 1 + int(kfrac * (min(E, 6) - 1))
+    H = 8 * H8
+    wl = P.W.Workload("propdq", R=R, epr=epr, bs=bs, H=H, k=k, seed=seed)
+    idx, wt = P.W.routing(wl)
+    idx, wt = idx.numpy(), wt.numpy()
+    L = oracle_mod.layout(idx, R, epr)
+    N = oracle_mod.notify(L["count"], R, bs, epr)
+    rng = np.random.default_rng(seed)
+    acc2 = rng.integers(-256, 257, (wl.P, H)).astype(np.int32)
+    args = (idx, wt, L["send_idx"], N["put_offset"], N["rank_recv_base"], R, epr, dtype)
+    out, stt = oracle_mod.deq_combine(acc2, np.ones((E, H), np.float32),
+                                      np.ones(wl.P, np.float32), *args)
+    assert stt == 0
+    ref, _ = oracle_mod.combine(oracle_mod.from_f32(acc2.astype(np.float32), dtype), *args)
+    np.testing.assert_array_equal(out, ref)
+
+
+@settings(**SETTINGS)
+@given(M=st.integers(1, 12), I8=st.integers(1, 40), seed=st.integers(0, 2 ** 31 - 1))
+def test_swiglu_quant_any_shape(oracle_mod, M, I8, seed):
+    """GMM1 epilogue against a float64 restatement of dequant -> SwiGLU: the
+    stored 1/scale, the dequantisation error bound, codes equal to the
+    round-half-even of the float64 value away from ties, and zero pads."""
+    I = 8 * I8
+    rng = np.random.default_rng(seed)
+    acc = np.round(rng.standard_normal((M, 2 * I)) * 2.0 ** 17).astype(np.int32)
+    ws = (rng.uniform(0.5, 1.5, 2 * I) * 4e-4).astype(np.float32)
+    ts = rng.uniform(0.005, 0.03, M).astype(np.float32)
+    img = oracle_mod.swiglu_quant(acc, ws, ts)
+    ia = (I + 31) // 32 * 32
+    assert img.shape == (M, ia + 32)
+    assert not img[:, I:ia].any() and not img[:, ia + 4:].any()
+    q = img[:, :I].view(np.int8).astype(np.int64)
+    inv = img[:, ia:ia + 4].copy().view(np.float32)[:, 0].astype(np.float64)
+    v = acc.astype(np.float64) * ws.astype(np.float64) * ts.astype(np.float64)[:, None]
+    gate, up = v[:, :I], v[:, I:]
+    h = gate / (1.0 + np.exp(-gate)) * up
+    amax = np.abs(h).max(axis=1)
+    np.testing.assert_allclose(inv, (amax + 1e-12) / 127, rtol=1e-5)
+    err = np.abs(q * inv[:, None] - h)
+    assert (err <= (amax[:, None] + 1e-12) / 254 * (1 + 2.0 ** -10) + 1e-6 * np.abs(h)).all()
+    t = h * (127.0 / (amax + 1e-12))[:, None]
+    ok = np.abs(np.abs(t - np.floor(t)) - 0.5) > 1e-3
+    np.testing.assert_array_equal(q[ok], np.rint(t)[ok].astype(np.int64))
