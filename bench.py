@@ -749,9 +749,11 @@ def cpu_baseline(w, idx_h, wt_h, x_h, y_h, seconds):
     model, avail = host_cpu()
     return {"value": _oracle_tokens_per_s(w, t_ln, t_dc, n), "unit": "tokens/s",
             "cores": 1, "kind": "oracle", "cpu": model, "host_cores_available": avail,
-            "sample": "layout+notify on all %d tokens (%.3f s), dispatch+combine "
-                      "on %d random tokens (%.2f s), scaled to the full batch"
-                      % (w.T, t_ln, n, t_dc)}
+            "sample": "layout+notify on all %d tokens (%.2f ms), dispatch+combine on %s "
+                      "(%.2f s)%s"
+                      % (w.T, t_ln * 1e3,
+                         "all %d tokens" % n if n == w.T else "%d random tokens" % n, t_dc,
+                         "" if n == w.T else ", scaled to the full batch")}
 
 
 def run_reference(args, w):

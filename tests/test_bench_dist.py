@@ -84,3 +84,18 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2
     assert rec["value"] > 0 and rec["e2e"]["h2d_bytes_per_step"] == 0
     assert rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_cpu_baseline_leg_on_the_host():
+    """The cpu_baseline object the GPU arm adds: the oracle timed on the host
+    over a bounded sample (here the whole tiny batch fits), with the keys the
+    JSON line needs."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    w = W.WORKLOADS["tiny"]
+    idx, wt = W.routing(w)
+    cb = bench.cpu_baseline(w, idx, wt, W.tokens(w), W.expert_outputs(w), 0.5)
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["unit"] == "tokens/s"
+    assert cb["value"] > 0 and cb["host_cores_available"] >= 1
+    assert "all %d tokens" % w.T in cb["sample"]
