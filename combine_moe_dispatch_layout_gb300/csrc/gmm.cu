@@ -26,7 +26,9 @@
 // accumulator (tcgen05.ld; a warp reads its TMEM lane quarter, one output row
 // per thread, and one half of the columns) into int32 registers while the
 // next chunk accumulates, then store the tile's rows.  Every mbarrier wait is
-// bounded: a timeout sets MOE_ERR_TIMEOUT and the CTA stops issuing work.
+// bounded: a timeout sets MOE_ERR_TIMEOUT and the CTA stops issuing work,
+// then waits (bounded again) for the copies, MMAs and stores it already
+// issued before it releases TMEM and retires.
 #include <cuda.h>
 
 #include <algorithm>
@@ -320,7 +322,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     // ---- TMA producer ---------------------------------------------------------
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0;
+      uint32_t phase = 0, nload = 0;   // nload: stage fills issued
       for (int64_t t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
         const Tile tl = decode_tile(t, goff, tpre, G, ntn);
         const int brow = tl.g * N + tl.n0;
@@ -335,6 +337,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                       static_cast<int>(tl.row0), full + stage);
           tma_load_2d(smem_addr(smem + kOffB + stage * kTileBBytes), &tmB, kb * BK, brow,
                       full + stage);
+          ++nload;
           if (++stage == kStages) { stage = 0; phase ^= 1u; }
         }
       }
@@ -346,12 +349,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         if (++stage == kStages) { stage = 0; phase ^= 1u; }
       }
+      // after a timeout the stages may still be filling: wait (bounded) for
+      // the last fill of each stage, fill i being phase i / kStages of
+      // full[i % kStages], so no copy lands in shared memory after the CTA
+      // has retired
+      if (*abort_flag)
+        for (uint32_t i = nload > kStages ? nload - kStages : 0; i < nload; ++i)
+          mbar_wait_bounded(full + i % kStages, (i / kStages) & 1u, kSpin);
     }
   } else if (warp == 1) {
     // ---- MMA issuer -----------------------------------------------------------
     if (lane == 0) {
       int stage = 0;
-      uint32_t phase = 0, chunk_ctr = 0;
+      uint32_t phase = 0, chunk_ctr = 0, ncommit = 0;   // ncommit: stage releases
       bool ok = true;
       for (int64_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
         for (int c = 0; ok && c < nchunks; ++c, ++chunk_ctr) {
@@ -376,6 +386,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               mma_bf16(d, ad + 2 * kk, bd + 2 * kk,
                        (kb != c * kChunkBlocks || kk != 0) ? 1u : 0u);
             mma_commit(empty + stage);             // frees the stage when read
+            ++ncommit;
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
           }
           mma_commit(tfull + b);                   // the chunk's sums are final
@@ -384,6 +395,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       if (!ok) {
         set_status(dev_status, MOE_ERR_TIMEOUT);
         *abort_flag = 1;
+      }
+      // after a timeout, the MMAs already issued finish before TMEM is
+      // released: the last stage release (phase k / kStages of
+      // empty[k % kStages]) arrives once every earlier MMA of this thread is
+      // complete
+      if (*abort_flag && ncommit > 0) {
+        const uint32_t k = ncommit - 1;
+        mbar_wait_bounded(empty + k % kStages, (k / kStages) & 1u, kSpin);
       }
     }
   } else {
