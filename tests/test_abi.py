@@ -140,3 +140,54 @@ def test_status_strings(lib):
     assert lib.moe_status_string(0) == b"ok"
     assert b"expert" in lib.moe_status_string(2)
     assert lib.moe_status_string(99) == b"unknown status"
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "moe_ep.h"
+
+typedef void (*any_fn)(void);
+/* every declared entry point, so the declarations are type-checked */
+static any_fn all_entry_points[] = { %s };
+
+int main(void) {
+  moe_shape s;
+  int32_t dummy = 0;
+  s.R = 8; s.bs = 16; s.k = 8; s.experts_per_rank = 32; s.H = 7168; s.dtype = MOE_BF16;
+  if (moe_recv_row_bytes(&s, 1) != 7168 + 32) return 1;
+  if (moe_recv_row_bytes(&s, 0) != 2 * 7168) return 2;
+  if (moe_layout_workspace_bytes(&s) == 0) return 3;
+  if (strcmp(moe_status_string(MOE_OK), "ok") != 0) return 4;
+  /* host-side checks only: nothing here reaches the GPU */
+  if (moe_dispatch(&s, NULL, NULL, NULL, NULL, NULL, 1, NULL, 0, &dummy, NULL)
+      != MOE_ERR_INVALID_ARG) return 5;
+  s.H = 60;
+  if (moe_recv_row_bytes(&s, 1) != -1) return 6;
+  printf("%%d entry points\n", (int)(sizeof all_entry_points / sizeof all_entry_points[0]));
+  return 0;
+}
+"""
+
+
+@pytest.mark.parametrize("compiler,std", [("gcc", "-std=c99"), ("g++", "-std=c++17")])
+def test_header_is_plain_c_and_links(lib, tmp_path, compiler, std):
+    """The header compiles as strict C99 (and as C++) with warnings as errors,
+    and a C program linked to libmoe_ep.so calls the host-side entry points."""
+    if shutil.which(compiler) is None:
+        pytest.skip(compiler + " not available")
+    import __graft_entry__
+    so = __graft_entry__._load_builder().build()
+    names = declared_functions()
+    src = tmp_path / ("abi.c" if compiler == "gcc" else "abi.cpp")
+    src.write_text(C_PROGRAM % ", ".join("(any_fn)%s" % n for n in names))
+    exe = tmp_path / "abi"
+    import subprocess
+    r = subprocess.run([compiler, std, "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        "-I", os.path.join(ROOT, "include"), str(src), so,
+                        "-Wl,-rpath," + os.path.dirname(so), "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-3000:]
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stderr[-2000:])
+    assert r.stdout.strip() == "%d entry points" % len(names)
