@@ -60,6 +60,7 @@ def _load():
     L.moe_layout_workspace_bytes.argtypes = [sp]
     L.moe_layout_workspace_bytes.restype = ctypes.c_size_t
     L.moe_dispatch_layout.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_dispatch_layout_static.argtypes = [sp, vp, vp, vp, vp, vp, vp]
     L.moe_notify_dispatch.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_dispatch.argtypes = [sp, vp, vp, vp, vp, vp, ctypes.c_int, vp, i64,
                                vp, vp]
@@ -100,7 +101,7 @@ def _load():
                  "moe_grouped_gemm_i8_dequant", "moe_combine_f32",
                  "moe_dispatch_expand", "moe_swiglu_quant_grouped_bf16",
                  "moe_grouped_gemm_i8_swiglu", "moe_interleave_gate_up",
-                 "moe_quant_rows_bf16"):
+                 "moe_quant_rows_bf16", "moe_dispatch_layout_static"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -174,6 +175,22 @@ def moe_dispatch_layout(shape, topk_idx, count, rank_send, send_idx,
         _ptr(workspace, None, None, "workspace"),
         _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
     return _check(st, "moe_dispatch_layout")
+
+
+def moe_dispatch_layout_static(shape, topk_idx, count, rank_send, send_idx,
+                               dev_status, stream=None):
+    """Stage 1 without a caller workspace: the library's own scratch array
+    (for callers that cannot allocate device memory); calls that overlap on
+    the GPU must be serialised by the caller."""
+    R, E = shape.R, shape.R * shape.experts_per_rank
+    P = shape.R * shape.bs * shape.k
+    st = _lib.moe_dispatch_layout_static(
+        ctypes.byref(shape), _ptr(topk_idx, torch.int32, P, "topk_idx"),
+        _ptr(count, torch.int32, R * E, "count"),
+        _ptr(rank_send, torch.int32, R * R, "rank_send"),
+        _ptr(send_idx, torch.int32, P, "send_idx"),
+        _ptr(dev_status, torch.int32, 1, "dev_status"), _stream(stream))
+    return _check(st, "moe_dispatch_layout_static")
 
 
 def moe_notify_dispatch(shape, count, put_offset, total_recv, rank_recv_base,
@@ -562,3 +579,11 @@ def moe_quant_rows_bf16(h, group_off, codes, inv_scale, stream=None):
         int(G), _ptr(codes, torch.bfloat16, M * I, "codes"),
         _ptr(inv_scale, torch.float32, M, "inv_scale"), _stream(stream))
     return _check(st, "moe_quant_rows_bf16")
+
+
+# the size queries and the status names under the C entry points' own names
+moe_status_string = status_string
+moe_recv_row_bytes = recv_row_bytes
+moe_layout_workspace_bytes = layout_workspace_bytes
+moe_fused_workspace_bytes = fused_workspace_bytes
+moe_gmm_block_n = gmm_block_n

@@ -191,3 +191,29 @@ def test_header_is_plain_c_and_links(lib, tmp_path, compiler, std):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0, (r.returncode, r.stderr[-2000:])
     assert r.stdout.strip() == "%d entry points" % len(names)
+
+
+def test_python_binding_mirrors_the_header(lib):
+    """Every declared entry point has a Python function of the same name, and
+    the marshalling of the layout wrappers reaches the C side, which rejects
+    an invalid shape before any CUDA call (no GPU needed)."""
+    import combine_moe_dispatch_layout_gb300 as ep
+    missing = [n for n in declared_functions() if not callable(getattr(ep, n, None))]
+    assert not missing, missing
+
+    class HostStream:          # a stream handle the C side never uses here
+        cuda_stream = 0
+
+    bad = ep.make_shape(0, 16, 2, 2, 64)
+    for call in (lambda: ep.moe_dispatch_layout(bad, None, None, None, None, None, None,
+                                                HostStream()),
+                 lambda: ep.moe_dispatch_layout_static(bad, None, None, None, None, None,
+                                                       HostStream())):
+        with pytest.raises(ep.MoeError) as err:
+            call()
+        assert err.value.status == ep.MOE_ERR_INVALID_ARG
+    good = ep.make_shape(8, 16, 8, 32, 7168)
+    assert ep.moe_recv_row_bytes(good, 1) == 7200 and ep.moe_recv_row_bytes(good, 0) == 14336
+    assert ep.moe_layout_workspace_bytes(good) == ep.layout_workspace_bytes(good)
+    assert ep.moe_status_string(ep.MOE_ERR_CAPACITY) == "row outside the receive buffer"
+    assert ep.moe_gmm_block_n() > 0 and ep.moe_fused_workspace_bytes(good) > 0
