@@ -99,3 +99,19 @@ def test_cpu_baseline_leg_on_the_host():
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["unit"] == "tokens/s"
     assert cb["value"] > 0 and cb["host_cores_available"] >= 1
     assert "all %d tokens" % w.T in cb["sample"]
+
+
+@pytest.mark.parametrize("name,dispatch_gb,combine_gb", [
+    ("dsv3", 2.359, 4.231), ("skew", 1.082, 1.881), ("fp16", 1.210, 1.211),
+    ("maxrank", 3.540, 6.347)])
+def test_algorithmic_bytes_all_workloads(name, dispatch_gb, combine_gb):
+    """The roofline numerators: dispatch moves x once, k row images and the
+    pair indices (plus the count matrix and bases); combine moves k expert
+    rows, the pair indices and weights, and the output once.  Stated to
+    1 MB per workload."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    b = bench.alg_bytes(W.WORKLOADS[name])
+    assert b["dispatch"] / 1e9 == pytest.approx(dispatch_gb, abs=1e-3)
+    assert b["combine"] / 1e9 == pytest.approx(combine_gb, abs=1e-3)
