@@ -115,3 +115,31 @@ def test_algorithmic_bytes_all_workloads(name, dispatch_gb, combine_gb):
     b = bench.alg_bytes(W.WORKLOADS[name])
     assert b["dispatch"] / 1e9 == pytest.approx(dispatch_gb, abs=1e-3)
     assert b["combine"] / 1e9 == pytest.approx(combine_gb, abs=1e-3)
+
+
+def test_clock_record_parsing(tmp_path):
+    """The clocks object of the JSON line from nvidia-smi's CSV rows: median SM
+    clock under load, the maximum, and every throttle reason seen Active (a
+    run with a slowdown reason is rejected, so the parse must see it)."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class Done:                            # stands in for the finished nvidia-smi
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    rows = ["0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 1980, 2070, 1390.5, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 2070, 2070, 1200.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "0, 1500, 2070, 1400.0, 0x8, Active, Not Active, Not Active, Not Active"]
+    s = bench.ClockSampler(0, path=str(tmp_path / "clocks.csv"))
+    s.f = open(s.path, "w")
+    s.f.write("\n".join(rows) + "\n")
+    s.proc = Done()
+    rec = s.stop()
+    assert rec["samples"] == 4 and rec["sm_max_mhz"] == 2070.0
+    assert rec["sm_mhz"] == 2025.0                     # median of 1500, 1980, 2070, 2070
+    assert rec["reasons"] == ["hw_slowdown", "sw_power_cap"]
