@@ -1,7 +1,6 @@
-// combine_quant.cu -- stage 4 over INT8 expert outputs: the "+ dequant" of
-// the pipeline diagram (UMDK/CAM deep analysis v2, section 2.1, stage 4:
-// shmem read + weighted sum + dequant) on top of section 2.6's
-// ReadBufferAndWeightedSum.
+// combine_quant.cu -- stage 4 over INT8 expert outputs: the dequantisation
+// that the pipeline diagram (UMDK/CAM deep analysis v2, section 2.1) adds to
+// stage 4, on top of section 2.6's ReadBufferAndWeightedSum.
 //
 // Each expert-output row is a dispatched-style INT8 row image (codes, fp32
 // 1/scale at align32(H)).  Every element is dequantised as float(q) *

@@ -1,5 +1,5 @@
 // gmm.cu -- grouped GEMM of the fused deep MoE (UMDK/CAM deep analysis v2,
-// sections 4.1 and 4.3: GMM1 and GMM2, "INT8 x INT8 -> INT32", one weight
+// sections 4.1 and 4.3: GMM1 and GMM2, INT8 operands with INT32 sums, one weight
 // matrix per expert, each expert's rows contiguous in the receive buffer).
 //
 // sm_103a has no INT8 tensor-core MMA (tcgen05 .kind::i8 is not available on

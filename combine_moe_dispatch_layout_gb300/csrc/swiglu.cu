@@ -1,6 +1,6 @@
 // swiglu.cu -- GMM1 epilogue of the fused deep MoE, standalone (UMDK/CAM deep
 // analysis v2, section 4.8.1 PerTokenDequantSwiGLU and section 8.7
-// "INT32 -> [Cast + Dequant + SwiGLU + Quant] -> INT8").
+// int32 sums cast, dequantised, SwiGLU, requantised to INT8).
 //
 // Row m of the grouped GEMM's int32 accumulator acc [M][2I] becomes one INT8
 // row image, in one pass over HBM:

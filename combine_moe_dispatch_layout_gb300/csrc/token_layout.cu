@@ -1,6 +1,6 @@
 // token_layout.cu -- distinct tokens per destination rank (UMDK/CAM deep
-// analysis v2, section 2.3: "how many tokens each rank/expert must
-// receive", read at token granularity).  moe_dispatch_layout counts
+// analysis v2, section 2.3: the per-rank receive count, read at token
+// granularity).  moe_dispatch_layout counts
 // (token, k) pairs; this stage counts a token once per destination rank it
 // reaches, and records the token x rank membership map, as an expert-
 // parallel runtime that sends one copy of a token per rank would need.

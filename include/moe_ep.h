@@ -152,8 +152,8 @@ moe_status moe_dispatch_layout_static(const moe_shape* shape,
                                       int32_t* rank_send, int32_t* send_idx,
                                       int32_t* dev_status, void* stream);
 
-/* (1') Token-level layout -- section 2.3's "how many tokens each rank must
- * receive" counted in distinct tokens: a token that routes several of its k
+/* (1') Token-level layout -- section 2.3's per-rank receive count, counted
+ * in distinct tokens: a token that routes several of its k
  * pairs to experts of the same rank counts once for that rank.
  *   topk_idx        int32 [R][bs][k] (read)
  *   tokens_per_rank int32 [R][R]  tokens of source rank s reaching rank r
@@ -253,7 +253,7 @@ moe_status moe_dispatch_fused(const moe_shape* shape, const void* x,
 
 /* GMM1 epilogue of the fused deep MoE, as a standalone pass over the grouped
  * GEMM's int32 output (section 4.8.1 PerTokenDequantSwiGLU; section 8.7
- * "INT32 -> [Cast + Dequant + SwiGLU + Quant] -> INT8").  Per row m:
+ * int32 sums cast, dequantised, SwiGLU, requantised to INT8).  Per row m:
  *   v = fp32(acc[m][c]) * weight_scale[c] * token_scale[m]   (c < 2I)
  *   h[j] = (v[j] / (1 + exp(-v[j]))) * v[I + j]                (j < I)
  * then h is quantised like moe_dispatch's INT8 rows (scale = 127/(max|h| +
@@ -270,8 +270,8 @@ moe_status moe_swiglu_quant(const int32_t* acc, int64_t M, int32_t I,
                             const float* weight_scale, const float* token_scale,
                             void* out, int32_t* dev_status, void* stream);
 
-/* (4') Combine over INT8 expert outputs -- the "+ dequant" of the pipeline
- * diagram (section 2.1, stage 4: shmem read + weighted sum + dequant).
+/* (4') Combine over INT8 expert outputs -- the dequantisation the pipeline
+ * diagram of section 2.1 adds to stage 4 (remote read, weighted sum).
  * Same gather and arithmetic as moe_combine, except that each expert-output
  * row is an INT8 row image in the layout moe_dispatch writes
  * (moe_recv_row_bytes(shape, 1) bytes: H int8 codes, fp32 1/scale at byte
@@ -336,8 +336,8 @@ moe_status moe_grouped_gemm_i8(const void* a, int64_t a_rows, int32_t K, const v
                                int32_t G, int32_t N, const int32_t* group_rows, int32_t* c,
                                int32_t* dev_status, void* stream);
 
-/* Stage 1 of the fused deep MoE (section 4.3: "expand_x [M, h] (INT8)",
- * "dynamic_scale [M]"): moe_dispatch's dynamic INT8 quantisation with the two
+/* Stage 1 of the fused deep MoE (section 4.3's stage-1 outputs expand_x [M, h]
+ * INT8 and dynamic_scale [M]): moe_dispatch's dynamic INT8 quantisation with the two
  * outputs as separate arrays laid out for the tensor-core GEMM: the codes of
  * each (token, k) pair's row written as bf16 values (exactly the int8 codes
  * moe_dispatch writes, -127..127), and that row's 1/scale into
@@ -362,7 +362,7 @@ moe_status moe_swiglu_quant_grouped_bf16(const int32_t* acc, int64_t M, int32_t 
                                          void* stream);
 
 /* moe_grouped_gemm_i8 with the GMM2 dequantisation of section 4.3 stage 3
- * ("Read INT32 -> Cast FP32 -> x weight_scale -> x per_token_scale") done
+ * (the int32 sums cast to fp32, times the weight scale, times the per-token scale) done
  * in the GEMM's epilogue registers: for row m of group g,
  *   y[m][n] = (fp32(c[m][n]) * col_scale[g][n]) * row_scale(m)
  * with each product rounded to nearest even, row_scale(m) the fp32 at byte

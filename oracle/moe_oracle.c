@@ -343,7 +343,7 @@ int oracle_combine_tokens(int R, int bs, int k, int epr, int H, int dtype,
   return status;
 }
 
-/* ---- combine over INT8 expert outputs (section 2.1 "+ dequant") ---------- */
+/* ---- combine over INT8 expert outputs (section 2.1, stage 4 dequantised) - */
 
 int oracle_combine_quant_tokens(int R, int bs, int k, int epr, int H, int dtype,
                                 const uint8_t* yq, int64_t y_rows,

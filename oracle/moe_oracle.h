@@ -108,8 +108,8 @@ int oracle_combine_tokens(int R, int bs, int k, int epr, int H, int dtype,
                           const int64_t* rank_recv_base,
                           const int64_t* tokens, int64_t ntok, uint16_t* out);
 
-/* Token-level layout (the per-rank count read as distinct tokens, section
- * 2.3 "how many tokens each rank/expert must receive"): in_rank[g][r] = 1
+/* Token-level layout (section 2.3's per-rank receive count, read as distinct
+ * tokens): in_rank[g][r] = 1
  * when token g routes at least one of its k pairs to an expert of rank r;
  * tokens_per_rank[s][r] = number of tokens of source rank s with
  * in_rank = 1.  Ids outside [0,E) are ignored (return 2). */
@@ -139,8 +139,8 @@ void oracle_swiglu_quant_rows(int64_t M, int I, const int32_t* acc,
                               const float* token_scale, const int64_t* rows,
                               int64_t nrows, uint8_t* out);
 
-/* Combine over INT8 expert outputs (the "+ dequant" of the pipeline diagram,
- * section 2.1).  yq holds y_rows rows of oracle_row_bytes(H, 1) bytes laid
+/* Combine over INT8 expert outputs (the dequantisation the pipeline diagram
+ * of section 2.1 adds to stage 4).  yq holds y_rows rows of oracle_row_bytes(H, 1) bytes laid
  * out like a dispatched INT8 row (H codes, fp32 1/scale at align32(H)).
  * Per element: t = float(q) * inv (one rounding), then the combine of
  * section 2.6: acc = acc + (t * w), RNE to the token dtype. */
