@@ -316,3 +316,39 @@ def test_swiglu_quant_any_shape(oracle_mod, M, I8, seed):
     t = h * (127.0 / (amax + 1e-12))[:, None]
     ok = np.abs(np.abs(t - np.floor(t)) - 0.5) > 1e-3
     np.testing.assert_array_equal(q[ok], np.rint(t)[ok].astype(np.int64))
+
+
+@settings(**SETTINGS)
+@given(case=routings(), frac=st.floats(0.0, 0.5), seed=st.integers(0, 2 ** 31 - 1))
+def test_invalid_ids_any_shape(oracle_mod, case, frac, seed):
+    """Pairs with an expert id outside [0, E) (-1, E, or far out of range) are
+    not counted, get send index -1 and status 2; the valid pairs keep the
+    stable numbering and their receive rows are a bijection onto
+    [0, valid pairs) in the closed-form order of the valid pairs alone."""
+    R, epr, bs, k, idx = case
+    E = R * epr
+    rng = np.random.default_rng(seed)
+    idx = idx.copy()
+    bad = rng.random(idx.shape) < frac
+    idx[bad] = rng.choice(np.array([-1, E, E + 7, -(2 ** 31)], dtype=np.int64),
+                          size=int(bad.sum())).astype(np.int32)
+    L = oracle_mod.layout(idx, R, epr)
+    assert L["status"] == (2 if bad.any() else 0)
+    assert (L["send_idx"][bad] == -1).all()
+    valid = ~bad
+    cnt = L["count"].astype(np.int64)
+    assert cnt.sum() == int(valid.sum())
+    for s in range(R):
+        sub_idx = idx[s * bs:(s + 1) * bs].reshape(-1)
+        sub_send = L["send_idx"][s * bs:(s + 1) * bs].reshape(-1)
+        for e in range(E):
+            np.testing.assert_array_equal(sub_send[sub_idx == e], np.arange(cnt[s, e]))
+    N = oracle_mod.notify(L["count"], R, bs, epr)
+    rows = oracle_mod.dst_rows(idx, L["send_idx"], N["put_offset"], N["rank_recv_base"],
+                               R, epr)
+    assert (rows[bad] == -1).all()
+    assert sorted(rows[valid].tolist()) == list(range(int(valid.sum())))
+    # closed form over the valid pairs: ordered by (expert, token, k)
+    g, kk = np.nonzero(valid)
+    order = np.lexsort((kk, g, idx[valid]))
+    np.testing.assert_array_equal(rows[g[order], kk[order]], np.arange(len(order)))
