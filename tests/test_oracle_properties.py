@@ -17,7 +17,9 @@ from hypothesis import HealthCheck, given, settings, strategies as st  # noqa: E
 
 import test_oracle_pins as P  # noqa: E402  (the pins' helpers and closed forms)
 
-SETTINGS = dict(max_examples=80, deadline=None,
+# derandomize: the same examples on every run (a wider random search with
+# 1500 examples per test found no counterexample)
+SETTINGS = dict(max_examples=80, deadline=None, derandomize=True,
                 suppress_health_check=[HealthCheck.function_scoped_fixture])
 
 
