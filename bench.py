@@ -211,25 +211,26 @@ class ClockSampler:
 # the GPU arm
 # ---------------------------------------------------------------------------
 
-def run_gpu(args, w):
-    world, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    init_dist(world, "nccl")
-    import combine_moe_dispatch_layout_gb300 as ep  # noqa: F401 (loads the .so)
-    from combine_moe_dispatch_layout_gb300 import pipeline as pl
-    dev = torch.device("cuda", local)
+def _events(n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
-    idx_h, wt_h = W.routing(w)
-    x_h = W.tokens(w)
-    y_h = W.expert_outputs(w)
-    idx, wt, x = idx_h.to(dev), wt_h.to(dev), x_h.to(dev)
-    y = y_h.to(dev)
+
+def _mean_us(pairs):
+    return float(np.mean([a.elapsed_time(c) for a, c in pairs])) * 1e3
+
+
+def measure_pipeline(w, dev, stream, flush, x, idx, wt, y, steps, warmup,
+                     barrier_fn=None):
+    """The four-stage step on one workload: per-stage device times (CUDA
+    events on the launching stream, L2 flushed before every step), the same
+    step replayed from a CUDA graph, and the one-launch dispatch against the
+    three separate launches (eager and graph-replayed).  Returns (record,
+    buffers)."""
+    from combine_moe_dispatch_layout_gb300 import pipeline as pl
     b = pl.PipelineBuffers(w.R, w.bs, w.k, w.epr, w.H, w.dtype, w.quant,
                            device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
-    def step(evs=None, st=None):
+    def step(evs=None, st=None, upto=4):
         st = stream if st is None else st
         if evs:
             evs[0].record(st)
@@ -245,116 +246,179 @@ def run_gpu(args, w):
         pl.run_dispatch(b, x, idx, st)
         if evs:
             evs[3].record(st)
-        pl.run_combine(b, y, idx, wt, st)
-        if evs:
-            evs[4].record(st)
+        if upto > 3:
+            pl.run_combine(b, y, idx, wt, st)
+            if evs:
+                evs[4].record(st)
 
-    for i in range(args.warmup):
+    def check(what):
+        torch.cuda.synchronize()
+        if b.status() != 0:
+            raise RuntimeError("%s: device status %d in %s" % (w.name, b.status(), what))
+
+    for i in range(warmup):
         flush.fill_(i & 0xff)
         step()
-    torch.cuda.synchronize()
-    if b.status() != 0:
-        raise RuntimeError("device status %d after warm-up" % b.status())
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
-           for _ in range(args.steps)]
-    clocks = ClockSampler(local, args.clocks_csv)
-    clocks.start()
-    barrier(world)
+    check("warm-up")
+    evs = [_events(5) for _ in range(steps)]
+    if barrier_fn:
+        barrier_fn()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(steps):
         flush.fill_(i & 0xff)        # between steps, outside the events
         step(evs[i])
-    torch.cuda.synchronize()
-    barrier(world)
+    check("timed steps")
+    if barrier_fn:
+        barrier_fn()
     wall = time.perf_counter() - t0
-    clk = clocks.stop()
-    if b.status() != 0:
-        raise RuntimeError("device status %d after timed steps" % b.status())
+    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)]
+                         for i in range(steps)])
 
-    stage_ms = np.array([[evs[i][j].elapsed_time(evs[i][j + 1])
-                          for j in range(4)] for i in range(args.steps)])
-    step_ms = stage_ms.sum(axis=1)
-    mean_step_ms = float(step_ms.mean())
+    def graph_of(fn):
+        gs = torch.cuda.Stream(dev)
+        gs.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gs):
+            with torch.cuda.graph(g, stream=gs):
+                fn(gs)
+        stream.wait_stream(gs)
+        return g
+
+    def timed(fn, n):
+        pairs = []
+        for i in range(n):
+            flush.fill_(i & 0xff)
+            a0, a1 = _events(2)
+            a0.record(stream)
+            fn()
+            a1.record(stream)
+            pairs.append((a0, a1))
+        return pairs
+
+    n_extra = min(steps, EXTRA_STEPS)
+    g_step = graph_of(lambda st: step(st=st))
+    graph_step = timed(g_step.replay, n_extra)
+    check("graph replay")
+    del g_step
+    for i in range(3):
+        pl.run_dispatch_fused(b, x, idx, stream)
+    check("one-launch dispatch")
+    fused = timed(lambda: pl.run_dispatch_fused(b, x, idx, stream), n_extra)
+    check("one-launch dispatch")
+    g_fused = graph_of(lambda st: pl.run_dispatch_fused(b, x, idx, st))
+    g_sep = graph_of(lambda st: step(st=st, upto=3))
+    fused_graph = timed(g_fused.replay, n_extra)
+    sep_graph = timed(g_sep.replay, n_extra)
+    check("graph replay of the dispatch paths")
+    del g_fused, g_sep
+    stage_mean = stage_ms.mean(axis=0)
+    rec = {"steps": steps, "stage_ms": stage_mean, "step_ms": stage_ms.sum(axis=1),
+           "wall_s": wall,
+           "graph_step_us": _mean_us(graph_step),
+           "dispatch_fused": {
+               "us": _mean_us(fused),
+               "separate_us": float(stage_mean[0] + stage_mean[1] + stage_mean[2]) * 1e3,
+               "graph_us": _mean_us(fused_graph),
+               "separate_graph_us": _mean_us(sep_graph),
+               "note": "layout+notify+dispatch in one cooperative launch vs three "
+                       "launches; graph_us / separate_graph_us: the same replayed "
+                       "from CUDA graphs (device time without host enqueue)"}}
+    return rec, b
+
+
+def config_record(w, m, peak, peak_kind, cpu=None):
+    """The per-workload object of the JSON line from measure_pipeline's
+    record: step and stage times, tokens/s, and dispatch / combine against
+    the HBM roofline."""
+    stage_mean = m["stage_ms"]
+    names = ["layout", "notify", "dispatch", "combine"]
+    ab = alg_bytes(w)
+    step_ms = float(m["step_ms"].mean())
+
+    def roof(n, j):
+        ms = float(stage_mean[j])
+        gbs = ab[n] / (ms * 1e-3) / 1e9
+        return {"kernel": n, "bound": "hbm", "achieved": gbs, "peak": peak,
+                "peak_source": peak_kind, "unit": "GB/s", "frac": gbs / peak,
+                "traffic": recorded_traffic(n, w.name), "algorithmic_bytes": ab[n],
+                "avg_launch_ms": ms, "tokens_per_s": w.T / (ms * 1e-3)}
+    disp, comb = roof("dispatch", 2), roof("combine", 3)
+    return {
+        "workload": workload_desc(w),
+        "steps": m["steps"],
+        "step_us": step_ms * 1e3,
+        "tokens_per_s": w.T / (step_ms * 1e-3),
+        "dispatch_combine_tokens_per_s": w.T / ((stage_mean[2] + stage_mean[3]) * 1e-3),
+        "stages_us": {n: float(stage_mean[j] * 1e3) for j, n in enumerate(names)},
+        "stages_gbs": {n: ab[n] / (stage_mean[j] * 1e-3) / 1e9 for j, n in enumerate(names)},
+        "roofline": comb if comb["avg_launch_ms"] >= disp["avg_launch_ms"] else disp,
+        "roofline_dispatch": disp,
+        "roofline_combine": comb,
+        "graph_step_us": m["graph_step_us"],
+        "dispatch_fused": m["dispatch_fused"],
+        "cpu_baseline": cpu,
+    }
+
+
+def run_gpu(args, w):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    import combine_moe_dispatch_layout_gb300 as ep  # noqa: F401 (loads the .so)
+    from combine_moe_dispatch_layout_gb300 import pipeline as pl
+    dev = torch.device("cuda", local)
+    peak, peak_kind = measured_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+
+    idx_h, wt_h = W.routing(w)
+    x_h = W.tokens(w)
+    idx, wt, x = idx_h.to(dev), wt_h.to(dev), x_h.to(dev)
+    y = W.expert_outputs_device(w, dev)
+
+    clocks = ClockSampler(local, args.clocks_csv)
+    clocks.start()
+    m, b = measure_pipeline(w, dev, stream, flush, x, idx, wt, y, args.steps,
+                            args.warmup, barrier_fn=lambda: barrier(world))
+    clk = clocks.stop()
+    stage_mean = m["stage_ms"]
+    mean_step_ms = float(m["step_ms"].mean())
     max_step_ms = reduce_max(mean_step_ms, world, dev)
     value = aggregate_tokens_per_s(w.T, world, max_step_ms / 1e3)
-    stage_mean = stage_ms.mean(axis=0)
     ab = alg_bytes(w)
-    names = ["layout", "notify", "dispatch", "combine"]
-    peak, peak_kind = measured_peaks()
-    gbs = {n: ab[n] / (stage_mean[j] * 1e-3) / 1e9 for j, n in enumerate(names)}
+    gbs = {n: ab[n] / (stage_mean[j] * 1e-3) / 1e9
+           for j, n in enumerate(["layout", "notify", "dispatch", "combine"])}
 
     # ---- combine over INT8 expert outputs (moe_combine_quant) -------------
+    def timed(fn, n):
+        pairs = []
+        for i in range(n):
+            flush.fill_(i & 0xff)
+            a0, a1 = _events(2)
+            a0.record(stream)
+            fn()
+            a1.record(stream)
+            pairs.append((a0, a1))
+        torch.cuda.synchronize()
+        return _mean_us(pairs)
+    n_extra = min(args.steps, EXTRA_STEPS)
     cq = None
     if w.quant:
         yq = W.expert_outputs_int8(w).to(dev)
         for i in range(3):
             pl.run_combine_quant(b, yq, idx, wt, stream)
-        cq_ms = []
-        for i in range(min(args.steps, EXTRA_STEPS)):
-            flush.fill_(i & 0xff)
-            c0 = torch.cuda.Event(enable_timing=True)
-            c1 = torch.cuda.Event(enable_timing=True)
-            c0.record(stream)
-            pl.run_combine_quant(b, yq, idx, wt, stream)
-            c1.record(stream)
-            cq_ms.append((c0, c1))
-        torch.cuda.synchronize()
+        cq_us = timed(lambda: pl.run_combine_quant(b, yq, idx, wt, stream), n_extra)
         if b.status() != 0:
             raise RuntimeError("device status %d in combine_quant" % b.status())
-        cq_us = float(np.mean([a.elapsed_time(c) for a, c in cq_ms])) * 1e3
-        cq_bytes = alg_bytes(w)["combine_quant"]
+        cq_bytes = ab["combine_quant"]
         cq = {"us": cq_us, "achieved_gbs": cq_bytes / (cq_us * 1e-6) / 1e9,
               "algorithmic_bytes": cq_bytes,
               "traffic": recorded_traffic("combine_quant", w.name),
               "frac": cq_bytes / (cq_us * 1e-6) / 1e9 / peak,
               "tokens_per_s": w.T / (cq_us * 1e-6)}
         del yq
-
-    # ---- the same step replayed as a CUDA graph (no host enqueue cost) ------
-    gs = torch.cuda.Stream(dev)
-    gs.wait_stream(stream)
-    with torch.cuda.stream(gs):
-        step_graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(step_graph, stream=gs):
-            step(st=gs)
-    stream.wait_stream(gs)
-    graph_ev = []
-    for i in range(min(args.steps, EXTRA_STEPS)):
-        flush.fill_(i & 0xff)
-        g0 = torch.cuda.Event(enable_timing=True)
-        g1 = torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        step_graph.replay()
-        g1.record(stream)
-        graph_ev.append((g0, g1))
-    torch.cuda.synchronize()
-    if b.status() != 0:
-        raise RuntimeError("device status %d in graph replay" % b.status())
-    graph_us = float(np.mean([a.elapsed_time(c) for a, c in graph_ev])) * 1e3
-    del step_graph
-
-    # ---- one-launch low-latency dispatch vs the three separate launches ------
-    def timed(fn, n):
-        evs = []
-        for i in range(n):
-            flush.fill_(i & 0xff)
-            a0 = torch.cuda.Event(enable_timing=True)
-            a1 = torch.cuda.Event(enable_timing=True)
-            a0.record(stream)
-            fn()
-            a1.record(stream)
-            evs.append((a0, a1))
-        torch.cuda.synchronize()
-        return float(np.mean([a.elapsed_time(c) for a, c in evs])) * 1e3
-    for i in range(3):
-        pl.run_dispatch_fused(b, x, idx, stream)
-    fused_us = timed(lambda: pl.run_dispatch_fused(b, x, idx, stream),
-                     min(args.steps, EXTRA_STEPS))
-    if b.status() != 0:
-        raise RuntimeError("device status %d in fused dispatch" % b.status())
-    separate_us = float(stage_mean[0] + stage_mean[1] + stage_mean[2]) * 1e3
 
     # ---- GMM1 epilogue (moe_swiglu_quant): one row per dispatched pair, I=2048
     sw = None
@@ -368,8 +432,9 @@ def run_gpu(args, w):
         for i in range(3):
             ep.moe_swiglu_quant(acc_d, ws_d, ts_d, sw_out, b.dev_status, stream)
         sw_us = timed(lambda: ep.moe_swiglu_quant(acc_d, ws_d, ts_d, sw_out,
-                                                  b.dev_status, stream),
-                      min(args.steps, EXTRA_STEPS))
+                                                  b.dev_status, stream), n_extra)
+        if b.status() != 0:
+            raise RuntimeError("device status %d in swiglu_quant" % b.status())
         sw_bytes = w.P * (8 * I + (I + 31) // 32 * 32 + 32 + 4) + 8 * I
         sw = {"us": sw_us, "rows": w.P, "I": I, "algorithmic_bytes": sw_bytes,
               "traffic": recorded_traffic("swiglu_quant", w.name),
@@ -382,19 +447,10 @@ def run_gpu(args, w):
     inr = torch.empty((w.T, w.R), dtype=torch.uint8, device=dev)
     for i in range(3):
         ep.moe_token_layout(b.shape, idx, tpr, inr, b.dev_status, stream)
-    tl_ev = []
-    for i in range(min(args.steps, EXTRA_STEPS)):
-        flush.fill_(i & 0xff)
-        t0e = torch.cuda.Event(enable_timing=True)
-        t1e = torch.cuda.Event(enable_timing=True)
-        t0e.record(stream)
-        ep.moe_token_layout(b.shape, idx, tpr, inr, b.dev_status, stream)
-        t1e.record(stream)
-        tl_ev.append((t0e, t1e))
-    torch.cuda.synchronize()
+    tl_us = timed(lambda: ep.moe_token_layout(b.shape, idx, tpr, inr, b.dev_status,
+                                              stream), n_extra)
     if b.status() != 0:
         raise RuntimeError("device status %d in token_layout" % b.status())
-    tl_us = float(np.mean([a.elapsed_time(c) for a, c in tl_ev])) * 1e3
     del tpr, inr
 
     # ---- fused deep MoE (dispatch -> GMM1 -> DeqSwigluQuant -> GMM2 ->
@@ -406,14 +462,28 @@ def run_gpu(args, w):
     # ---- end to end through the public API with host buffers --------------
     e2e = run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush)
     e2e_max_ms = reduce_max(e2e["ms_per_step"], world, dev)
+    y_h = y.cpu() if want_cpu else None
+    del b, y
+    torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if want_cpu:
         cpu = cpu_baseline(w, idx_h, wt_h, x_h, y_h, args.cpu_seconds)
+    del y_h
+    head = config_record(w, m, peak, peak_kind, cpu)
+
+    # ---- the other workloads, measured the same way -------------------------
+    per_config = {}
+    if not args.no_per_config and world == 1:
+        for name in W.ORDER:
+            if name == w.name:
+                per_config[name] = head
+                continue
+            per_config[name] = run_other_config(args, W.WORKLOADS[name], dev, stream,
+                                                flush, peak, peak_kind, want_cpu)
 
     if rank != 0:
         return None
-    comb_ms = float(stage_mean[3])
     rec = {
         "metric": "dispatch+combine tokens/s",
         "value": value,
@@ -426,7 +496,8 @@ def run_gpu(args, w):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "data": "synthetic",
+        "data": "synthetic (seeded: routing, weights and x drawn on the host, "
+                "expert outputs drawn on the device)",
         "config": {
             "workload": workload_desc(w),
             "step": "layout+notify+dispatch+combine, inputs resident in HBM",
@@ -435,50 +506,54 @@ def run_gpu(args, w):
             "io_dtype": "bf16" if w.dtype == W.BF16 else "fp16",
             "recv_rows": "int8 + fp32 1/scale" if w.quant else "verbatim",
         },
-        "roofline": {
-            "kernel": "combine",
-            "bound": "hbm",
-            "achieved": gbs["combine"],
-            "peak": peak,
-            "peak_source": peak_kind,
-            "unit": "GB/s",
-            "frac": gbs["combine"] / peak,
-            "traffic": recorded_traffic("combine", w.name),
-            "algorithmic_bytes": ab["combine"],
-            "avg_launch_ms": comb_ms,
-        },
-        "roofline_dispatch": {
-            "bound": "hbm", "achieved": gbs["dispatch"], "peak": peak,
-            "unit": "GB/s", "frac": gbs["dispatch"] / peak,
-            "traffic": recorded_traffic("dispatch", w.name),
-            "algorithmic_bytes": ab["dispatch"],
-            "avg_launch_ms": float(stage_mean[2]),
-        },
+        "roofline": dict(head["roofline_combine"]),
+        "roofline_dispatch": head["roofline_dispatch"],
         "combine_quant": cq,
         "token_layout_us": tl_us,
-        "graph_step_us": graph_us,
+        "graph_step_us": m["graph_step_us"],
         "swiglu_quant": sw,
         "deep_moe": deep,
-        "dispatch_fused": {"us": fused_us, "separate_us": separate_us,
-                           "note": "layout+notify+dispatch in one cooperative "
-                                   "launch vs three launches"},
-        "stages_us": {n: float(stage_mean[j] * 1e3) for j, n in enumerate(names)},
+        "dispatch_fused": m["dispatch_fused"],
+        "stages_us": head["stages_us"],
         "stages_gbs": gbs,
-        "dispatch_combine_tokens_per_s": w.T / ((stage_mean[2] + stage_mean[3]) * 1e-3),
+        "dispatch_combine_tokens_per_s": head["dispatch_combine_tokens_per_s"],
         "e2e": {"value": aggregate_tokens_per_s(w.T, world, e2e_max_ms / 1e3),
                 "unit": "tokens/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "ms_per_step": e2e_max_ms, "steps": e2e["steps"],
+                "link_ms_per_step": e2e["link_ms_per_step"],
+                "frac_of_link": e2e["link_ms_per_step"] / e2e["ms_per_step"],
                 "note": "every step copies x, topk_idx, topk_weights from pinned "
                         "host memory and out back inside the timed region; copies "
                         "of neighbouring steps overlap compute (3 streams); expert "
-                        "outputs y stay on the device (they are produced there)"},
+                        "outputs y stay on the device (they are produced there). "
+                        "link_ms_per_step: the same copies on the same streams and "
+                        "buffers with no kernels, timed first in this run"},
         "gpu_launches": 4 * args.steps,
         "clocks": clk,
-        "wall_s_timed_region": wall,
+        "wall_s_timed_region": m["wall_s"],
         "cpu_baseline": cpu,
+        "per_config": per_config,
     }
     return rec
+
+
+def run_other_config(args, w, dev, stream, flush, peak, peak_kind, want_cpu):
+    """One non-headline workload: inputs drawn, the four-stage step timed
+    (fewer steps than the headline), the oracle timed beside it."""
+    idx_h, wt_h = W.routing(w)
+    x_h = W.tokens(w)
+    idx, wt, x = idx_h.to(dev), wt_h.to(dev), x_h.to(dev)
+    y = W.expert_outputs_device(w, dev)
+    steps = max(3, min(args.steps, args.per_config_steps))
+    m, b = measure_pipeline(w, dev, stream, flush, x, idx, wt, y, steps, 3)
+    y_h = y.cpu() if want_cpu else None
+    del b, x, y, idx, wt
+    torch.cuda.empty_cache()
+    cpu = None
+    if want_cpu:
+        cpu = cpu_baseline(w, idx_h, wt_h, x_h, y_h, args.cpu_seconds)
+    return config_record(w, m, peak, peak_kind, cpu)
 
 
 def run_deep_moe_bench(args, w, ep, pl, x, idx, wt, stream, dev, flush):
@@ -639,7 +714,7 @@ def run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush):
     consumed = [torch.cuda.Event() for _ in range(2)]
     drained = [torch.cuda.Event() for _ in range(2)]
 
-    def one(i):
+    def one(i, compute=True):
         j = i % 2
         with torch.cuda.stream(s_h2d):
             if i >= 2:
@@ -653,31 +728,37 @@ def run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush):
         if i >= 2:
             stream.wait_event(drained[j])
         b.out = out_d[j]
-        pl.run_pipeline(b, x_d[j], idx_d[j], wt_d[j], y, stream)
+        if compute:
+            pl.run_pipeline(b, x_d[j], idx_d[j], wt_d[j], y, stream)
         consumed[j].record(stream)
         with torch.cuda.stream(s_d2h):
             s_d2h.wait_event(consumed[j])
             outs_p[j].copy_(out_d[j], non_blocking=True)
             drained[j].record(s_d2h)
 
-    for i in range(n_warm):
-        one(i)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(s_h2d)
-    for i in range(steps):
-        one(n_warm + i)
-    s_d2h.wait_event(consumed[(n_warm + steps - 1) % 2])
-    e1.record(s_d2h)
-    torch.cuda.synchronize()
+    def run(compute):
+        for i in range(n_warm):
+            one(i, compute)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s_h2d)
+        for i in range(steps):
+            one(n_warm + i, compute)
+        e1.record(s_d2h)      # after the last D2H copy, which waited for compute
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    # the ceiling first: the same copies, streams and buffers, no kernels
+    link_ms = run(False)
+    ms = run(True)
     b.out = out_d[0]
     if b.status() != 0:
         raise RuntimeError("device status %d in e2e" % b.status())
     h2d = (x_p.numel() * x_p.element_size() + idx_p.numel() * 4
            + wt_p.numel() * 4)
     d2h = outs_p[0].numel() * outs_p[0].element_size()
-    return {"ms_per_step": e0.elapsed_time(e1) / steps, "h2d": h2d, "d2h": d2h,
+    return {"ms_per_step": ms, "link_ms_per_step": link_ms, "h2d": h2d, "d2h": d2h,
             "steps": steps}
 
 
@@ -685,25 +766,88 @@ def run_e2e(args, w, b, pl, idx_h, wt_h, x_h, y, stream, dev, flush):
 # the oracle on the host (cpu_baseline and --impl reference)
 # ---------------------------------------------------------------------------
 
-def _oracle_step(o, w, idx_np, wt_np, x_bits, y_bits, tokens):
-    """One bounded sample: layout + notify over the whole batch, then
-    dispatch and combine of the sampled tokens.  Returns seconds per phase."""
-    t0 = time.perf_counter()
-    L = o.layout(idx_np, w.R, w.epr)
-    N = o.notify(L["count"], w.R, w.bs, w.epr)
-    t1 = time.perf_counter()
-    o.dispatch_tokens(x_bits, idx_np, L["send_idx"], N["put_offset"],
-                      N["rank_recv_base"], w.R, w.epr, w.dtype, w.quant, tokens)
-    o.combine(y_bits, idx_np, wt_np, L["send_idx"], N["put_offset"],
-              N["rank_recv_base"], w.R, w.epr, w.dtype, tokens=tokens)
-    t2 = time.perf_counter()
-    return t1 - t0, t2 - t1
+class OracleHost:
+    """The CPU oracle on the host cores, as it stands.  Layout and notify run
+    on one thread over the whole batch (the oracle's definitions walk the
+    pairs in order); dispatch and combine are split by contiguous token
+    ranges over ``threads`` threads, each calling the unchanged
+    single-threaded oracle on its range (ctypes releases the GIL during the
+    C call).  Outputs go to arrays allocated once here, so the timed calls
+    do not include allocation."""
 
+    def __init__(self, w, idx_h, wt_h, x_h, y_h, threads):
+        import oracle as o
+        from concurrent.futures import ThreadPoolExecutor
+        self.o, self.w = o, w
+        self.idx, self.wt = idx_h.numpy(), wt_h.numpy()
+        self.x, self.y = W.bits(x_h), W.bits(y_h)
+        S = o.row_bytes(w.H, w.quant)
+        self.images = np.empty((w.T, w.k, S), np.uint8)
+        self.row_ids = np.empty((w.T, w.k), np.int64)
+        self.out = np.empty((w.T, w.H), np.uint16)
+        self.tokens = np.arange(w.T, dtype=np.int64)
+        cuts = np.linspace(0, w.T, max(1, threads) + 1).astype(np.int64)
+        self.parts = [(int(a), int(c)) for a, c in zip(cuts[:-1], cuts[1:]) if c > a]
+        self.threads = max(1, len(self.parts))
+        self.pool = ThreadPoolExecutor(self.threads)
+        self.L = self.N = None
 
-def _oracle_tokens_per_s(w, t_ln, t_dc, n):
-    """Full-batch tokens/s extrapolated from the sample: layout+notify ran on
-    all T tokens, dispatch+combine on n of them."""
-    return w.T / (t_ln + t_dc * w.T / n)
+    def close(self):
+        self.pool.shutdown()
+
+    def layout_notify(self):
+        w, o = self.w, self.o
+        t0 = time.perf_counter()
+        self.L = o.layout(self.idx, w.R, w.epr)
+        t1 = time.perf_counter()
+        self.N = o.notify(self.L["count"], w.R, w.bs, w.epr)
+        t2 = time.perf_counter()
+        assert self.L["status"] == 0 and self.N["status"] == 0
+        return t1 - t0, t2 - t1
+
+    def dispatch(self, toks, images, row_ids):
+        w, L, N = self.w, self.L, self.N
+        _, _, st = self.o.dispatch_tokens(
+            self.x, self.idx, L["send_idx"], N["put_offset"], N["rank_recv_base"],
+            w.R, w.epr, w.dtype, w.quant, toks, images=images, row_ids=row_ids)
+        return st
+
+    def combine(self, toks, out):
+        w, L, N = self.w, self.L, self.N
+        _, st = self.o.combine(self.y, self.idx, self.wt, L["send_idx"],
+                               N["put_offset"], N["rank_recv_base"], w.R, w.epr,
+                               w.dtype, tokens=toks, out=out)
+        return st
+
+    def _over_parts(self, fn):
+        futs = [self.pool.submit(fn, a, c) for a, c in self.parts]
+        sts = [f.result() for f in futs]
+        assert all(st == 0 for st in sts), sts
+
+    def step(self):
+        """One whole step on all tokens; seconds per stage."""
+        t_lay, t_not = self.layout_notify()
+        t0 = time.perf_counter()
+        self._over_parts(lambda a, c: self.dispatch(self.tokens[a:c], self.images[a:c],
+                                                    self.row_ids[a:c]))
+        t1 = time.perf_counter()
+        self._over_parts(lambda a, c: self.combine(self.tokens[a:c], self.out[a:c]))
+        t2 = time.perf_counter()
+        return {"layout": t_lay, "notify": t_not, "dispatch": t1 - t0,
+                "combine": t2 - t1}
+
+    def one_thread(self, toks):
+        """Dispatch and combine of the listed tokens on this thread alone;
+        returns (seconds per stage, images, row_ids, out)."""
+        images = np.empty((toks.size,) + self.images.shape[1:], np.uint8)
+        row_ids = np.empty((toks.size, self.w.k), np.int64)
+        out = np.empty((toks.size, self.w.H), np.uint16)
+        t0 = time.perf_counter()
+        assert self.dispatch(toks, images, row_ids) == 0
+        t1 = time.perf_counter()
+        assert self.combine(toks, out) == 0
+        t2 = time.perf_counter()
+        return {"dispatch": t1 - t0, "combine": t2 - t1}, images, row_ids, out
 
 
 def host_cpu():
@@ -735,52 +879,87 @@ def host_cpu():
     return model, avail
 
 
-def cpu_baseline(w, idx_h, wt_h, x_h, y_h, seconds):
-    import oracle as o
-    idx_np, wt_np = idx_h.numpy(), wt_h.numpy()
-    x_bits, y_bits = W.bits(x_h), W.bits(y_h)
-    rng = np.random.default_rng(0)
-    probe = np.sort(rng.choice(w.T, size=min(w.T, 64), replace=False))
-    t_ln, t_dc = _oracle_step(o, w, idx_np, wt_np, x_bits, y_bits, probe)
-    per_tok = t_dc / len(probe)
-    n = int(min(w.T, max(64, (seconds - t_ln) / max(per_tok, 1e-9))))
-    tokens = np.sort(rng.choice(w.T, size=n, replace=False))
-    t_ln, t_dc = _oracle_step(o, w, idx_np, wt_np, x_bits, y_bits, tokens)
-    model, avail = host_cpu()
-    return {"value": _oracle_tokens_per_s(w, t_ln, t_dc, n), "unit": "tokens/s",
-            "cores": 1, "kind": "oracle", "cpu": model, "host_cores_available": avail,
-            "sample": "layout+notify on all %d tokens (%.2f ms), dispatch+combine on %s "
-                      "(%.2f s)%s"
-                      % (w.T, t_ln * 1e3,
-                         "all %d tokens" % n if n == w.T else "%d random tokens" % n, t_dc,
-                         "" if n == w.T else ", scaled to the full batch")}
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, idx_h, wt_h, x_h, y_h, seconds, threads=None):
+    """The oracle timed on the host: a whole step on every host core (layout
+    and notify on one thread, dispatch and combine split by token ranges),
+    and dispatch + combine on one thread over a random token sample that
+    takes about ``seconds``, scaled to the batch.  The sample's outputs must
+    equal the all-core run's for the same tokens byte for byte."""
+    threads = threads or host_threads()
+    oh = OracleHost(w, idx_h, wt_h, x_h, y_h, threads)
+    try:
+        oh.step()                                  # first touch of the outputs
+        runs = [oh.step() for _ in range(2)]
+        stages = {k: float(np.median([r[k] for r in runs])) for k in runs[0]}
+        all_s = sum(stages.values())
+        rng = np.random.default_rng(0)
+        probe = np.sort(rng.choice(w.T, size=min(w.T, 16), replace=False))
+        t1, _, _, _ = oh.one_thread(probe)
+        per_tok = (t1["dispatch"] + t1["combine"]) / probe.size
+        n = int(min(w.T, max(16, seconds / max(per_tok, 1e-9))))
+        sample = np.sort(rng.choice(w.T, size=n, replace=False))
+        t1, images, row_ids, out = oh.one_thread(sample)
+        identical = (np.array_equal(images, oh.images[sample])
+                     and np.array_equal(row_ids, oh.row_ids[sample])
+                     and np.array_equal(out, oh.out[sample]))
+        if not identical:
+            raise RuntimeError("%s: the all-core oracle differs from the one-thread "
+                               "oracle on the sample" % w.name)
+        one_s = (stages["layout"] + stages["notify"]
+                 + (t1["dispatch"] + t1["combine"]) * w.T / n)
+        model, avail = host_cpu()
+        return {
+            "value": w.T / all_s, "unit": "tokens/s", "cores": oh.threads,
+            "kind": "oracle", "cpu": model, "host_cores_available": avail,
+            "stages_ms": {k: v * 1e3 for k, v in stages.items()},
+            "sample": "whole batch of %d tokens per step (median of 2 steps after "
+                      "one untimed): layout+notify on 1 thread, dispatch+combine "
+                      "split by token ranges over %d threads" % (w.T, oh.threads),
+            "one_core": {
+                "value": w.T / one_s, "cores": 1,
+                "stages_ms": {"dispatch": t1["dispatch"] * 1e3 * w.T / n,
+                              "combine": t1["combine"] * 1e3 * w.T / n},
+                "sample": "dispatch+combine of %s on one thread (%.2f s), scaled "
+                          "to the batch; layout+notify as above"
+                          % ("all %d tokens" % n if n == w.T else "%d random tokens" % n,
+                             t1["dispatch"] + t1["combine"])},
+            "identical_to_one_thread": identical,
+        }
+    finally:
+        oh.close()
 
 
 def run_reference(args, w):
+    """The reference arm: the CPU oracle, as it stands, on the host cores.
+    Each step is the whole pipeline on the whole batch (see OracleHost)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return None                       # rank 0 alone runs the oracle
-    import oracle as o
     idx_h, wt_h = W.routing(w)
     x_h = W.tokens(w)
     y_h = W.expert_outputs(w)
-    idx_np, wt_np = idx_h.numpy(), wt_h.numpy()
-    x_bits, y_bits = W.bits(x_h), W.bits(y_h)
-    rng = np.random.default_rng(1)
-    n = min(w.T, args.ref_tokens)
-    samples = [np.sort(rng.choice(w.T, size=n, replace=False))
-               for _ in range(args.warmup + args.steps)]
-    for i in range(args.warmup):
-        _oracle_step(o, w, idx_np, wt_np, x_bits, y_bits, samples[i])
-    secs = []
-    t0 = time.perf_counter()
-    for i in range(args.steps):
-        t_ln, t_dc = _oracle_step(o, w, idx_np, wt_np, x_bits, y_bits,
-                                  samples[args.warmup + i])
-        secs.append(t_ln + t_dc * w.T / n)
-    wall = time.perf_counter() - t0
-    step_s = float(np.mean(secs))
+    oh = OracleHost(w, idx_h, wt_h, x_h, y_h, host_threads())
+    try:
+        for i in range(args.warmup):
+            oh.step()
+        runs = []
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            runs.append(oh.step())
+        wall = time.perf_counter() - t0
+    finally:
+        oh.close()
+    step_s = wall / args.steps
     value = w.T / step_s
+    model, avail = host_cpu()
+    stages = {k: float(np.mean([r[k] for r in runs])) * 1e3 for k in runs[0]}
     return {
         "impl": "reference",
         "metric": "dispatch+combine tokens/s",
@@ -797,12 +976,14 @@ def run_reference(args, w):
         "data": "synthetic",
         "config": {"workload": workload_desc(w),
                    "step": "layout+notify+dispatch+combine (CPU oracle)"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1,
-                         "kind": "oracle", "cpu": host_cpu()[0],
-                         "host_cores_available": host_cpu()[1],
-                         "sample": "each step: layout+notify on all %d tokens, "
-                                   "dispatch+combine on %d random tokens, "
-                                   "scaled to the full batch" % (w.T, n)},
+        "stages_ms": stages,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oh.threads,
+                         "kind": "oracle", "cpu": model,
+                         "host_cores_available": avail,
+                         "sample": "every step: the whole batch of %d tokens; "
+                                   "layout+notify on 1 thread, dispatch+combine "
+                                   "split by token ranges over %d threads"
+                                   % (w.T, oh.threads)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -821,15 +1002,19 @@ def parse_args(argv=None):
     p.add_argument("--clocks-csv", default=None,
                    help="where the nvidia-smi clock samples of the timed steps go "
                         "(default: a file in /tmp)")
-    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--cpu-seconds", type=float, default=2.0,
+                   help="one-thread oracle sample per workload (seconds)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="time the named workload only")
+    p.add_argument("--per-config-steps", type=int, default=20,
+                   help="timed steps of each non-headline workload")
     p.add_argument("--no-deep-moe", action="store_true",
                    help="skip the fused deep MoE section")
     p.add_argument("--gemm", default=None, metavar="G,ROWS,N,K",
                    help="time the grouped GEMM alone and exit")
     p.add_argument("--gemm-epilogue", default="int32", choices=["int32", "dequant", "swiglu"],
                    help="epilogue of the --gemm benchmark")
-    p.add_argument("--ref-tokens", type=int, default=32)
     p.add_argument("--bs", type=int, default=None,
                    help="override tokens per rank (small profiling cases)")
     p.add_argument("--hidden", type=int, default=None,

@@ -62,8 +62,8 @@ def lib():
                                             _i64p, _i64p, i64, _u16p]
         L.oracle_token_layout.argtypes = [i, i, i, i, _i32p, _i32p, _u8p]
         L.oracle_exp_f32.argtypes = [_f32p, _f32p, i64]
-        L.oracle_swiglu_quant_rows.argtypes = [i64, i, _i32p, _f32p, _f32p, _i64p,
-                                               i64, _u8p]
+        for name in ("oracle_swiglu_quant_rows", "oracle_swiglu_quant_rows_libm"):
+            getattr(L, name).argtypes = [i64, i, _i32p, _f32p, _f32p, _i64p, i64, _u8p]
         L.oracle_combine_quant_tokens.argtypes = [i, i, i, i, i, i, _u8p, i64,
                                                   _i32p, _f32p, _i32p, _i32p,
                                                   _i64p, _i64p, i64, _u16p]
@@ -213,9 +213,11 @@ def dispatch(x_bits, topk_idx, send_idx, put_offset, rank_recv_base, R, epr,
 
 
 def dispatch_tokens(x_bits, topk_idx, send_idx, put_offset, rank_recv_base,
-                    R, epr, dtype, quant, tokens):
+                    R, epr, dtype, quant, tokens, images=None, row_ids=None):
     """Stage 3 for the listed tokens only.  Returns (images uint8
-    [n, k, S], row_ids int64 [n, k], status)."""
+    [n, k, S], row_ids int64 [n, k], status).  ``images`` / ``row_ids``:
+    optional caller-provided C-contiguous output arrays of those shapes
+    (every byte is written)."""
     x = _c(x_bits, np.uint16)
     idx = _c(topk_idx, np.int32)
     T, H = x.shape
@@ -223,8 +225,12 @@ def dispatch_tokens(x_bits, topk_idx, send_idx, put_offset, rank_recv_base,
     bs = T // R
     toks = _c(tokens, np.int64)
     S = row_bytes(H, quant)
-    images = np.zeros((toks.size, k, S), np.uint8)
-    row_ids = np.zeros((toks.size, k), np.int64)
+    if images is None:
+        images = np.zeros((toks.size, k, S), np.uint8)
+    if row_ids is None:
+        row_ids = np.zeros((toks.size, k), np.int64)
+    assert images.shape == (toks.size, k, S) and images.dtype == np.uint8
+    assert row_ids.shape == (toks.size, k) and row_ids.dtype == np.int64
     st = lib().oracle_dispatch_tokens(
         R, bs, k, epr, H, dtype, int(bool(quant)), _p(x, _u16p),
         _p(idx, _i32p), _p(_c(send_idx, np.int32), _i32p),
@@ -235,9 +241,10 @@ def dispatch_tokens(x_bits, topk_idx, send_idx, put_offset, rank_recv_base,
 
 
 def combine(y_bits, topk_idx, topk_weights, send_idx, put_offset,
-            rank_recv_base, R, epr, dtype, tokens=None):
+            rank_recv_base, R, epr, dtype, tokens=None, out=None):
     """Stage 4.  y uint16 [rows, H]; returns (out uint16 [n, H], status),
-    n = T when ``tokens`` is None, else len(tokens)."""
+    n = T when ``tokens`` is None, else len(tokens).  ``out``: optional
+    caller-provided C-contiguous uint16 [n, H] output array."""
     y = _c(y_bits, np.uint16)
     idx = _c(topk_idx, np.int32)
     w = _c(topk_weights, np.float32)
@@ -250,7 +257,9 @@ def combine(y_bits, topk_idx, topk_weights, send_idx, put_offset,
     else:
         toks = _c(tokens, np.int64)
         n = toks.size
-    out = np.zeros((n, H), np.uint16)
+    if out is None:
+        out = np.zeros((n, H), np.uint16)
+    assert out.shape == (n, H) and out.dtype == np.uint16
     st = lib().oracle_combine_tokens(
         R, bs, k, epr, H, dtype, _p(y, _u16p), y.shape[0], _p(idx, _i32p),
         _p(w, _f32p), _p(_c(send_idx, np.int32), _i32p),
@@ -307,9 +316,12 @@ def exp_f32(x):
     return out
 
 
-def swiglu_quant(acc, weight_scale, token_scale, rows=None):
+def swiglu_quant(acc, weight_scale, token_scale, rows=None, exp="cw"):
     """GMM1 epilogue: acc int32 [M, 2I] -> INT8 row images uint8
-    [n, align32(I) + 32] (n = M, or len(rows))."""
+    [n, align32(I) + 32] (n = M, or len(rows)).  exp="cw": Exp is the
+    oracle's fp32 evaluation (exp_f32); exp="libm": Exp is the float
+    nearest to e^x (libm's double exp rounded once)."""
+    fn = {"cw": "oracle_swiglu_quant_rows", "libm": "oracle_swiglu_quant_rows_libm"}[exp]
     acc = _c(acc, np.int32)
     M, N = acc.shape
     I = N // 2
@@ -322,9 +334,8 @@ def swiglu_quant(acc, weight_scale, token_scale, rows=None):
         rr = _c(rows, np.int64)
         n = rr.size
     out = np.zeros((n, row_bytes(I, 1)), np.uint8)
-    lib().oracle_swiglu_quant_rows(M, I, _p(acc, _i32p), _p(ws, _f32p), _p(ts, _f32p),
-                                   None if rr is None else _p(rr, _i64p), n,
-                                   _p(out, _u8p))
+    getattr(lib(), fn)(M, I, _p(acc, _i32p), _p(ws, _f32p), _p(ts, _f32p),
+                       None if rr is None else _p(rr, _i64p), n, _p(out, _u8p))
     return out
 
 

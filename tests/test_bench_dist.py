@@ -88,17 +88,53 @@ def test_reference_arm_under_torchrun_two_ranks():
 
 def test_cpu_baseline_leg_on_the_host():
     """The cpu_baseline object the GPU arm adds: the oracle timed on the host
-    over a bounded sample (here the whole tiny batch fits), with the keys the
-    JSON line needs."""
+    cores over the whole batch (dispatch and combine split over threads),
+    with the one-thread figure beside it and the keys the JSON line needs."""
     sys.path.insert(0, ROOT)
     import bench
     import workloads as W
     w = W.WORKLOADS["tiny"]
     idx, wt = W.routing(w)
-    cb = bench.cpu_baseline(w, idx, wt, W.tokens(w), W.expert_outputs(w), 0.5)
-    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["unit"] == "tokens/s"
+    cb = bench.cpu_baseline(w, idx, wt, W.tokens(w), W.expert_outputs(w), 0.5,
+                            threads=3)
+    assert cb["kind"] == "oracle" and cb["cores"] == 3 and cb["unit"] == "tokens/s"
     assert cb["value"] > 0 and cb["host_cores_available"] >= 1
-    assert "all %d tokens" % w.T in cb["sample"]
+    assert cb["identical_to_one_thread"] is True
+    assert cb["one_core"]["cores"] == 1 and cb["one_core"]["value"] > 0
+    assert "all %d tokens" % w.T in cb["one_core"]["sample"]
+    assert set(cb["stages_ms"]) == {"layout", "notify", "dispatch", "combine"}
+
+
+@pytest.mark.parametrize("threads", [1, 4, 7])
+def test_threaded_oracle_equals_the_whole_batch_oracle(threads):
+    """The all-core timing runs the oracle's dispatch and combine over token
+    ranges on several threads; the assembled outputs must be byte-identical
+    to one call over the whole batch (a ragged split: T not a multiple of
+    the thread count)."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import bench
+    import oracle
+    import workloads as W
+    w = W.Workload("small", R=3, epr=5, bs=37, H=96, k=4, seed=77)
+    idx, wt = W.routing(w)
+    x, y = W.tokens(w), W.expert_outputs(w)
+    oh = bench.OracleHost(w, idx, wt, x, y, threads)
+    try:
+        oh.step()
+    finally:
+        oh.close()
+    L = oracle.layout(idx.numpy(), w.R, w.epr)
+    N = oracle.notify(L["count"], w.R, w.bs, w.epr)
+    images, rows, st = oracle.dispatch_tokens(
+        W.bits(x), idx.numpy(), L["send_idx"], N["put_offset"], N["rank_recv_base"],
+        w.R, w.epr, w.dtype, w.quant, np.arange(w.T))
+    out, st2 = oracle.combine(W.bits(y), idx.numpy(), wt.numpy(), L["send_idx"],
+                              N["put_offset"], N["rank_recv_base"], w.R, w.epr, w.dtype)
+    assert st == 0 and st2 == 0
+    assert np.array_equal(images, oh.images)
+    assert np.array_equal(rows, oh.row_ids)
+    assert np.array_equal(out, oh.out)
 
 
 @pytest.mark.parametrize("name,dispatch_gb,combine_gb", [

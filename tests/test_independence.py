@@ -34,7 +34,8 @@ def _imports(path):
     def walk(node, func):
         for child in ast.iter_child_nodes(node):
             f = func
-            if func is None and isinstance(child, (ast.FunctionDef, ast.AsyncFunctionDef)):
+            if func is None and isinstance(child, (ast.FunctionDef, ast.AsyncFunctionDef,
+                                                   ast.ClassDef)):
                 f = child.name
             if isinstance(child, ast.Import):
                 out.extend((a.name, f) for a in child.names)
@@ -91,8 +92,16 @@ def test_input_generators_import_neither_side():
 
 
 def test_bench_reaches_the_oracle_only_in_its_cpu_legs():
-    users = {f for mod, f in _imports(os.path.join(ROOT, "bench.py")) if _top(mod) == "oracle"}
-    assert users and users <= {"cpu_baseline", "run_reference"}, users
+    path = os.path.join(ROOT, "bench.py")
+    users = {f for mod, f in _imports(path) if _top(mod) == "oracle"}
+    assert users and users <= {"cpu_baseline", "run_reference", "OracleHost"}, users
+    # and the class that runs the oracle is used only by those two legs
+    tree = ast.parse(open(path).read(), filename=path)
+    for top in tree.body:
+        if isinstance(top, (ast.FunctionDef, ast.ClassDef)) and top.name not in (
+                "cpu_baseline", "run_reference", "OracleHost"):
+            names = {n.id for n in ast.walk(top) if isinstance(n, ast.Name)}
+            assert "OracleHost" not in names, top.name
 
 
 def test_entry_reaches_the_oracle_only_in_build_and_smoke():

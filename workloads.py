@@ -154,6 +154,24 @@ def expert_outputs(w: Workload, rows: Optional[int] = None) -> torch.Tensor:
     return _rows(n, w.H, w.dtype, "normal", 1.0, _gen(w.seed, _S_Y))
 
 
+def expert_outputs_device(w: Workload, device, rows: Optional[int] = None,
+                          chunk_elems: int = 1 << 28) -> torch.Tensor:
+    """Expert outputs y [rows, H] ~ N(0,1) in the token dtype, drawn on
+    ``device`` with that device's generator (seeded like the host stream;
+    the values differ from expert_outputs', the distribution does not).
+    For benchmarks, where drawing billions of host normals would dominate
+    start-up."""
+    n = w.P if rows is None else rows
+    g = torch.Generator(device=device)
+    g.manual_seed(w.seed * 16 + _S_Y)
+    out = torch.empty((n, w.H), dtype=_TORCH_DTYPE[w.dtype], device=device)
+    rows_per_chunk = max(1, chunk_elems // max(w.H, 1))
+    for r0 in range(0, n, rows_per_chunk):
+        r1 = min(n, r0 + rows_per_chunk)
+        out[r0:r1] = torch.randn((r1 - r0, w.H), generator=g, device=device).to(out.dtype)
+    return out
+
+
 def expert_outputs_int8(w: Workload, rows: Optional[int] = None) -> torch.Tensor:
     """Synthetic INT8 expert outputs: rows laid out like a dispatched INT8
     row (H int8 codes, zeros to align32(H), fp32 1/scale, zeros to
