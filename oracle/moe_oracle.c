@@ -453,10 +453,15 @@ void oracle_exp_f32(const float* in, float* out, int64_t n) {
 
 /* ---- GMM1 epilogue: dequant, SwiGLU, requant (sections 4.8.1, 8.7) ------- */
 
-void oracle_swiglu_quant_rows(int64_t M, int I, const int32_t* acc,
-                              const float* weight_scale,
-                              const float* token_scale, const int64_t* rows,
-                              int64_t nrows, uint8_t* out) {
+/* The plain definition of Exp: the float nearest to e^x, through libm's
+ * double exp (accurate far beyond fp32; the one rounding to float can round
+ * twice only when e^x lies within 2^-29 ulp of a tie). */
+static float exp_libm(float x) { return (float)exp((double)x); }
+
+static void swiglu_quant_rows_with(float (*exp_fn)(float), int64_t M, int I,
+                                   const int32_t* acc, const float* weight_scale,
+                                   const float* token_scale, const int64_t* rows,
+                                   int64_t nrows, uint8_t* out) {
   const int64_t S = oracle_row_bytes(I, 1);
   const int64_t i_align = (int64_t)((I + 31) / 32) * 32;
   float* h = (float*)malloc(sizeof(float) * (size_t)(I > 0 ? I : 1));
@@ -476,7 +481,7 @@ void oracle_swiglu_quant_rows(int64_t M, int I, const int32_t* acc,
       up = up * weight_scale[I + j];
       up = up * ts;
       /* 4. SwiGLU: Muls(-1), Exp, Adds(1), Div on the left half */
-      const float e = exp_cw(-gate);
+      const float e = exp_fn(-gate);
       const float d = e + 1.0f;
       const float sg = gate / d;
       h[j] = sg * up;
@@ -495,6 +500,20 @@ void oracle_swiglu_quant_rows(int64_t M, int I, const int32_t* acc,
     memcpy(img + i_align, &inv, 4);
   }
   free(h);
+}
+
+void oracle_swiglu_quant_rows(int64_t M, int I, const int32_t* acc,
+                              const float* weight_scale,
+                              const float* token_scale, const int64_t* rows,
+                              int64_t nrows, uint8_t* out) {
+  swiglu_quant_rows_with(exp_cw, M, I, acc, weight_scale, token_scale, rows, nrows, out);
+}
+
+void oracle_swiglu_quant_rows_libm(int64_t M, int I, const int32_t* acc,
+                                   const float* weight_scale,
+                                   const float* token_scale, const int64_t* rows,
+                                   int64_t nrows, uint8_t* out) {
+  swiglu_quant_rows_with(exp_libm, M, I, acc, weight_scale, token_scale, rows, nrows, out);
 }
 
 /* ---- fused deep MoE: grouped INT8 GEMM (sections 4.1, 4.3: GMM1 / GMM2,

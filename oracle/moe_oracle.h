@@ -139,6 +139,15 @@ void oracle_swiglu_quant_rows(int64_t M, int I, const int32_t* acc,
                               const float* token_scale, const int64_t* rows,
                               int64_t nrows, uint8_t* out);
 
+/* The same epilogue with Exp taken as the float nearest to e^x (libm's
+ * double exp, rounded once to float) instead of oracle_exp_f32: the page
+ * names the operation, not an algorithm for it, so this is the plainest
+ * reading, written independently of any fast evaluation. */
+void oracle_swiglu_quant_rows_libm(int64_t M, int I, const int32_t* acc,
+                                   const float* weight_scale,
+                                   const float* token_scale, const int64_t* rows,
+                                   int64_t nrows, uint8_t* out);
+
 /* Combine over INT8 expert outputs (the dequantisation the pipeline diagram
  * of section 2.1 adds to stage 4).  yq holds y_rows rows of oracle_row_bytes(H, 1) bytes laid
  * out like a dispatched INT8 row (H codes, fp32 1/scale at align32(H)).

@@ -272,6 +272,49 @@ def test_deep_moe_pipeline(oracle_mod, ep, pl, w):
         ref["out"])
 
 
+@pytest.mark.parametrize("w", DEEP_CASES, ids=lambda w: w.name)
+def test_deep_moe_swiglu_vs_plain_exp(oracle_mod, pl, w):
+    """Both GMM1 epilogue routes (SwiGLU in the GEMM's epilogue + the
+    requantisation pass, and the int32 GEMM + the grouped epilogue kernel)
+    against the oracle whose Exp is the float nearest to e^x, within the
+    bound that one exp ulp allows."""
+    from conftest import assert_near_plain_exp
+    I = 136 if w.H > 512 else 128
+    idx, wt, x, (w1, ws1, w2, ws2) = _deep_inputs(w, I, w.seed)
+    ref = oracle_mod.deep_moe(W.bits(x), idx.numpy(), wt.numpy(), w.R, w.epr, w.dtype,
+                              w1.numpy(), ws1.numpy(), w2.numpy(), ws2.numpy())
+    ts1 = oracle_mod.row_inv_scale(
+        oracle_mod.dispatch(W.bits(x), idx.numpy(), *_layout_notify_args(oracle_mod, idx, w),
+                            w.R, w.epr, w.dtype, True)[0], w.H)
+    grp = np.searchsorted(ref["group_off"], ref["rows"], side="right") - 1
+    x2 = np.zeros_like(ref["x2"])
+    for e in np.unique(grp):
+        sel = np.nonzero(grp == e)[0]
+        x2[sel] = oracle_mod.swiglu_quant(ref["acc1"][sel], ws1.numpy()[e], ts1[sel],
+                                          exp="libm")
+    dev = torch.device("cuda")
+    b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype)
+    wts = pl.DeepMoeWeights(w1.to(dev), ws1.to(dev), w2.to(dev), ws2.to(dev))
+    idx_d, x_d = idx.to(dev), x.to(dev)
+    pl.run_layout_notify(b, idx_d)
+    pl.run_dispatch_expand(b, x_d, idx_d)
+    for fused in (True, False):
+        b.a2.zero_()
+        b.ts2.zero_()
+        pl.run_deep_moe_experts(b, wts, fused_swiglu=fused)
+        assert b.status() == 0
+        n = ref["rows"].size
+        codes = b.a2[:n].float().cpu().numpy().astype(np.int64)
+        assert_near_plain_exp("a2 (%s)" % ("fused" if fused else "kernel"), codes,
+                              b.ts2[:n].cpu().numpy(), x2, I)
+
+
+def _layout_notify_args(oracle_mod, idx, w):
+    L = oracle_mod.layout(idx.numpy(), w.R, w.epr)
+    N = oracle_mod.notify(L["count"], w.R, w.bs, w.epr)
+    return L["send_idx"], N["put_offset"], N["rank_recv_base"]
+
+
 def test_deep_moe_dsv3_size_sampled(oracle_mod, pl):
     """DeepSeek-V3 shape (R = 8, E = 256, bs = 4096, k = 8, H = 7168,
     I = 2048), weights drawn on the device; sampled tokens are checked

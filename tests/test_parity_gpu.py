@@ -508,6 +508,36 @@ def test_swiglu_quant_dsv3_size(oracle_mod, ep):
     _check_swiglu(oracle_mod, ep, 262144, 2048, sample=1500)
 
 
+@pytest.mark.parametrize("M,I,sample", [(3000, 2048, None), (500, 40, None),
+                                        (257, 16384, None), (777, 4096, None),
+                                        (300, 4104, None), (262144, 2048, 3000)])
+def test_swiglu_quant_vs_plain_exp(oracle_mod, ep, M, I, sample):
+    """The same kernel against the oracle whose Exp is the float nearest to
+    e^x (not the oracle's own fp32 evaluation), within the bound that one
+    exp ulp allows."""
+    from conftest import assert_near_plain_exp
+    acc, ws, ts = W.gmm1_accumulators(M, I, seed=M + I)
+    rb = (I + 31) // 32 * 32 + 32
+    out = torch.full((M, rb), 0xAB, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.moe_swiglu_quant(acc.cuda(), ws.cuda(), ts.cuda(), out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rows = None
+    if sample is not None:
+        rng = np.random.default_rng(6)
+        rows = np.unique(np.concatenate([[0, M - 1], rng.integers(0, M, sample)]))
+    ref = oracle_mod.swiglu_quant(acc.numpy(), ws.numpy(), ts.numpy(), rows=rows,
+                                  exp="libm")
+    got = (out if rows is None else out[torch.from_numpy(rows).cuda()]).cpu().numpy()
+    ia = (I + 31) // 32 * 32
+    assert_near_plain_exp("swiglu", got[:, :I].view(np.int8),
+                          got[:, ia:ia + 4].copy().view(np.float32)[:, 0], ref, I)
+    # everything but the codes and 1/scale is exact: the zero pads
+    _eq("pads", got[:, I:ia], ref[:, I:ia])
+    _eq("tail", got[:, ia + 4:], ref[:, ia + 4:])
+
+
 # ---------------------------------------------------------------------------
 # CUDA graph capture and replay of the four calls
 # ---------------------------------------------------------------------------
