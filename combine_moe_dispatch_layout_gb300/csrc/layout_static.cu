@@ -2,43 +2,19 @@
 // its scratch memory in a fixed, library-owned device array instead of a
 // caller-provided workspace, for callers that cannot allocate device memory.
 //
-// The scratch is one file-scope __device__ array of MOE_EP_STATIC_LAYOUT_WS_BYTES
-// bytes; every GPU that loads the library holds it until the process exits.
-// Host code never uses the array's name as an address: on the first call on
-// each device (with that device current) cudaGetSymbolAddress gives the
-// device address, which is cached per device and passed to the kernel.
-#include <mutex>
-
+// The scratch is one file-scope static __device__ array of
+// MOE_EP_STATIC_LAYOUT_WS_BYTES bytes; every GPU that loads the library holds
+// it until the process exits.  Host code never uses the array's name as an
+// address: every call, with the stream's device current, asks
+// cudaGetSymbolAddress for the array's device address on that device and
+// passes it to the kernel.  The first call on a device is the set-up: that
+// lookup also loads the library's module onto the device.  Later lookups
+// are cheap, and not caching the address keeps a call made after
+// cudaDeviceReset (which unloads the module and frees the array) from
+// writing through a stale pointer.
 #include "moe_ep_internal.cuh"
 
-namespace {
-
-constexpr int kMaxDevices = 64;
-
-__device__ __align__(256) unsigned char g_layout_scratch[MOE_EP_STATIC_LAYOUT_WS_BYTES];
-
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_layout_scratch on the current device (set-up on the
-// first call per device).
-cudaError_t scratch_on_current_device(void** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_layout_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
-  return cudaSuccess;
-}
-
-}  // namespace
+static __device__ __align__(256) unsigned char g_layout_scratch[MOE_EP_STATIC_LAYOUT_WS_BYTES];
 
 extern "C" moe_status moe_dispatch_layout_static(
     const moe_shape* shape, const int32_t* topk_idx, int32_t* count,
@@ -58,9 +34,14 @@ extern "C" moe_status moe_dispatch_layout_static(
     return moe_dispatch_layout(shape, topk_idx, count, rank_send, send_idx,
                                nullptr, dev_status, stream);
   void* scratch = nullptr;
-  if (scratch_on_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
-  // The array keeps whatever the previous call left in it; the part this
-  // call uses is cleared first, on the caller's stream, so it starts at zero.
+  if (cudaGetSymbolAddress(&scratch, g_layout_scratch) != cudaSuccess || scratch == nullptr)
+    return MOE_ERR_CUDA;
+  // Ordinary calls would not need this clear: the layout kernel's per-launch
+  // epoch leaves the workspace ready for the next launch of any shape, and
+  // the array starts zero-filled.  It is here so that a call that follows
+  // one that stopped early (a wait that timed out) or that overlapped
+  // another call on the GPU starts from a clean workspace all the same.
+  // Keep it.
   if (cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return moe_dispatch_layout(shape, topk_idx, count, rank_send, send_idx,

@@ -4,15 +4,18 @@ It exists for callers that cannot allocate device memory (a plugin handed
 only its input and output buffers, or a serving loop whose memory is all
 reserved up front).  These tests call it through the C ABI and compare its
 outputs with the regular entry point's (which takes a caller-allocated
-workspace) bit for bit, on two calls in a row with different routings, so
-that the second call cannot pass on what the first left in the shared
-scratch array.  The file is named to be collected last.
+workspace) and with the CPU oracle's layout, bit for bit, on two calls in a
+row with different routings, so that the second call cannot pass on what
+the first left in the shared scratch array.  The file is named to be
+collected last.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -30,10 +33,10 @@ def lib():
     return ep, L
 
 
-def _run_both(ep, L, w, seed):
+def _run_both(ep, L, w, seed, stream=None):
     w = w.with_(seed=seed)
-    idx, _ = W.routing(w)
-    idx = idx.cuda()
+    idx_h, _ = W.routing(w)
+    idx = idx_h.cuda()
     shape = ep.make_shape(w.R, w.bs, w.k, w.epr, w.H)
     E, T = w.E, w.T
 
@@ -50,12 +53,13 @@ def _run_both(ep, L, w, seed):
     ep.moe_dispatch_layout(shape, idx, c1, r1, s1, ws, st1)
     # the allocation-free entry point, through the C ABI
     c2, r2, s2, st2 = outs()
-    stream = torch.cuda.current_stream().cuda_stream
+    st = torch.cuda.current_stream() if stream is None else stream
+    st.wait_stream(torch.cuda.current_stream())
     rc = L.moe_dispatch_layout_static(
         ctypes.byref(shape), ctypes.c_void_p(idx.data_ptr()),
         ctypes.c_void_p(c2.data_ptr()), ctypes.c_void_p(r2.data_ptr()),
         ctypes.c_void_p(s2.data_ptr()), ctypes.c_void_p(st2.data_ptr()),
-        ctypes.c_void_p(stream))
+        ctypes.c_void_p(st.cuda_stream))
     torch.cuda.synchronize()
     assert rc == 0, ep.status_string(rc)
     assert int(st1.item()) == 0 and int(st2.item()) == 0
@@ -63,6 +67,12 @@ def _run_both(ep, L, w, seed):
     assert torch.equal(c1, c2)
     assert torch.equal(r1, r2)
     assert torch.equal(s1, s2)
+    # and the oracle's layout of the same routing
+    ref = oracle.layout(idx_h.numpy(), w.R, w.epr)
+    assert ref["status"] == 0
+    np.testing.assert_array_equal(c2.cpu().numpy(), ref["count"])
+    np.testing.assert_array_equal(r2.cpu().numpy(), ref["rank_send"])
+    np.testing.assert_array_equal(s2.cpu().numpy(), ref["send_idx"])
 
 
 @pytest.mark.parametrize("w", [
@@ -74,6 +84,15 @@ def test_static_matches_workspace_entry_two_calls(lib, w):
     ep, L = lib
     _run_both(ep, L, w, seed=101)
     _run_both(ep, L, w, seed=202)
+
+
+def test_static_on_a_side_stream(lib):
+    """Two calls in a row on a stream other than torch's current one."""
+    ep, L = lib
+    side = torch.cuda.Stream()
+    w = W.Workload("ragged", R=5, epr=3, bs=700, k=4, H=64)
+    _run_both(ep, L, w, seed=303, stream=side)
+    _run_both(ep, L, w, seed=404, stream=side)
 
 
 def test_static_rejects_shapes_beyond_the_array(lib):
