@@ -326,6 +326,32 @@ moe_status moe_grouped_gemm_i8(const void* a, int64_t a_rows, int32_t K, const v
                                                static_cast<cudaStream_t>(stream)));
 }
 
+// Test hook, deliberately not declared in moe_ep.h: moe_grouped_gemm_i8 with
+// the pipeline's main-loop waits limited to `main_loop_polls` polls (0 makes
+// the first wait of every working CTA give up), so that a test can drive the
+// kernel's timeout path -- MOE_ERR_TIMEOUT in *dev_status, no further work
+// issued, every copy, MMA, commit and store already in flight drained under
+// the full bound before TMEM is released -- without a fault or a hang.
+extern "C" moe_status moe_test_grouped_gemm_i8_polls(const void* a, int64_t a_rows, int32_t K,
+                                                     const void* w, int32_t G, int32_t N,
+                                                     const int32_t* group_rows, int32_t* c,
+                                                     uint32_t main_loop_polls,
+                                                     int32_t* dev_status, void* stream) {
+  const int64_t bn = moe_ep::gmm_block_n();
+  if (a_rows < 1 || a_rows > INT32_MAX || K < 8 || K > MOE_EP_MAX_HIDDEN || K % 8 != 0 ||
+      G < 1 || G > MOE_EP_MAX_EXPERTS || N < 8 || N > MOE_EP_MAX_HIDDEN || N % 8 != 0 ||
+      !dev_status || !a || !w || !group_rows || !c)
+    return MOE_ERR_INVALID_ARG;
+  if ((a_rows / 128 + G) * ((N + bn - 1) / bn) > INT32_MAX) return MOE_ERR_INVALID_ARG;
+  if (!aligned(a, 16) || !aligned(w, 16) || !aligned(group_rows, 4) || !aligned(c, 16) ||
+      !aligned(dev_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(moe_ep::launch_grouped_gemm(a, a_rows, K, w, G, N, group_rows, c, 0,
+                                               nullptr, nullptr, 0, dev_status,
+                                               static_cast<cudaStream_t>(stream),
+                                               main_loop_polls));
+}
+
 moe_status moe_grouped_gemm_i8_dequant(const void* a, int64_t a_rows, int32_t K,
                                        const void* w, int32_t G, int32_t N,
                                        const int32_t* group_rows, const float* col_scale,

@@ -27,8 +27,12 @@
 // per thread, and one half of the columns) into int32 registers while the
 // next chunk accumulates, then store the tile's rows.  Every mbarrier wait is
 // bounded: a timeout sets MOE_ERR_TIMEOUT and the CTA stops issuing work,
-// then waits (bounded again) for the copies, MMAs and stores it already
-// issued before it releases TMEM and retires.
+// then waits (bounded again) for the copies, MMAs, commits and stores it
+// already issued before it releases TMEM and retires.  A chunk whose K
+// blocks were cut short is never handed to the epilogue.  The main-loop
+// waits (stage empty / full, accumulator free / final) take their poll
+// limit from the launch, so that a test can make them run out; the drain
+// waits always use the full bound.
 #include <cuda.h>
 
 #include <algorithm>
@@ -47,7 +51,7 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;   // TMA warp, MMA warp, epilogue
 constexpr int kEpiCols = BN / 2;             // columns per epilogue thread
 constexpr uint32_t kTileABytes = BM * BK * 2;
 constexpr uint32_t kTileBBytes = BN * BK * 2;
-constexpr uint32_t kSpin = 1u << 20;         // polls per wait (about a second at the least)
+constexpr uint32_t kSpin = kGemmSpin;        // polls per wait (about a second at the least)
 
 // Epilogue stores: each epilogue warp stages 32 rows x 16 columns (2 KB, the
 // TMA store box) in shared memory with the 64-byte swizzle and writes it with
@@ -227,7 +231,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC,
                     const int32_t* __restrict__ group_rows, int G, int64_t a_rows, int K,
-                    int N, int32_t* __restrict__ C, Dequant dq, int32_t* dev_status) {
+                    int N, int32_t* __restrict__ C, Dequant dq, uint32_t spin,
+                    int32_t* dev_status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -327,7 +332,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const Tile tl = decode_tile(t, goff, tpre, G, ntn);
         const int brow = tl.g * N + tl.n0;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait_bounded(empty + stage, phase ^ 1u, kSpin)) {
+          if (!mbar_wait_bounded(empty + stage, phase ^ 1u, spin)) {
             set_status(dev_status, MOE_ERR_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -342,8 +347,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
       }
       // every stage's last MMA read has completed before the CTA retires
+      // (a wait that also ends when another role aborts: the MMA issuer then
+      // drains its own MMAs)
       for (int s = 0; s < kStages && !*abort_flag; ++s) {
-        if (!mbar_wait_bounded(empty + stage, phase ^ 1u, kSpin)) {
+        bool done = false;
+        for (uint32_t i = 0; i < kSpin && !done && !*abort_flag; ++i)
+          done = mbar_try_wait(empty + stage, phase ^ 1u);
+        if (!done && !*abort_flag) {
           set_status(dev_status, MOE_ERR_TIMEOUT);
           *abort_flag = 1;
         }
@@ -366,7 +376,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       for (int64_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
         for (int c = 0; ok && c < nchunks; ++c, ++chunk_ctr) {
           const uint32_t b = chunk_ctr & 1u, use = (chunk_ctr >> 1) & 1u;
-          if (!mbar_wait_bounded(tempty + b, use ^ 1u, kSpin) || *abort_flag) {
+          if (!mbar_wait_bounded(tempty + b, use ^ 1u, spin) || *abort_flag) {
             ok = false;
             break;
           }
@@ -374,7 +384,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t d = tmem + b * BN;
           const int kb1 = (c + 1) * kChunkBlocks < nkb ? (c + 1) * kChunkBlocks : nkb;
           for (int kb = c * kChunkBlocks; kb < kb1; ++kb) {
-            if (!mbar_wait_bounded(full + stage, phase, kSpin) || *abort_flag) {
+            if (!mbar_wait_bounded(full + stage, phase, spin) || *abort_flag) {
               ok = false;
               break;
             }
@@ -389,6 +399,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             ++ncommit;
             if (++stage == kStages) { stage = 0; phase ^= 1u; }
           }
+          if (!ok) break;                          // a cut-short chunk is not final
           mma_commit(tfull + b);                   // the chunk's sums are final
         }
       }
@@ -396,13 +407,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         set_status(dev_status, MOE_ERR_TIMEOUT);
         *abort_flag = 1;
       }
-      // after a timeout, the MMAs already issued finish before TMEM is
-      // released: the last stage release (phase k / kStages of
-      // empty[k % kStages]) arrives once every earlier MMA of this thread is
-      // complete
-      if (*abort_flag && ncommit > 0) {
-        const uint32_t k = ncommit - 1;
-        mbar_wait_bounded(empty + k % kStages, (k / kStages) & 1u, kSpin);
+      if (*abort_flag) {
+        // after a timeout, the MMAs already issued finish before TMEM is
+        // released: the last stage release (phase k / kStages of
+        // empty[k % kStages]) arrives once every earlier MMA of this thread
+        // is complete; and the last chunk commit (phase (n-1) / 2 of
+        // tfull[(n-1) % 2], n = chunks committed) has landed in shared
+        // memory before the CTA can retire
+        if (ncommit > 0) {
+          const uint32_t k = ncommit - 1;
+          if (!mbar_wait_bounded(empty + k % kStages, (k / kStages) & 1u, kSpin))
+            set_status(dev_status, MOE_ERR_TIMEOUT);
+        }
+        if (chunk_ctr > 0) {
+          const uint32_t n = chunk_ctr - 1;
+          if (!mbar_wait_bounded(tfull + (n & 1u), (n >> 1) & 1u, kSpin))
+            set_status(dev_status, MOE_ERR_TIMEOUT);
+        }
       }
     }
   } else {
@@ -434,7 +455,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       bool ok = true;
       for (int c = 0; c < nchunks; ++c, ++chunk_ctr) {
         const uint32_t b = chunk_ctr & 1u, use = (chunk_ctr >> 1) & 1u;
-        const bool got = mbar_wait_bounded(tfull + b, use, kSpin) && !*abort_flag;
+        const bool got = mbar_wait_bounded(tfull + b, use, spin) && !*abort_flag;
         if (!__all_sync(0xffffffffu, got)) {   // the warp stays converged
           ok = false;
           break;
@@ -659,15 +680,15 @@ namespace {
 template <int STAGES, int MODE>
 cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                         const int32_t* group_rows, int G, int64_t a_rows, int K, int N,
-                        int32_t* c, const Dequant& dq, int32_t* dev_status, int sms,
-                        cudaStream_t st) {
+                        int32_t* c, const Dequant& dq, uint32_t spin, int32_t* dev_status,
+                        int sms, cudaStream_t st) {
   const size_t smem = SmemLayout<STAGES>::bytes(G);
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<STAGES, MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   grouped_gemm_kernel<STAGES, MODE><<<sms, kThreads, smem, st>>>(ma, mb, mc, group_rows, G,
-                                                                 a_rows, K, N, c, dq,
+                                                                 a_rows, K, N, c, dq, spin,
                                                                  dev_status);
   return cudaGetLastError();
 }
@@ -675,16 +696,16 @@ cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
 template <int STAGES>
 cudaError_t launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                           const int32_t* group_rows, int G, int64_t a_rows, int K, int N,
-                          int32_t* c, const Dequant& dq, int32_t* dev_status, int sms,
-                          cudaStream_t st) {
+                          int32_t* c, const Dequant& dq, uint32_t spin, int32_t* dev_status,
+                          int sms, cudaStream_t st) {
   if (dq.mode == kOutDequant)
     return launch_mode<STAGES, kOutDequant>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
-                                            dev_status, sms, st);
+                                            spin, dev_status, sms, st);
   if (dq.mode == kOutSwiGLU)
     return launch_mode<STAGES, kOutSwiGLU>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
-                                           dev_status, sms, st);
+                                           spin, dev_status, sms, st);
   return launch_mode<STAGES, kOutInt32>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
-                                        dev_status, sms, st);
+                                        spin, dev_status, sms, st);
 }
 
 }  // namespace
@@ -707,7 +728,7 @@ cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void
                                 int N, const int32_t* group_rows, void* c, int mode,
                                 const float* col_scale, const void* row_scale,
                                 int64_t row_scale_stride, int32_t* dev_status,
-                                cudaStream_t st) {
+                                cudaStream_t st, uint32_t main_loop_polls) {
   CUtensorMap ma, mb, mc;
   cudaError_t e = encode_kmajor(&ma, a, a_rows, K, BM);
   if (e == cudaSuccess) e = encode_kmajor(&mb, b, int64_t(G) * N, K, BN);
@@ -724,9 +745,10 @@ cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void
   int32_t* out = static_cast<int32_t*>(c);
   // four stages unless the group tables (12 bytes per group) crowd them out
   if (SmemLayout<4>::bytes(G) <= size_t(optin))
-    return launch_stages<4>(ma, mb, mc, group_rows, G, a_rows, K, N, out, dq, dev_status, sms,
-                            st);
-  return launch_stages<3>(ma, mb, mc, group_rows, G, a_rows, K, N, out, dq, dev_status, sms, st);
+    return launch_stages<4>(ma, mb, mc, group_rows, G, a_rows, K, N, out, dq, main_loop_polls,
+                            dev_status, sms, st);
+  return launch_stages<3>(ma, mb, mc, group_rows, G, a_rows, K, N, out, dq, main_loop_polls,
+                          dev_status, sms, st);
 }
 
 }  // namespace moe_ep

@@ -261,6 +261,14 @@ struct Shape {
   int64_t P() const { return T() * k; }
 };
 
+// Launch facts (launch_cache.cu): the current device and its SM count, and
+// the CTAs of kernel `fn` resident per SM at a block size and dynamic shared
+// memory (occupancy cached per kernel, device and size; the >48 KB dynamic
+// shared memory attribute is set first when needed).
+cudaError_t current_device_sms(int* dev, int* sms);
+cudaError_t ensure_dynamic_smem(const void* fn, size_t smem);
+cudaError_t kernel_blocks_per_sm(const void* fn, int threads, size_t smem, int* per_sm);
+
 size_t layout_workspace_bytes(const Shape& s);
 cudaError_t launch_layout(const Shape& s, const int32_t* topk_idx,
                           int32_t* count, int32_t* rank_send,
@@ -301,12 +309,16 @@ cudaError_t launch_codes_to_bf16(const void* src, int64_t rows, int64_t stride, 
 
 int gmm_block_n();
 
-// mode: 0 int32 c, 1 dequantised fp32, 2 SwiGLU of interleaved gate/up pairs
+// mode: 0 int32 c, 1 dequantised fp32, 2 SwiGLU of interleaved gate/up pairs.
+// main_loop_polls: polls of each main-loop mbarrier wait before it gives up
+// (kGemmSpin in every entry point of the header; smaller only in the test
+// hook that makes the waits run out).
+constexpr uint32_t kGemmSpin = 1u << 20;
 cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void* b, int G,
                                 int N, const int32_t* group_rows, void* c, int mode,
                                 const float* col_scale, const void* row_scale,
                                 int64_t row_scale_stride, int32_t* dev_status,
-                                cudaStream_t st);
+                                cudaStream_t st, uint32_t main_loop_polls = kGemmSpin);
 
 cudaError_t launch_interleave_gate_up(const void* w, const float* ws, int G, int I, int K,
                                      void* wi, float* wsi, cudaStream_t st);
