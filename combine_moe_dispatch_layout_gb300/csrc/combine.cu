@@ -18,7 +18,6 @@
 // the add (__fmul_rn / __fadd_rn; the unit is also built with -fmad=false),
 // k in order; out = round-to-nearest-even in the token dtype.
 #include <algorithm>
-#include <atomic>
 
 #include "moe_ep_internal.cuh"
 
@@ -104,28 +103,6 @@ int compute_threads(int nch, int cpt) {
 // k rows are in flight while its CTA gathers them.
 constexpr int64_t kInFlightBytes = 160 * 1024;
 
-// CTAs of combine_kernel<DT> per SM for a block size, queried once per device
-// and block size (the launcher asks for two sizes on every call; the query
-// costs host time that small, launch-bound calls would otherwise pay).
-template <int DT>
-cudaError_t blocks_per_sm(int dev, int threads, int* out) {
-  constexpr int kDevs = 16, kSizes = kMaxThreads / 32 + 1;
-  static std::atomic<int> cache[kDevs][kSizes];   // 0: not known yet
-  const bool cached = dev >= 0 && dev < kDevs && threads % 32 == 0 && threads <= kMaxThreads;
-  if (cached) {
-    const int v = cache[dev][threads / 32].load(std::memory_order_relaxed);
-    if (v > 0) {
-      *out = v;
-      return cudaSuccess;
-    }
-  }
-  const cudaError_t e =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, combine_kernel<DT>, threads, 0);
-  if (e == cudaSuccess && cached && *out > 0)
-    cache[dev][threads / 32].store(*out, std::memory_order_relaxed);
-  return e;
-}
-
 template <int DT>
 cudaError_t launch_t(const Shape& s, const void* y, int64_t y_rows,
                      const int32_t* topk_idx, const float* weights,
@@ -134,8 +111,7 @@ cudaError_t launch_t(const Shape& s, const void* y, int64_t y_rows,
                      int32_t* dev_status, cudaStream_t st) {
   const int nch = s.H / 8;
   int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = current_device_sms(&dev, &sms);
   if (e != cudaSuccess) return e;
   // Two chunks per compute thread (a shorter gather per token) when the CTAs
   // that fit still keep kInFlightBytes of rows in flight per SM, else four
@@ -145,7 +121,8 @@ cudaError_t launch_t(const Shape& s, const void* y, int64_t y_rows,
   int threads = 0, per_sm = 0;
   for (int cpt = 2; cpt <= 4; cpt += 2) {
     threads = compute_threads(nch, cpt) + 32;
-    e = blocks_per_sm<DT>(dev, threads, &per_sm);
+    e = kernel_blocks_per_sm(reinterpret_cast<const void*>(combine_kernel<DT>), threads, 0,
+                             &per_sm);
     if (e != cudaSuccess) return e;
     if (int64_t(per_sm) * s.k * s.H * 2 >= kInFlightBytes) break;
   }

@@ -214,11 +214,10 @@ cudaError_t launch_quant_t(const Shape& s, const void* yq, int64_t y_rows,
                            int32_t* dev_status, cudaStream_t st) {
   constexpr int threads = kCqWarps * 32;
   int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = current_device_sms(&dev, &sms);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, combine_quant_kernel<DT, KB, MULTI>, threads, 0);
+    e = kernel_blocks_per_sm(reinterpret_cast<const void*>(combine_quant_kernel<DT, KB, MULTI>),
+                             threads, 0, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t max_ctas = int64_t(std::max(1, per_sm)) * sms;
   const int parts = parts_for(s.T(), s.H / 8, max_ctas * kCqWarps);

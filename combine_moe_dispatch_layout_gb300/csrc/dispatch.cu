@@ -341,14 +341,10 @@ dispatch_copy_kernel(const unsigned char* __restrict__ x,
 template <typename Kernel>
 cudaError_t launch_persistent(Kernel kernel, int threads, int smem, int64_t T,
                               int* grid_out) {
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-  }
   int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+  cudaError_t e = current_device_sms(&dev, &sms);
+  if (e == cudaSuccess)
+    e = kernel_blocks_per_sm(reinterpret_cast<const void*>(kernel), threads, smem, &per_sm);
   if (e != cudaSuccess) return e;
   *grid_out = static_cast<int>(std::min<int64_t>(T, int64_t(std::max(1, per_sm)) * sms));
   return cudaSuccess;

@@ -535,13 +535,10 @@ cudaError_t launch_t(const Shape& s, Params p, cudaStream_t st) {
   auto kernel = fused_dispatch_kernel<DT, QUANT, STAGED, CPS>;
   const size_t smem = static_cast<size_t>(
       fused_smem(s.R, s.E(), s.H, p.row_bytes, STAGED, QUANT).bytes);
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
   int dev = 0, sms = 0, per_sm = 0;
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = current_device_sms(&dev, &sms);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, smem);
+    e = kernel_blocks_per_sm(reinterpret_cast<const void*>(kernel), kThreads, smem, &per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   // a CTA per token (or tile), few enough for a cheap barrier; all co-resident

@@ -26,9 +26,14 @@
  *
  * Conventions for every entry point:
  *  - All array arguments are DEVICE pointers, allocated and owned by the
- *    caller; the library allocates nothing, keeps no global state, and
- *    never synchronises.  Work is enqueued on `stream` (a cudaStream_t;
- *    NULL = the legacy default stream) and returns immediately.
+ *    caller; the library allocates nothing and never synchronises.  Work is
+ *    enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and returns immediately.
+ *  - Global state: two things only.  The launchers remember each device's
+ *    SM count and, per kernel, block size and shared-memory size, the
+ *    occupancy they queried on first use (read-only device facts, behind a
+ *    mutex; they change no result).  moe_dispatch_layout_static owns one
+ *    device array (see there).  Nothing else outlives a call.
  *  - Host-checkable problems (NULL or misaligned pointers, sizes out of
  *    range) are reported synchronously by the return value and nothing is
  *    enqueued.  A failed launch returns MOE_ERR_CUDA.
@@ -138,15 +143,19 @@ moe_status moe_dispatch_layout(const moe_shape* shape, const int32_t* topk_idx,
  * enqueued.  No call allocates or frees memory (no cudaMalloc, cudaFree or
  * allocating library routine).
  *
- * The first call on each device does a one-time set-up with that device
- * current: it looks up the array's device address (cudaGetSymbolAddress)
- * and caches it; make that first call before any stream capture.  Every
- * call then clears the part of the array it uses (cudaMemsetAsync on
- * `stream`) and launches the layout kernel on it.  All calls share the one
- * array, which keeps the last call's contents: calls that overlap on the
- * GPU (different streams, or several host threads) race and must be
- * serialised by the caller.  The current device must be the device of
- * `stream`.  Returns MOE_ERR_CUDA if the set-up or the clear fails. */
+ * Every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress), so the current device must be the device of
+ * `stream`.  The first call on each device is also the set-up: that lookup
+ * loads the library's kernels onto the device, so make that first call
+ * before any stream capture.  The address is not cached, so a call after
+ * cudaDeviceReset finds the reloaded array.  Every call then clears the
+ * part of the array it uses (cudaMemsetAsync on `stream`; needed only to
+ * recover from an earlier call that timed out or overlapped another, but
+ * always done) and launches the layout kernel on it: two operations on the
+ * stream.  All calls share the one array, which keeps the last call's
+ * contents: calls that overlap on the GPU (different streams, or several
+ * host threads) race and must be serialised by the caller.  Returns
+ * MOE_ERR_CUDA if the lookup or the clear fails. */
 moe_status moe_dispatch_layout_static(const moe_shape* shape,
                                       const int32_t* topk_idx, int32_t* count,
                                       int32_t* rank_send, int32_t* send_idx,
