@@ -243,8 +243,11 @@ moe_status moe_combine(const moe_shape* shape, const void* expert_out,
  * token output inside one kernel (section 3.2).  Same arguments and results
  * as moe_dispatch_layout + moe_notify_dispatch + moe_dispatch (bit for
  * bit), for small batches where three launches cost more than the work.
- * One cooperative launch of persistent CTAs with grid barriers between the
- * phases; for large batches the separate calls are faster.
+ * A problem that fits one SM's shared memory (R <= 32, T <= 256, T*k <=
+ * 4096, R*E <= 8192, T*H*2 <= 64 KB) runs in one CTA with no grid barrier;
+ * larger ones in one cooperative launch of persistent CTAs with grid
+ * barriers between the phases (the one-CTA kernel leaves the workspace
+ * untouched, so both kinds of call may share it).
  *   workspace  moe_fused_workspace_bytes() bytes, 16-byte aligned,
  *              zero-filled once before first use (each call leaves it ready;
  *              after MOE_ERR_TIMEOUT zero it again)

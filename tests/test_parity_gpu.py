@@ -467,6 +467,46 @@ def test_fused_dispatch_edges_and_reuse(oracle_mod, pl):
     assert b0.rank_recv_base.cpu().tolist() == [0] * (w0.R + 1)
 
 
+@pytest.mark.parametrize("w", [
+    W.Workload("fs_k40", R=4, epr=16, bs=25, k=40, H=136, seed=81),      # k > 32 rows per lane
+    W.Workload("fs_r32", R=32, epr=3, bs=8, k=5, H=64, seed=82),         # 32 source ranks
+    W.Workload("fs_x64k", R=8, epr=4, bs=32, k=16, H=128, seed=83),      # 64 KB of x, 4096 pairs
+    W.Workload("fs_fp16", R=3, epr=2, bs=40, k=2, H=264, dtype=W.FP16, quant=False,
+               x_dist="uniform", x_scale=4.0, seed=84),                  # verbatim rows
+    W.Workload("fs_zipf", R=5, epr=7, bs=30, k=6, H=200, routing="zipf", weights="sigmoid",
+               x_scale=2.0, seed=85),
+], ids=lambda w: w.name)
+def test_fused_dispatch_one_cta_shapes(oracle_mod, pl, w):
+    """Shapes small enough for the one-CTA kernel (every intermediate in one
+    SM's shared memory), at the edges of its limits."""
+    _check_fused(oracle_mod, pl, w)
+
+
+def test_fused_dispatch_one_cta_edges(oracle_mod, pl):
+    """The one-CTA kernel with bad ids, a short receive buffer and duplicate
+    experts in a token, interleaved with multi-CTA launches on the same
+    workspace (the one-CTA kernel leaves the grid barrier's words alone)."""
+    small = W.Workload("fse", R=4, epr=3, bs=20, k=4, H=96, seed=86)
+    big = W.Workload("fse", R=4, epr=3, bs=600, k=4, H=96, seed=86)
+    b = pl.PipelineBuffers(big.R, big.bs, big.k, big.epr, big.H, big.dtype, big.quant)
+    bs_ = pl.PipelineBuffers(small.R, small.bs, small.k, small.epr, small.H, small.dtype,
+                             small.quant)
+    bs_._fused_ws = b.fused_workspace             # one workspace for both shapes
+    _check_fused(oracle_mod, pl, small, b=bs_)
+    _check_fused(oracle_mod, pl, big, b=b)
+    idx = W.routing(small)[0].numpy().copy()
+    idx[3, 1] = -1
+    idx[7, 0] = small.E
+    _check_fused(oracle_mod, pl, small, idx=idx, expect_status=2, b=bs_)
+    _check_fused(oracle_mod, pl, big, b=b)
+    _check_fused(oracle_mod, pl, small, capacity=small.P - 37, expect_status=3, b=bs_)
+    idx = W.routing(small)[0].numpy().copy()
+    idx[:, 1] = idx[:, 0]                         # each token names one expert twice
+    idx[5, :] = 2                                 # ... or four times
+    _check_fused(oracle_mod, pl, small, idx=idx, b=bs_)
+    _check_fused(oracle_mod, pl, big.with_(seed=87), b=b)
+
+
 # ---------------------------------------------------------------------------
 # GMM1 epilogue (moe_swiglu_quant)
 # ---------------------------------------------------------------------------
