@@ -108,9 +108,11 @@ def _file_hash(rel):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of that kernel (else None)."""
+def recorded_traffic(kernel, workload, key="traffic_bytes_per_launch"):
+    """Bytes per launch from the committed ncu record, if it was taken on the
+    current source of that kernel (else None).  key: traffic_bytes_per_launch
+    (DRAM reads + the SMs' writes into L2) or dram_bytes_per_launch (DRAM
+    reads + DRAM writes; writes still in L2 at kernel end are missing)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
@@ -118,9 +120,13 @@ def recorded_traffic(kernel, workload):
         ent = d[kernel][workload]
         if ent["source_sha256_16"] != _file_hash(KERNEL_SOURCES[kernel]):
             return None
-        return float(ent["dram_bytes_per_launch"])
+        return float(ent[key])
     except (OSError, KeyError, ValueError):
         return None
+
+
+TRAFFIC_NOTE = ("traffic = DRAM reads + the bytes the SMs wrote into L2 (ncu, a small case "
+                "scaled to a launch); traffic_dram = DRAM reads + DRAM writes")
 
 
 # ---------------------------------------------------------------------------
@@ -341,7 +347,9 @@ def config_record(w, m, peak, peak_kind, cpu=None):
         gbs = ab[n] / (ms * 1e-3) / 1e9
         return {"kernel": n, "bound": "hbm", "achieved": gbs, "peak": peak,
                 "peak_source": peak_kind, "unit": "GB/s", "frac": gbs / peak,
-                "traffic": recorded_traffic(n, w.name), "algorithmic_bytes": ab[n],
+                "traffic": recorded_traffic(n, w.name),
+                "traffic_dram": recorded_traffic(n, w.name, "dram_bytes_per_launch"),
+                "traffic_note": TRAFFIC_NOTE, "algorithmic_bytes": ab[n],
                 "avg_launch_ms": ms, "tokens_per_s": w.T / (ms * 1e-3)}
     disp, comb = roof("dispatch", 2), roof("combine", 3)
     return {
@@ -416,6 +424,8 @@ def run_gpu(args, w):
         cq = {"us": cq_us, "achieved_gbs": cq_bytes / (cq_us * 1e-6) / 1e9,
               "algorithmic_bytes": cq_bytes,
               "traffic": recorded_traffic("combine_quant", w.name),
+              "traffic_dram": recorded_traffic("combine_quant", w.name,
+                                               "dram_bytes_per_launch"),
               "frac": cq_bytes / (cq_us * 1e-6) / 1e9 / peak,
               "tokens_per_s": w.T / (cq_us * 1e-6)}
         del yq
@@ -438,6 +448,8 @@ def run_gpu(args, w):
         sw_bytes = w.P * (8 * I + (I + 31) // 32 * 32 + 32 + 4) + 8 * I
         sw = {"us": sw_us, "rows": w.P, "I": I, "algorithmic_bytes": sw_bytes,
               "traffic": recorded_traffic("swiglu_quant", w.name),
+              "traffic_dram": recorded_traffic("swiglu_quant", w.name,
+                                               "dram_bytes_per_launch"),
               "achieved_gbs": sw_bytes / (sw_us * 1e-6) / 1e9,
               "frac": sw_bytes / (sw_us * 1e-6) / 1e9 / peak}
         del acc_d, sw_out
