@@ -13,10 +13,11 @@
 // and 1/scales into its own shared-memory table, then each lane walks
 // 8-code chunks of the item (one 8-byte load per row; all k rows of a chunk
 // in one batch when k <= 8, batches of 8 rows otherwise), issuing the next
-// (chunk, batch)'s loads before it computes the current one.  Per element: a sign-extending byte permute, an int-to-float
-// conversion, two multiplies and an add -- the arithmetic is about as long
-// as the HBM time, so keeping loads in flight across the compute is what
-// matters.  Rows are half the bytes of bf16 rows.
+// (chunk, batch)'s loads before it computes the current one.  Per element: a
+// byte permute and a subtraction (the code as a float, see code_f), two
+// multiplies and an add, all on the FP32 pipe -- the arithmetic is about as
+// long as the HBM time, so keeping loads in flight across the compute is
+// what matters.  Rows are half the bytes of bf16 rows.
 #include <algorithm>
 
 #include "moe_ep_internal.cuh"
@@ -35,12 +36,15 @@ __device__ __forceinline__ uint2 ld_stream_8(const void* p) {
   return v;
 }
 
-// Byte i of w, sign-extended (byte permute), converted to float (exact).
+// The INT8 code in byte i of w as a float, exactly, without the conversion
+// pipe (int-to-float runs at a quarter of the FP32 rate, and this kernel
+// converts k codes per output): with wb = w ^ 0x80808080 the byte holds
+// u = q + 128 in 0..255; a byte permute places it under the exponent of 2^23
+// (bits 0x4B0000uu = 2^23 + u, exact), and subtracting 2^23 + 128 leaves q
+// (an exact fp32 subtraction of integers below 2^24).
 template <int I>
-__device__ __forceinline__ float code_f(uint32_t w) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(w), "n"(0x8880 | (I * 0x1111)));
-  return __int2float_rn(static_cast<int32_t>(r));
+__device__ __forceinline__ float code_f(uint32_t wb) {
+  return __fsub_rn(__uint_as_float(__byte_perm(wb, 0x4B000000u, 0x7650 + I)), 8388736.0f);
 }
 
 // One row of the warp's table: the row's first byte (nullptr for padding or
@@ -122,7 +126,7 @@ combine_quant_kernel(const unsigned char* __restrict__ yq, int64_t y_rows,
         if (!MULTI || b * KB + j < k) {           // warp-uniform: padding rows skipped
           const float2 wi = *reinterpret_cast<const float2*>(&ref[b * KB + j].w);
           const float wk = wi.x, sk = wi.y;
-          const uint32_t lo = v[j].x, hi = v[j].y;
+          const uint32_t lo = v[j].x ^ 0x80808080u, hi = v[j].y ^ 0x80808080u;
           const float q[8] = {code_f<0>(lo), code_f<1>(lo), code_f<2>(lo), code_f<3>(lo),
                               code_f<0>(hi), code_f<1>(hi), code_f<2>(hi), code_f<3>(hi)};
 #pragma unroll
