@@ -7,17 +7,19 @@
 // (1/scale) (one rounding) before the combine's multiply-then-add
 // (__fmul_rn / __fadd_rn, k in order), then rounded to the token dtype.
 //
+// Per element: a byte permute and a subtraction give the code as a float
+// (see code_raw), then two multiplies and an add; these run as packed fp32x2
+// operations on pairs of elements (mul2_rn / add2_rn, bit-identical to the
+// scalar ones), which halves the arithmetic's instruction count.
+//
 // Work is split per warp, with no block barrier: a work item is one token,
 // or a contiguous part of its hidden dimension when that evens out the last
 // round over the grid's warps.  The warp resolves the item's k rows, weights
 // and 1/scales into its own shared-memory table, then each lane walks
 // 8-code chunks of the item (one 8-byte load per row; all k rows of a chunk
 // in one batch when k <= 8, batches of 8 rows otherwise), issuing the next
-// (chunk, batch)'s loads before it computes the current one.  Per element: a
-// byte permute and a subtraction (the code as a float, see code_f), two
-// multiplies and an add, all on the FP32 pipe -- the arithmetic is about as
-// long as the HBM time, so keeping loads in flight across the compute is
-// what matters.  Rows are half the bytes of bf16 rows.
+// (chunk, batch)'s loads before it computes the current one.  Rows are half
+// the bytes of bf16 rows.
 #include <algorithm>
 
 #include "moe_ep_internal.cuh"
@@ -43,8 +45,8 @@ __device__ __forceinline__ uint2 ld_stream_8(const void* p) {
 // (bits 0x4B0000uu = 2^23 + u, exact), and subtracting 2^23 + 128 leaves q
 // (an exact fp32 subtraction of integers below 2^24).
 template <int I>
-__device__ __forceinline__ float code_f(uint32_t wb) {
-  return __fsub_rn(__uint_as_float(__byte_perm(wb, 0x4B000000u, 0x7650 + I)), 8388736.0f);
+__device__ __forceinline__ float code_raw(uint32_t wb) {
+  return __uint_as_float(__byte_perm(wb, 0x4B000000u, 0x7650 + I));
 }
 
 // One row of the warp's table: the row's first byte (nullptr for padding or
@@ -57,8 +59,10 @@ struct __align__(16) RowRef {
 
 // KB: rows per batch.  MULTI = false: KB == k (one batch, no padding).
 // MULTI = true: KB = 8, k > 8 split into batches, the last one padded.
+// Three CTAs per SM (at most 80 registers); seven rows per batch need a few
+// more registers than that without spilling, so that variant runs two.
 template <int DT, int KB, bool MULTI>
-__global__ void __launch_bounds__(kCqWarps * 32, 3)
+__global__ void __launch_bounds__(kCqWarps * 32, KB == 7 ? 2 : 3)
 combine_quant_kernel(const unsigned char* __restrict__ yq, int64_t y_rows,
                      int64_t row_bytes, const int32_t* __restrict__ topk_idx,
                      const float* __restrict__ weights,
@@ -66,7 +70,7 @@ combine_quant_kernel(const unsigned char* __restrict__ yq, int64_t y_rows,
                      const int32_t* __restrict__ put_offset,
                      const int64_t* __restrict__ rank_recv_base, int R, int bs,
                      int k, int epr, int H, int64_t T, int parts,
-                     uint4* __restrict__ out, int32_t* dev_status) {
+                     uint4* __restrict__ out, int32_t* dev_status, float neg_zero) {
   __shared__ RowRef s_ref[kCqWarps][MOE_EP_MAX_TOPK];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   RowRef* ref = s_ref[warp];
@@ -120,19 +124,22 @@ combine_quant_kernel(const unsigned char* __restrict__ yq, int64_t y_rows,
         if (p != nullptr) v[j] = ld_stream_8(p + 8 * int64_t(c));
       }
     };
-    auto accumulate = [&](int b, const uint2 (&v)[KB], float (&acc)[8]) {
+    auto accumulate = [&](int b, const uint2 (&v)[KB], float2 (&acc)[4]) {
 #pragma unroll
       for (int j = 0; j < KB; ++j) {
         if (!MULTI || b * KB + j < k) {           // warp-uniform: padding rows skipped
           const float2 wi = *reinterpret_cast<const float2*>(&ref[b * KB + j].w);
-          const float wk = wi.x, sk = wi.y;
+          const float2 wk = make_float2(wi.x, wi.x), sk = make_float2(wi.y, wi.y);
+          const float2 bias = make_float2(-8388736.0f, -8388736.0f);
           const uint32_t lo = v[j].x ^ 0x80808080u, hi = v[j].y ^ 0x80808080u;
-          const float q[8] = {code_f<0>(lo), code_f<1>(lo), code_f<2>(lo), code_f<3>(lo),
-                              code_f<0>(hi), code_f<1>(hi), code_f<2>(hi), code_f<3>(hi)};
+          const float2 q[4] = {add2_rn(make_float2(code_raw<0>(lo), code_raw<1>(lo)), bias),
+                               add2_rn(make_float2(code_raw<2>(lo), code_raw<3>(lo)), bias),
+                               add2_rn(make_float2(code_raw<0>(hi), code_raw<1>(hi)), bias),
+                               add2_rn(make_float2(code_raw<2>(hi), code_raw<3>(hi)), bias)};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float t = __fmul_rn(q[e], sk);                 // dequantise
-            acc[e] = __fadd_rn(acc[e], __fmul_rn(t, wk));        // Muls, Add
+          for (int e = 0; e < 4; ++e) {   // elements 2e, 2e + 1
+            const float2 t = mul2_rn(q[e], sk, neg_zero);              // dequantise
+            acc[e] = add2_rn(acc[e], mul2_rn(t, wk, neg_zero));        // Muls, Add
           }
         }
       }
@@ -140,17 +147,22 @@ combine_quant_kernel(const unsigned char* __restrict__ yq, int64_t y_rows,
     uint2 va[KB], vb[KB];
 #pragma unroll
     for (int j = 0; j < KB; ++j) va[j] = vb[j] = make_uint2(0u, 0u);
-    float acc[8];
+    float2 acc[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+    for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.0f, 0.0f);
+    auto packed = [&]() {
+      const float f[8] = {acc[0].x, acc[0].y, acc[1].x, acc[1].y,
+                          acc[2].x, acc[2].y, acc[3].x, acc[3].y};
+      return pack8<DT>(f);
+    };
     int c = c0 + lane;
     if (!MULTI) {
       // One batch per chunk; two register sets alternate (chunk c + 32 loads
       // while chunk c computes).
       auto finish = [&](int cc) {
-        out[g * nch + cc] = pack8<DT>(acc);
+        out[g * nch + cc] = packed();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+        for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.0f, 0.0f);
       };
       if (c < c1) load(c, 0, va);
       while (c < c1) {
@@ -177,9 +189,9 @@ combine_quant_kernel(const unsigned char* __restrict__ yq, int64_t y_rows,
         if (cn < c1) load(cn, bn, vb);
         accumulate(b, va, acc);
         if (bn == 0) {
-          out[g * nch + c] = pack8<DT>(acc);
+          out[g * nch + c] = packed();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+          for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.0f, 0.0f);
         }
         c = cn;
         b = bn;
@@ -230,7 +242,7 @@ cudaError_t launch_quant_t(const Shape& s, const void* yq, int64_t y_rows,
   combine_quant_kernel<DT, KB, MULTI><<<static_cast<unsigned>(grid), threads, 0, st>>>(
       static_cast<const unsigned char*>(yq), y_rows, align_up(s.H, 32) + 32, topk_idx,
       weights, send_idx, put_offset, rank_recv_base, s.R, s.bs, s.k, s.epr, s.H, s.T(), parts,
-      static_cast<uint4*>(out), dev_status);
+      static_cast<uint4*>(out), dev_status, -0.0f);
   return cudaGetLastError();
 }
 

@@ -54,7 +54,7 @@ template <int kCpt, bool BF16OUT>
 __global__ void __launch_bounds__(kMaxThreads)
 swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc sc,
                     unsigned char* __restrict__ out, int64_t row_bytes,
-                    float* __restrict__ out_scale) {
+                    float* __restrict__ out_scale, float nz) {
   __shared__ float s_wmax[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nwarps = nthreads / 32;
@@ -99,16 +99,18 @@ swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc 
         const float4 wu1 = __ldg(reinterpret_cast<const float4*>(weight_scale + I + 8 * c + 4));
         const float wg[8] = {wg0.x, wg0.y, wg0.z, wg0.w, wg1.x, wg1.y, wg1.z, wg1.w};
         const float wu[8] = {wu0.x, wu0.y, wu0.z, wu0.w, wu1.x, wu1.y, wu1.z, wu1.w};
+        const float2 ts2 = bcast2(ts);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float gate = __int2float_rn(gi[j]);
-          gate = __fmul_rn(gate, wg[j]);
-          gate = __fmul_rn(gate, ts);
-          float up = __int2float_rn(ui[j]);
-          up = __fmul_rn(up, wu[j]);
-          up = __fmul_rn(up, ts);
-          h[i][j] = swiglu_rn(gate, up);
-          amax = fmaxf(amax, fabsf(h[i][j]));
+        for (int j = 0; j < 8; j += 2) {   // two outputs per packed operation
+          float2 gate = make_float2(__int2float_rn(gi[j]), __int2float_rn(gi[j + 1]));
+          gate = mul2_rn(mul2_rn(gate, make_float2(wg[j], wg[j + 1]), nz), ts2, nz);
+          float2 up = make_float2(__int2float_rn(ui[j]), __int2float_rn(ui[j + 1]));
+          up = mul2_rn(mul2_rn(up, make_float2(wu[j], wu[j + 1]), nz), ts2, nz);
+          const float2 hh = swiglu2_rn(gate, up, nz);
+          h[i][j] = hh.x;
+          h[i][j + 1] = hh.y;
+          amax = fmaxf(amax, fabsf(hh.x));
+          amax = fmaxf(amax, fabsf(hh.y));
         }
       }
     }
@@ -128,16 +130,20 @@ swiglu_quant_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc 
         // q = rint(h * scale) in [-127, 127]; after adding kRoundMagic the
         // low byte of the float's bits is q as an int8.
         uint32_t b[8];
+        float2 bv[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          b[j] = __float_as_uint(__fadd_rn(__fmul_rn(h[i][j], scale), kRoundMagic));
+        for (int j = 0; j < 4; ++j) {
+          bv[j] = add2_rn(mul2_rn(make_float2(h[i][2 * j], h[i][2 * j + 1]), bcast2(scale), nz),
+                          bcast2(kRoundMagic));
+          b[2 * j] = __float_as_uint(bv[j].x);
+          b[2 * j + 1] = __float_as_uint(bv[j].y);
+        }
         if (BF16OUT) {   // q itself (exact subtraction), then its bf16 bits (exact)
           uint32_t w4[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float q0 = __fsub_rn(__uint_as_float(b[2 * j]), kRoundMagic);
-            const float q1 = __fsub_rn(__uint_as_float(b[2 * j + 1]), kRoundMagic);
-            w4[j] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632);
+            const float2 q = add2_rn(bv[j], bcast2(-kRoundMagic));
+            w4[j] = __byte_perm(__float_as_uint(q.x), __float_as_uint(q.y), 0x7632);
           }
           *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         } else {
@@ -171,7 +177,7 @@ template <bool BF16OUT>
 __global__ void __launch_bounds__(256, 3)
 swiglu_quant_warp_kernel(const int32_t* __restrict__ acc, int64_t M, int I, ScaleSrc sc,
                          unsigned char* __restrict__ out, int64_t row_bytes,
-                         float* __restrict__ out_scale) {
+                         float* __restrict__ out_scale, float nz) {
   extern __shared__ float4 s_hbuf[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
   float* hb = reinterpret_cast<float*>(s_hbuf) + int64_t(warp) * I;
@@ -235,16 +241,18 @@ swiglu_quant_warp_kernel(const int32_t* __restrict__ acc, int64_t M, int I, Scal
       const float wg[8] = {wg0.x, wg0.y, wg0.z, wg0.w, wg1.x, wg1.y, wg1.z, wg1.w};
       const float wu[8] = {wu0.x, wu0.y, wu0.z, wu0.w, wu1.x, wu1.y, wu1.z, wu1.w};
       float h[8];
+      const float2 ts2 = bcast2(ts);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float gate = __int2float_rn(gi[j]);
-        gate = __fmul_rn(gate, wg[j]);
-        gate = __fmul_rn(gate, ts);
-        float up = __int2float_rn(ui[j]);
-        up = __fmul_rn(up, wu[j]);
-        up = __fmul_rn(up, ts);
-        h[j] = swiglu_rn(gate, up);
-        amax = fmaxf(amax, fabsf(h[j]));
+      for (int j = 0; j < 8; j += 2) {   // two outputs per packed operation
+        float2 gate = make_float2(__int2float_rn(gi[j]), __int2float_rn(gi[j + 1]));
+        gate = mul2_rn(mul2_rn(gate, make_float2(wg[j], wg[j + 1]), nz), ts2, nz);
+        float2 up = make_float2(__int2float_rn(ui[j]), __int2float_rn(ui[j + 1]));
+        up = mul2_rn(mul2_rn(up, make_float2(wu[j], wu[j + 1]), nz), ts2, nz);
+        const float2 hh = swiglu2_rn(gate, up, nz);
+        h[j] = hh.x;
+        h[j + 1] = hh.y;
+        amax = fmaxf(amax, fabsf(hh.x));
+        amax = fmaxf(amax, fabsf(hh.y));
       }
       *reinterpret_cast<float4*>(hb + 8 * c) = make_float4(h[0], h[1], h[2], h[3]);
       *reinterpret_cast<float4*>(hb + 8 * c + 4) = make_float4(h[4], h[5], h[6], h[7]);
@@ -264,16 +272,20 @@ swiglu_quant_warp_kernel(const int32_t* __restrict__ acc, int64_t M, int I, Scal
       // q = rint(h * scale) in [-127, 127]; after adding kRoundMagic the low
       // byte of the float's bits is q as an int8.
       uint32_t b[8];
+      float2 bv[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        b[j] = __float_as_uint(__fadd_rn(__fmul_rn(h[j], scale), kRoundMagic));
+      for (int j = 0; j < 4; ++j) {
+        bv[j] = add2_rn(mul2_rn(make_float2(h[2 * j], h[2 * j + 1]), bcast2(scale), nz),
+                        bcast2(kRoundMagic));
+        b[2 * j] = __float_as_uint(bv[j].x);
+        b[2 * j + 1] = __float_as_uint(bv[j].y);
+      }
       if (BF16OUT) {   // q itself (exact subtraction), then its bf16 bits (exact)
         uint32_t w4[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float q0 = __fsub_rn(__uint_as_float(b[2 * j]), kRoundMagic);
-          const float q1 = __fsub_rn(__uint_as_float(b[2 * j + 1]), kRoundMagic);
-          w4[j] = __byte_perm(__float_as_uint(q0), __float_as_uint(q1), 0x7632);
+          const float2 q = add2_rn(bv[j], bcast2(-kRoundMagic));
+          w4[j] = __byte_perm(__float_as_uint(q.x), __float_as_uint(q.y), 0x7632);
         }
         *reinterpret_cast<uint4*>(dst + 16 * c) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       } else {
@@ -313,7 +325,7 @@ cudaError_t launch_warp_t(const int32_t* acc, int64_t M, int I, const ScaleSrc& 
       std::min<int64_t>((M + W - 1) / W, int64_t(std::max(1, per_sm)) * sms);
   kernel<<<static_cast<unsigned>(grid), threads, smem, st>>>(
       acc, M, I, sc, static_cast<unsigned char*>(out),
-      BF16OUT ? int64_t(I) * 2 : align_up(I, 32) + 32, out_scale);
+      BF16OUT ? int64_t(I) * 2 : align_up(I, 32) + 32, out_scale, -0.0f);
   return cudaGetLastError();
 }
 
@@ -332,7 +344,7 @@ cudaError_t launch_t(const int32_t* acc, int64_t M, int I, const ScaleSrc& sc, v
   const int64_t grid = std::min<int64_t>(M, int64_t(std::max(1, per_sm)) * sms);
   swiglu_quant_kernel<kCpt, BF16OUT><<<static_cast<unsigned>(grid), threads, 0, st>>>(
       acc, M, I, sc, static_cast<unsigned char*>(out),
-      BF16OUT ? int64_t(I) * 2 : align_up(I, 32) + 32, out_scale);
+      BF16OUT ? int64_t(I) * 2 : align_up(I, 32) + 32, out_scale, -0.0f);
   return cudaGetLastError();
 }
 

@@ -360,6 +360,8 @@ def test_combine_quant_full_size(oracle_mod, pl, name):
     dict(R=3, epr=2, bs=500, k=3, H=1032),                 # k = 3
     dict(R=2, epr=5, bs=333, k=5, H=264, dtype=W.FP16),    # k = 5, fp16 out
     dict(R=8, epr=8, bs=64, k=64, H=256),                  # largest k
+    dict(R=4, epr=8, bs=200, k=13, H=512),                 # CTA form: a partial row batch
+    dict(R=3, epr=3, bs=90, k=6, H=272, dtype=W.FP16),     # CTA form, fp16 out
 ], ids=lambda c: "-".join("%s%s" % kv for kv in c.items()))
 def test_combine_quant_mid(oracle_mod, pl, case):
     _check_combine_quant(oracle_mod, pl, W.Workload("cq", **case))
