@@ -6,9 +6,10 @@
 // kernel, so its answer is remembered per (kernel, device, block size,
 // dynamic shared memory), and the SM count per device.  Both are properties
 // of the device and the compiled kernel: caching them changes no result.
-// The dynamic shared memory limit above 48 KB is a per-context function
-// attribute, which a device reset clears, so it is set on every launch
-// that needs it (a cheap call) rather than remembered.
+// The dynamic shared memory limit above the default 48 KB per block (static
+// plus dynamic) is a per-context function attribute, which a device reset
+// clears, so it is set on every launch that needs it (a cheap call) rather
+// than remembered; the kernel's static size it depends on is looked up once.
 #include <mutex>
 #include <vector>
 
@@ -26,8 +27,14 @@ struct OccEntry {
 
 constexpr int kMaxDevs = 64;
 
+struct StaticEntry {
+  const void* fn;
+  size_t bytes;
+};
+
 std::mutex g_mu;
 std::vector<OccEntry> g_occ;
+std::vector<StaticEntry> g_static;
 int g_sms[kMaxDevs] = {};
 
 }  // namespace
@@ -50,8 +57,33 @@ cudaError_t current_device_sms(int* dev, int* sms) {
   return e;
 }
 
+// Static shared memory of a kernel (a property of the compiled function,
+// looked up once).
+cudaError_t static_smem(const void* fn, size_t* bytes) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (const StaticEntry& e : g_static)
+      if (e.fn == fn) {
+        *bytes = e.bytes;
+        return cudaSuccess;
+      }
+  }
+  cudaFuncAttributes a;
+  const cudaError_t e = cudaFuncGetAttributes(&a, fn);
+  if (e != cudaSuccess) return e;
+  *bytes = a.sharedSizeBytes;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_static.size() < 4096) g_static.push_back({fn, a.sharedSizeBytes});
+  return cudaSuccess;
+}
+
 cudaError_t ensure_dynamic_smem(const void* fn, size_t smem) {
-  if (smem <= 48 * 1024) return cudaSuccess;   // within the default limit
+  if (smem == 0) return cudaSuccess;
+  size_t stat = 0;
+  cudaError_t e = static_smem(fn, &stat);
+  if (e != cudaSuccess) return e;
+  // the default per-block limit (48 KB) covers static plus dynamic memory
+  if (smem + stat <= 48 * 1024) return cudaSuccess;
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(smem));
 }

@@ -335,12 +335,10 @@ cudaError_t launch_t(const Shape& s, const int32_t* topk_idx, int32_t* count,
   const int tpr = tiles_per_rank_of(s);
   const int num_tiles = s.R * tpr;
   const size_t smem = smem_bytes(W, s.E());
-  if (smem > 48 * 1024) {   // opt in to more than 48 KB (large E only)
-    cudaError_t e = cudaFuncSetAttribute(layout_kernel<W, ROUNDS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-  }
+  // opt in above the default 48 KB per block (large E only)
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(layout_kernel<W, ROUNDS>),
+                                      smem);
+  if (e != cudaSuccess) return e;
   layout_kernel<W, ROUNDS><<<num_tiles, W * 32, smem, st>>>(
       topk_idx, s.R, s.epr, int64_t(s.bs) * s.k, tpr, num_tiles, count,
       rank_send, send_idx, workspace, dev_status);
