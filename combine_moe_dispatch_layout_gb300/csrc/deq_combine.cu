@@ -148,11 +148,10 @@ cudaError_t launch_t(const Shape& s, const int32_t* acc2, int64_t y_rows,
                      int32_t* dev_status, cudaStream_t st) {
   const int threads = compute_threads(s.H / 8) + 32;
   int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = current_device_sms(&dev, &sms);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, deq_combine_kernel<DT, DEQ>,
-                                                      threads, 0);
+    e = kernel_blocks_per_sm(reinterpret_cast<const void*>(deq_combine_kernel<DT, DEQ>),
+                             threads, 0, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(s.T(), int64_t(std::max(1, per_sm)) * sms);
   deq_combine_kernel<DT, DEQ><<<static_cast<unsigned>(grid), threads, 0, st>>>(

@@ -662,8 +662,7 @@ cudaError_t launch_codes_to_bf16(const void* src, int64_t rows, int64_t stride, 
                                  void* dst, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = current_device_sms(&dev, &sms);
   if (e != cudaSuccess) return e;
   const int64_t n = rows * (K / 8);
   const int threads = 256;
@@ -683,9 +682,8 @@ cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
                         int32_t* c, const Dequant& dq, uint32_t spin, int32_t* dev_status,
                         int sms, cudaStream_t st) {
   const size_t smem = SmemLayout<STAGES>::bytes(G);
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<STAGES, MODE>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e =
+      ensure_dynamic_smem(reinterpret_cast<const void*>(grouped_gemm_kernel<STAGES, MODE>), smem);
   if (e != cudaSuccess) return e;
   grouped_gemm_kernel<STAGES, MODE><<<sms, kThreads, smem, st>>>(ma, mb, mc, group_rows, G,
                                                                  a_rows, K, N, c, dq, spin,
@@ -713,8 +711,7 @@ cudaError_t launch_stages(const CUtensorMap& ma, const CUtensorMap& mb, const CU
 cudaError_t launch_interleave_gate_up(const void* w, const float* ws, int G, int I, int K,
                                      void* wi, float* wsi, cudaStream_t st) {
   int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = current_device_sms(&dev, &sms);
   if (e != cudaSuccess) return e;
   const int64_t n = int64_t(G) * 2 * I * (K / 8);
   const int threads = 256;
@@ -735,8 +732,7 @@ cudaError_t launch_grouped_gemm(const void* a, int64_t a_rows, int K, const void
   if (e == cudaSuccess) e = encode_out(&mc, c, a_rows, mode == kOutSwiGLU ? N / 2 : N);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0, optin = 0;
-  e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = current_device_sms(&dev, &sms);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;

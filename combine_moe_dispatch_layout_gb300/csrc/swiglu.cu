@@ -314,12 +314,9 @@ cudaError_t launch_warp_t(const int32_t* acc, int64_t M, int I, const ScaleSrc& 
   const size_t smem = size_t(W) * I * sizeof(float);
   auto kernel = swiglu_quant_warp_kernel<BF16OUT>;
   int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = current_device_sms(&dev, &sms);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+    e = kernel_blocks_per_sm(reinterpret_cast<const void*>(kernel), threads, smem, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t grid =
       std::min<int64_t>((M + W - 1) / W, int64_t(std::max(1, per_sm)) * sms);
@@ -335,11 +332,10 @@ cudaError_t launch_t(const int32_t* acc, int64_t M, int I, const ScaleSrc& sc, v
   const int nch = I / 8;
   const int threads = std::max(32, std::min(kMaxThreads, ((nch + kCpt - 1) / kCpt + 31) / 32 * 32));
   int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = current_device_sms(&dev, &sms);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &per_sm, swiglu_quant_kernel<kCpt, BF16OUT>, threads, 0);
+    e = kernel_blocks_per_sm(reinterpret_cast<const void*>(swiglu_quant_kernel<kCpt, BF16OUT>),
+                             threads, 0, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(M, int64_t(std::max(1, per_sm)) * sms);
   swiglu_quant_kernel<kCpt, BF16OUT><<<static_cast<unsigned>(grid), threads, 0, st>>>(
@@ -421,11 +417,10 @@ cudaError_t launch_quant_rows_t(const float* h, int64_t M, int I, const int64_t*
   const int nch = I / 8;
   const int threads = std::max(32, std::min(kMaxThreads, ((nch + kCpt - 1) / kCpt + 31) / 32 * 32));
   int dev = 0, sms = 0, per_sm = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaError_t e = current_device_sms(&dev, &sms);
   if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quant_rows_bf16_kernel<kCpt>,
-                                                      threads, 0);
+    e = kernel_blocks_per_sm(reinterpret_cast<const void*>(quant_rows_bf16_kernel<kCpt>),
+                             threads, 0, &per_sm);
   if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(M, int64_t(std::max(1, per_sm)) * sms);
   quant_rows_bf16_kernel<kCpt><<<static_cast<unsigned>(grid), threads, 0, st>>>(
