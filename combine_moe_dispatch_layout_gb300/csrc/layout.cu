@@ -7,8 +7,9 @@
 // atomics:
 //
 //   * the pairs of each source rank are cut into tiles whose size follows the
-//     shape (one warp x 32 rounds of 32 pairs when a rank has at most 1024
-//     pairs, else eight warps x 16 rounds); a CTA takes the next tile from an
+//     shape (one warp x 8 rounds of 32 pairs when a rank has at most 256
+//     pairs, eight warps x 4 rounds up to 1024 pairs, else eight warps x 8
+//     rounds); a CTA takes the next tile from an
 //     atomic ticket, so a tile only ever waits for tiles that started before
 //     it (forward progress without assuming co-residency);
 //   * inside a tile each warp walks its contiguous segment 32 pairs at a
@@ -312,11 +313,18 @@ struct Geometry {
   int tile() const { return warps * rounds * 32; }
 };
 
+// Measured (one launch, L2 flushed, all geometries bit-identical): a tile of
+// 2048 pairs as 8 warps x 8 rounds beat 4096-pair tiles (8 x 16) on every
+// multi-tile workload (DeepSeek-V3 shape 18.3 -> 16.7 us) -- shorter
+// per-warp chains outweigh the longer look-back -- and smaller tiles lost
+// again (1024 pairs: 21.3 us); a rank of at most 1024 pairs is one tile of
+// 8 warps x 4 rounds (384 ranks x 1024 pairs: 11.0 us, against 22.8 with
+// 4096-pair tiles), and a rank of at most 256 pairs one warp.
 Geometry geometry_of(const Shape& s) {
   const int64_t per_rank = int64_t(s.bs) * s.k;
   if (per_rank <= 256) return {1, 8};
-  if (per_rank <= 1024) return {1, 32};
-  return {8, 16};
+  if (per_rank <= 1024) return {8, 4};
+  return {8, 8};
 }
 
 int tiles_per_rank_of(const Shape& s) {
@@ -359,11 +367,11 @@ cudaError_t launch_layout(const Shape& s, const int32_t* topk_idx,
                           int32_t* send_idx, void* workspace,
                           int32_t* dev_status, cudaStream_t st) {
   const Geometry g = geometry_of(s);
-  if (g.warps == 1 && g.rounds == 8)
-    return launch_t<1, 8>(s, topk_idx, count, rank_send, send_idx, workspace, dev_status, st);
   if (g.warps == 1)
-    return launch_t<1, 32>(s, topk_idx, count, rank_send, send_idx, workspace, dev_status, st);
-  return launch_t<8, 16>(s, topk_idx, count, rank_send, send_idx, workspace, dev_status, st);
+    return launch_t<1, 8>(s, topk_idx, count, rank_send, send_idx, workspace, dev_status, st);
+  if (g.rounds == 4)
+    return launch_t<8, 4>(s, topk_idx, count, rank_send, send_idx, workspace, dev_status, st);
+  return launch_t<8, 8>(s, topk_idx, count, rank_send, send_idx, workspace, dev_status, st);
 }
 
 }  // namespace moe_ep

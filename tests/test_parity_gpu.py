@@ -168,10 +168,10 @@ def test_named_workload_full_size(oracle_mod, pl, name):
 
 
 @pytest.mark.parametrize("case", [
-    dict(R=3, epr=5, bs=1500, k=7, H=1000),             # 3 tiles/rank, ragged
+    dict(R=3, epr=5, bs=1500, k=7, H=1000),             # 6 tiles/rank, ragged
     dict(R=5, epr=3, bs=2000, k=4, H=136, dtype=W.FP16),   # fp16 + quant
     dict(R=4, epr=6, bs=1111, k=5, H=520, quant=False),    # bf16 verbatim
-    dict(R=1, epr=16, bs=70000, k=8, H=64),             # 137 tiles in one rank
+    dict(R=1, epr=16, bs=70000, k=8, H=64),             # 274 tiles in one rank
     dict(R=7, epr=1, bs=333, k=1, H=2048),              # k = 1, one expert/rank
 ], ids=lambda c: "-".join("%s%s" % kv for kv in c.items()))
 def test_mid_size(oracle_mod, pl, case):
@@ -298,7 +298,7 @@ def test_unzeroed_workspace_is_reported_and_recovers(oracle_mod, ep, pl):
     touches nothing, and every CTA still reaches the end-of-launch
     bookkeeping, which resets the workspace: the next call is correct."""
     import time
-    w = W.Workload("ws_bad", R=2, epr=8, bs=4096, k=4, H=64)   # 4 tiles/rank
+    w = W.Workload("ws_bad", R=2, epr=8, bs=4096, k=4, H=64)   # 8 tiles/rank
     idx, _ = W.routing(w)
     shape = ep.make_shape(w.R, w.bs, w.k, w.epr, w.H)
     b = pl.PipelineBuffers(w.R, w.bs, w.k, w.epr, w.H, w.dtype, w.quant)
@@ -588,7 +588,7 @@ def test_pipeline_graph_capture_and_replay(oracle_mod, pl):
     """The four entry points enqueue nothing but kernels (and memsets) on the
     caller's stream, so the pipeline can be captured once and replayed; the
     layout workspace's epoch protocol works across replays."""
-    w = W.Workload("graph", R=4, epr=4, bs=600, k=4, H=256)    # 3 tiles/rank
+    w = W.Workload("graph", R=4, epr=4, bs=600, k=4, H=256)    # 2 layout tiles/rank
     b = pl.PipelineBuffers(w.R, w.bs, w.k, w.epr, w.H, w.dtype, w.quant)
     idx_d = torch.empty((w.T, w.k), dtype=torch.int32, device="cuda")
     wt_d = torch.empty((w.T, w.k), dtype=torch.float32, device="cuda")
