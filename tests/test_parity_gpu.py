@@ -194,6 +194,34 @@ def test_odd_expert_count_after_dirty_shared_memory(oracle_mod, pl, case):
     _check_full(oracle_mod, pl, W.Workload("odd", **case))
 
 
+@pytest.mark.parametrize("case", [
+    dict(R=3, epr=4, bs=64, k=4),               # 256 pairs a rank: the one-warp tile, full
+    dict(R=3, epr=4, bs=257, k=1),              # 257: one 8-warp x 4-round tile
+    dict(R=3, epr=4, bs=128, k=8),              # 1024: that tile, full
+    dict(R=3, epr=5, bs=205, k=5),              # 1025: one 2048-pair tile
+    dict(R=3, epr=4, bs=256, k=8),              # 2048: that tile, full
+    dict(R=3, epr=4, bs=683, k=3),              # 2049: two tiles, the second one pair
+    dict(R=2, epr=8, bs=1025, k=4),             # 4100: three tiles
+    dict(R=4, epr=8, bs=700, k=6, routing="zipf"),   # 4200, skewed experts
+], ids=lambda c: "R%d-bs%d-k%d%s" % (c["R"], c["bs"], c["k"], "-zipf" if "routing" in c else ""))
+def test_layout_tile_geometry_boundaries(oracle_mod, pl, case):
+    """Pairs per rank at and around the layout's tile-size steps (one warp up
+    to 256 pairs, one 8 x 4 tile up to 1024, 2048-pair tiles beyond): layout
+    and notify bit-exact against the oracle, the workspace reused across the
+    cases."""
+    w = W.Workload("geom", H=64, seed=900 + case["bs"], **case)
+    idx_t, _ = W.routing(w)
+    L = oracle_mod.layout(idx_t.numpy(), w.R, w.epr)
+    N = oracle_mod.notify(L["count"], w.R, w.bs, w.epr)
+    b = pl.PipelineBuffers(w.R, w.bs, w.k, w.epr, w.H, w.dtype, w.quant)
+    for _ in range(2):                           # the second call reuses the workspace
+        b.send_idx.fill_(-7)
+        pl.run_layout_notify(b, idx_t.cuda())
+        torch.cuda.synchronize()
+        assert b.status() == 0
+        _check_layout_notify(b, dict(L=L, N=N))
+
+
 def test_duplicate_experts_in_token(oracle_mod, pl):
     w = W.Workload("dup", R=3, epr=2, bs=500, k=6, H=96)
     rng = np.random.default_rng(11)
