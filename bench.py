@@ -81,6 +81,19 @@ def workload_desc(w):
         "int8-quant" if w.quant else "verbatim"))
 
 
+def step_config(w, world):
+    """The `config` object of the step, the same on both arms (the reference
+    arm runs the identical workload on the host cores)."""
+    return {
+        "workload": workload_desc(w),
+        "step": "layout+notify+dispatch+combine, inputs resident in HBM",
+        "l2": "flushed between steps (256 MiB write outside the step events)",
+        "parallelism": "replicas" if world > 1 else "single GPU",
+        "io_dtype": "bf16" if w.dtype == W.BF16 else "fp16",
+        "recv_rows": "int8 + fp32 1/scale" if w.quant else "verbatim",
+    }
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -510,14 +523,7 @@ def run_gpu(args, w):
         "dtype": "f32",
         "data": "synthetic (seeded: routing, weights and x drawn on the host, "
                 "expert outputs drawn on the device)",
-        "config": {
-            "workload": workload_desc(w),
-            "step": "layout+notify+dispatch+combine, inputs resident in HBM",
-            "l2": "flushed between steps (256 MiB write outside the step events)",
-            "parallelism": "replicas" if world > 1 else "single GPU",
-            "io_dtype": "bf16" if w.dtype == W.BF16 else "fp16",
-            "recv_rows": "int8 + fp32 1/scale" if w.quant else "verbatim",
-        },
+        "config": step_config(w, world),
         "roofline": dict(head["roofline_combine"]),
         "roofline_dispatch": head["roofline_dispatch"],
         "combine_quant": cq,
@@ -986,8 +992,9 @@ def run_reference(args, w):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": workload_desc(w),
-                   "step": "layout+notify+dispatch+combine (CPU oracle)"},
+        "config": step_config(w, world),
+        "arm": "the CPU oracle on the host cores: the same step on the same inputs, "
+               "in host memory",
         "stages_ms": stages,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oh.threads,
                          "kind": "oracle", "cpu": model,
