@@ -333,6 +333,7 @@ def measure_pipeline(w, dev, stream, flush, x, idx, wt, y, steps, warmup,
     del g_fused, g_sep
     stage_mean = stage_ms.mean(axis=0)
     rec = {"steps": steps, "stage_ms": stage_mean, "step_ms": stage_ms.sum(axis=1),
+           "stage_ms_median": np.median(stage_ms, axis=0),
            "wall_s": wall,
            "graph_step_us": _mean_us(graph_step),
            "dispatch_fused": {
@@ -372,6 +373,9 @@ def config_record(w, m, peak, peak_kind, cpu=None):
         "tokens_per_s": w.T / (step_ms * 1e-3),
         "dispatch_combine_tokens_per_s": w.T / ((stage_mean[2] + stage_mean[3]) * 1e-3),
         "stages_us": {n: float(stage_mean[j] * 1e3) for j, n in enumerate(names)},
+        "step_us_median": float(np.median(m["step_ms"])) * 1e3,
+        "stages_us_median": {n: float(m["stage_ms_median"][j] * 1e3)
+                             for j, n in enumerate(names)},
         "stages_gbs": {n: ab[n] / (stage_mean[j] * 1e-3) / 1e9 for j, n in enumerate(names)},
         "roofline": comb if comb["avg_launch_ms"] >= disp["avg_launch_ms"] else disp,
         "roofline_dispatch": disp,
@@ -533,6 +537,8 @@ def run_gpu(args, w):
         "deep_moe": deep,
         "dispatch_fused": m["dispatch_fused"],
         "stages_us": head["stages_us"],
+        "stages_us_median": head["stages_us_median"],
+        "step_us_median": head["step_us_median"],
         "stages_gbs": gbs,
         "dispatch_combine_tokens_per_s": head["dispatch_combine_tokens_per_s"],
         "e2e": {"value": aggregate_tokens_per_s(w.T, world, e2e_max_ms / 1e3),
