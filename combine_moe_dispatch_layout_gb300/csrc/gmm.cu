@@ -225,14 +225,17 @@ struct Dequant {
 // and 10 warps put 3 on some of them, so at most 168 registers per thread.
 // MODE (kOut*) is a template parameter so each epilogue gets its own
 // register allocation.
-template <int STAGES, int MODE>
+template <int STAGES, int MODE, bool POLLS>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC,
                     const int32_t* __restrict__ group_rows, int G, int64_t a_rows, int K,
-                    int N, int32_t* __restrict__ C, Dequant dq, uint32_t spin,
+                    int N, int32_t* __restrict__ C, Dequant dq, uint32_t spin_arg,
                     int32_t* dev_status) {
+  // the main-loop poll bound: the launch argument only in the test build of
+  // the kernel (POLLS); a compile-time constant otherwise
+  const uint32_t spin = POLLS ? spin_arg : kSpin;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -676,19 +679,30 @@ int gmm_block_n() { return BN; }
 
 namespace {
 
+template <int STAGES, int MODE, bool POLLS>
+cudaError_t launch_polls(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                         const int32_t* group_rows, int G, int64_t a_rows, int K, int N,
+                         int32_t* c, const Dequant& dq, uint32_t spin, int32_t* dev_status,
+                         int sms, cudaStream_t st) {
+  const size_t smem = SmemLayout<STAGES>::bytes(G);
+  auto kernel = grouped_gemm_kernel<STAGES, MODE, POLLS>;
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<sms, kThreads, smem, st>>>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq, spin,
+                                      dev_status);
+  return cudaGetLastError();
+}
+
 template <int STAGES, int MODE>
 cudaError_t launch_mode(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                         const int32_t* group_rows, int G, int64_t a_rows, int K, int N,
                         int32_t* c, const Dequant& dq, uint32_t spin, int32_t* dev_status,
                         int sms, cudaStream_t st) {
-  const size_t smem = SmemLayout<STAGES>::bytes(G);
-  cudaError_t e =
-      ensure_dynamic_smem(reinterpret_cast<const void*>(grouped_gemm_kernel<STAGES, MODE>), smem);
-  if (e != cudaSuccess) return e;
-  grouped_gemm_kernel<STAGES, MODE><<<sms, kThreads, smem, st>>>(ma, mb, mc, group_rows, G,
-                                                                 a_rows, K, N, c, dq, spin,
-                                                                 dev_status);
-  return cudaGetLastError();
+  if (spin == kSpin)
+    return launch_polls<STAGES, MODE, false>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq,
+                                             spin, dev_status, sms, st);
+  return launch_polls<STAGES, MODE, true>(ma, mb, mc, group_rows, G, a_rows, K, N, c, dq, spin,
+                                          dev_status, sms, st);
 }
 
 template <int STAGES>
