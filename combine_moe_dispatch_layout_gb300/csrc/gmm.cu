@@ -31,8 +31,9 @@
 // already issued before it releases TMEM and retires.  A chunk whose K
 // blocks were cut short is never handed to the epilogue.  The main-loop
 // waits (stage empty / full, accumulator free / final) take their poll
-// limit from the launch, so that a test can make them run out; the drain
-// waits always use the full bound.
+// limit from the launch in a separate test instantiation (POLLS), so that a
+// test can make them run out; the production kernel keeps the limit a
+// compile-time constant, and the drain waits always use the full bound.
 #include <cuda.h>
 
 #include <algorithm>
