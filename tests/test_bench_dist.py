@@ -84,6 +84,13 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2
     assert rec["value"] > 0 and rec["e2e"]["h2d_bytes_per_step"] == 0
     assert rec["cpu_baseline"]["kind"] == "oracle"
+    # the same metric, unit, direction and config object as the GPU arm
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    assert rec["config"] == bench.step_config(W.WORKLOADS["tiny"], 2)
+    assert rec["metric"] == "dispatch+combine tokens/s" and rec["unit"] == "tokens/s"
+    assert rec["higher_is_better"] is True and rec["e2e"]["value"] == rec["value"]
 
 
 def test_cpu_baseline_leg_on_the_host():
