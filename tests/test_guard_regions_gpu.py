@@ -6,9 +6,9 @@ buffer itself is pre-filled with a second sentinel.  After the stage runs:
 the margins are unchanged (no write landed outside a buffer), and the
 outputs equal the oracle bit for bit (so every element the stage owns was
 written: a leftover sentinel would differ).  Covers the four stages, the
-one-launch dispatch, the INT8 combine, the token-level layout and the GMM1
-epilogue, on shapes with ragged tiles and tails, and on the two-kernel notify
-path (R > 64)."""
+one-launch dispatch, the INT8 combine, the token-level layout, the GMM1
+epilogue and the whole deep MoE, on shapes with ragged tiles and tails, and
+on the two-kernel notify path (R > 64)."""
 import numpy as np
 import pytest
 import torch
@@ -193,3 +193,45 @@ def test_gmm1_epilogue_stays_inside(oracle_mod, ep, M, I):
     ref = oracle_mod.swiglu_quant(acc_h.numpy(), ws_h.numpy(), ts_h.numpy())
     ref = ref[0] if isinstance(ref, tuple) else ref
     assert np.array_equal(out.cpu().numpy().reshape(ref.shape), ref), "GMM1 epilogue"
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["int32_gmm1", "swiglu_in_gmm1"])
+def test_deep_moe_stays_inside_its_buffers(oracle_mod, pl, fused):
+    """The fused deep MoE (dispatch_expand, group offsets, the grouped GEMMs
+    with their int32 / SwiGLU / dequantising epilogues, the requantisation
+    and the fp32 combine) on a ragged Zipf-routed shape, every intermediate
+    in a guarded view."""
+    w = W.Workload("g_deep", R=3, epr=3, bs=70, H=1096, k=3, routing="zipf",
+                   weights="sigmoid", x_scale=2.0, seed=75)
+    I = 264
+    idx, wt = W.routing(w)
+    x = W.tokens(w)
+    w1, ws1, w2, ws2 = W.moe_weights(w.E, w.H, I, seed=7)
+    ref = oracle_mod.deep_moe(W.bits(x), idx.numpy(), wt.numpy(), w.R, w.epr, w.dtype,
+                              w1.numpy(), ws1.numpy(), w2.numpy(), ws2.numpy())
+    G = Guarded()
+    b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype)
+    base = _guarded_buffers(pl, w.with_(quant=True), G)
+    for name in ("count", "rank_send", "send_idx", "workspace", "put_offset", "total_recv",
+                 "rank_recv_base", "recv_per_expert", "max_bs", "dev_status", "out"):
+        setattr(b, name, getattr(base, name))
+    P = w.P
+    b.group_off = G((w.E + 1,), torch.int64)
+    b.a1 = G((P, w.H), torch.bfloat16)
+    b.ts1 = G((P,), torch.float32)
+    b.acc1 = G((P, 2 * I), torch.int32)
+    b.h = G((P, I), torch.float32)
+    b.a2 = G((P, I), torch.bfloat16)
+    b.ts2 = G((P,), torch.float32)
+    b.y2 = G((P, w.H), torch.float32)
+    dev = torch.device("cuda")
+    wts = pl.DeepMoeWeights(w1.to(dev), ws1.to(dev), w2.to(dev), ws2.to(dev))
+    idx_d, wt_d, x_d = idx.to(dev), wt.to(dev), x.to(dev)
+    pl.run_layout_notify(b, idx_d)
+    pl.run_dispatch_expand(b, x_d, idx_d)
+    pl.run_deep_moe_experts(b, wts, fused_swiglu=fused)
+    pl.run_deep_combine(b, idx_d, wt_d)
+    G.assert_margins()
+    assert b.status() == 0
+    got = b.out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got.reshape(ref["out"].shape), ref["out"]), "deep MoE out"
