@@ -251,8 +251,11 @@ moe_status moe_combine(const moe_shape* shape, const void* expert_out,
  *   workspace  moe_fused_workspace_bytes() bytes, 16-byte aligned,
  *              zero-filled once before first use (each call leaves it ready;
  *              after MOE_ERR_TIMEOUT zero it again)
- * Calls sharing a workspace must not overlap on the GPU.  A grid-barrier
- * wait that exceeds about a second sets MOE_ERR_TIMEOUT. */
+ * Calls sharing a workspace must not overlap on the GPU.  The cooperative
+ * form is sized to fill the GPU, so do not run two such calls (or another
+ * kernel whose CTAs wait on one another) at the same time on different
+ * streams: their CTAs could not all be resident.  A grid-barrier wait that
+ * exceeds about a second sets MOE_ERR_TIMEOUT. */
 size_t moe_fused_workspace_bytes(const moe_shape* shape);
 moe_status moe_dispatch_fused(const moe_shape* shape, const void* x,
                               const int32_t* topk_idx, int quant, int32_t* count,
