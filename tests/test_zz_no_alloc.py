@@ -97,7 +97,7 @@ def test_static_on_a_side_stream(lib):
 
 def test_static_rejects_shapes_beyond_the_array(lib):
     ep, L = lib
-    # E = 4096 with 16 tiles per rank needs ~4.2 MB of scratch (> 4 MiB)
+    # E = 4096 with 32 tiles per rank needs ~8.4 MB of scratch (> 4 MiB)
     shape = ep.make_shape(8, 8192, 8, 512, 64)
     assert ep.layout_workspace_bytes(shape) > (4 << 20)
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
