@@ -1,0 +1,104 @@
+"""Randomised shapes: 120 seeded random problems (ranks, experts per rank,
+tokens per rank including 0, top-k, hidden size down to 8, both token
+dtypes, INT8 or verbatim rows, uniform or Zipf routing) through the four
+stages, the one-launch dispatch and, for INT8 rows, the INT8 combine, each
+compared with the oracle bit for bit.  The fixed cases elsewhere pin the
+known edges; this sweep crosses the kernels' internal size decisions (tile
+geometry, parts per token, one-CTA or cooperative one-launch form, chunks
+per thread) at combinations nobody chose by hand."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _shapes(n, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        R = int(rng.choice([1, 2, 3, 5, 8, 13, 24, 40, 70]))
+        epr = int(rng.integers(1, 9))
+        E = R * epr
+        if E > 4096:
+            continue
+        bs = int(rng.choice([0, 1, 7, 33, 64, 129, 300, 517],
+                            p=[0.04, 0.12, 0.14, 0.14, 0.14, 0.14, 0.14, 0.14]))
+        k = int(rng.integers(1, min(E, 12) + 1))
+        H = int(8 * rng.integers(1, 151))
+        dtype = W.BF16 if rng.random() < 0.6 else W.FP16
+        quant = bool(rng.random() < 0.7)
+        routing = "zipf" if (rng.random() < 0.25 and k < E) else "uniform"
+        out.append(W.Workload("rand%d" % len(out), R=R, epr=epr, bs=bs, H=H, k=k,
+                              dtype=dtype, quant=quant, routing=routing,
+                              seed=3000 + len(out)))
+    return out
+
+
+SHAPES = _shapes(120)
+
+
+@pytest.fixture(scope="module")
+def pl():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from combine_moe_dispatch_layout_gb300 import pipeline
+    return pipeline
+
+
+def _u16(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("w", SHAPES, ids=lambda w: "R%d-epr%d-bs%d-k%d-H%d-%s-%s%s" % (
+    w.R, w.epr, w.bs, w.k, w.H, "fp16" if w.dtype == W.FP16 else "bf16",
+    "q" if w.quant else "v", "-zipf" if w.routing == "zipf" else ""))
+def test_random_shape(oracle_mod, pl, w):
+    idx, wt = W.routing(w)
+    x, y = W.tokens(w), W.expert_outputs(w)
+    L = oracle_mod.layout(idx.numpy(), w.R, w.epr)
+    N = oracle_mod.notify(L["count"], w.R, w.bs, w.epr)
+    recv, st = oracle_mod.dispatch(W.bits(x), idx.numpy(), L["send_idx"], N["put_offset"],
+                                   N["rank_recv_base"], w.R, w.epr, w.dtype, w.quant)
+    out, st2 = oracle_mod.combine(W.bits(y), idx.numpy(), wt.numpy(), L["send_idx"],
+                                  N["put_offset"], N["rank_recv_base"], w.R, w.epr, w.dtype)
+    assert st == 0 and st2 == 0
+    dev = torch.device("cuda")
+    idx_d, wt_d, x_d, y_d = idx.to(dev), wt.to(dev), x.to(dev), y.to(dev)
+
+    def check(b, with_out):
+        assert b.status() == 0
+        np.testing.assert_array_equal(b.count.cpu().numpy(), L["count"])
+        np.testing.assert_array_equal(b.rank_send.cpu().numpy(), L["rank_send"])
+        np.testing.assert_array_equal(b.send_idx.cpu().numpy(), L["send_idx"])
+        np.testing.assert_array_equal(b.put_offset.cpu().numpy(), N["put_offset"])
+        np.testing.assert_array_equal(b.rank_recv_base.cpu().numpy(), N["rank_recv_base"])
+        np.testing.assert_array_equal(b.recv_per_expert.cpu().numpy(), N["recv_per_expert"])
+        np.testing.assert_array_equal(b.recv.cpu().numpy(), recv)
+        if with_out:
+            np.testing.assert_array_equal(_u16(b.out).reshape(out.shape), out)
+
+    b = pl.PipelineBuffers(w.R, w.bs, w.k, w.epr, w.H, w.dtype, w.quant)
+    b.recv.fill_(0xCD)
+    pl.run_pipeline(b, x_d, idx_d, wt_d, y_d)
+    torch.cuda.synchronize()
+    check(b, True)
+
+    b2 = pl.PipelineBuffers(w.R, w.bs, w.k, w.epr, w.H, w.dtype, w.quant)
+    b2.recv.fill_(0xCD)
+    pl.run_dispatch_fused(b2, x_d, idx_d)
+    torch.cuda.synchronize()
+    check(b2, False)
+
+    if w.quant and w.T > 0:
+        yq = W.expert_outputs_int8(w)
+        ref, s = oracle_mod.combine_quant(yq.numpy(), idx.numpy(), wt.numpy(), L["send_idx"],
+                                          N["put_offset"], N["rank_recv_base"], w.R, w.epr,
+                                          w.dtype, w.H)
+        assert s == 0
+        pl.run_combine_quant(b, yq.to(dev), idx_d, wt_d)
+        torch.cuda.synchronize()
+        assert b.status() == 0
+        np.testing.assert_array_equal(_u16(b.out).reshape(ref.shape), ref)
