@@ -2,7 +2,8 @@
 tokens per rank including 0, top-k, hidden size down to 8, both token
 dtypes, INT8 or verbatim rows, uniform or Zipf routing) through the four
 stages, the one-launch dispatch and, for INT8 rows, the INT8 combine, each
-compared with the oracle bit for bit.  The fixed cases elsewhere pin the
+compared with the oracle bit for bit; then random GMM1-epilogue shapes and
+random grouped GEMMs, also bit-exact.  The fixed cases elsewhere pin the
 known edges; this sweep crosses the kernels' internal size decisions (tile
 geometry, parts per token, one-CTA or cooperative one-launch form, chunks
 per thread) at combinations nobody chose by hand."""
@@ -102,3 +103,73 @@ def test_random_shape(oracle_mod, pl, w):
         torch.cuda.synchronize()
         assert b.status() == 0
         np.testing.assert_array_equal(_u16(b.out).reshape(ref.shape), ref)
+
+
+# ---- the GMM1 epilogue and the grouped GEMM over random shapes ----------------
+
+def _epilogue_shapes(n, seed=2025):
+    rng = np.random.default_rng(seed)
+    return [(int(rng.choice([1, 2, 17, 64, 300, 1000])),
+             int(8 * rng.choice([1, 3, 5, 32, 100, 255, 256, 257, 512, 513, 700, 1024]))
+             ) for _ in range(n)]
+
+
+@pytest.fixture(scope="module")
+def ep(pl):
+    import combine_moe_dispatch_layout_gb300 as ep
+    return ep
+
+
+@pytest.mark.parametrize("M,I", _epilogue_shapes(30), ids=lambda v: str(v))
+def test_random_gmm1_epilogue(oracle_mod, ep, M, I):
+    """Row widths from 8 to 8192 outputs: the warp form (I <= 4096) and the
+    CTA form (larger I), bit-exact against the oracle's exp reading."""
+    acc, ws, ts = W.gmm1_accumulators(M, I, seed=M * 7 + I)
+    rb = (I + 31) // 32 * 32 + 32
+    out = torch.full((M, rb), 0xAB, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ep.moe_swiglu_quant(acc.cuda(), ws.cuda(), ts.cuda(), out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = oracle_mod.swiglu_quant(acc.numpy(), ws.numpy(), ts.numpy())
+    np.testing.assert_array_equal(out.cpu().numpy(), ref)
+
+
+def _gemm_shapes(n, seed=2026):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        G = int(rng.choice([1, 2, 3, 7, 16, 40]))
+        sizes = tuple(int(v) for v in rng.choice([0, 1, 5, 63, 128, 129, 200, 333], G))
+        if sum(sizes) == 0:
+            sizes = (1,) + sizes[1:]
+        N = int(8 * rng.choice([1, 2, 17, 32, 33, 64, 96]))
+        K = int(8 * rng.choice([1, 8, 9, 127, 128, 129, 260]))
+        out.append((G, N, K, sizes))
+    return out
+
+
+@pytest.mark.parametrize("case", _gemm_shapes(20), ids=lambda c: "G%d_N%d_K%d" % c[:3])
+def test_random_grouped_gemm(oracle_mod, ep, case):
+    """Exact int32 sums for random group sizes (empty groups included),
+    output widths down to 8 and K from 8 to 2080 (one to three 1024-wide
+    exact chunks, ragged K blocks)."""
+    G, N, K, sizes = case
+    rng = np.random.default_rng(sum(sizes) * 31 + N + K)
+    M = sum(sizes)
+    a = rng.integers(-128, 128, (M, K)).astype(np.int8)
+    w = rng.integers(-128, 128, (G, N, K)).astype(np.int8)
+    dev = torch.device("cuda")
+    a_bf = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    w_bf = torch.empty((G, N, K), dtype=torch.bfloat16, device=dev)
+    ep.moe_codes_to_bf16(torch.from_numpy(a.view(np.uint8)).to(dev), M, K, K, a_bf)
+    ep.moe_codes_to_bf16(torch.from_numpy(w.view(np.uint8)).to(dev), G * N, K, K, w_bf)
+    gr = torch.tensor(sizes, dtype=torch.int32, device=dev)
+    c = torch.full((M, N), -7, dtype=torch.int32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ep.moe_grouped_gemm_i8(a_bf, w_bf, gr, c, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    np.testing.assert_array_equal(c.cpu().numpy(), oracle_mod.grouped_gemm(a.view(np.uint8),
+                                                                           off, w))
