@@ -3,7 +3,7 @@ tokens per rank including 0, top-k, hidden size down to 8, both token
 dtypes, INT8 or verbatim rows, uniform or Zipf routing) through the four
 stages, the one-launch dispatch and, for INT8 rows, the INT8 combine, each
 compared with the oracle bit for bit; then random GMM1-epilogue shapes and
-random grouped GEMMs, also bit-exact.  The fixed cases elsewhere pin the
+random grouped GEMMs and random small deep MoE problems, also bit-exact.  The fixed cases elsewhere pin the
 known edges; this sweep crosses the kernels' internal size decisions (tile
 geometry, parts per token, one-CTA or cooperative one-launch form, chunks
 per thread) at combinations nobody chose by hand."""
@@ -173,3 +173,42 @@ def test_random_grouped_gemm(oracle_mod, ep, case):
     off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
     np.testing.assert_array_equal(c.cpu().numpy(), oracle_mod.grouped_gemm(a.view(np.uint8),
                                                                            off, w))
+
+
+def _deep_shapes(n, seed=2027):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        R = int(rng.choice([1, 2, 3, 5]))
+        epr = int(rng.integers(1, 5))
+        k = int(rng.integers(1, min(R * epr, 4) + 1))
+        bs = int(rng.choice([1, 9, 40, 77]))
+        H = int(8 * rng.choice([16, 33, 64, 130]))
+        I = int(8 * rng.choice([2, 8, 33, 64]))
+        dtype = W.BF16 if rng.random() < 0.6 else W.FP16
+        out.append((W.Workload("rdeep%d" % i, R=R, epr=epr, bs=bs, H=H, k=k, dtype=dtype,
+                               x_dist="uniform" if dtype == W.FP16 else "normal",
+                               seed=5000 + i), I))
+    return out
+
+
+@pytest.mark.parametrize("w,I", _deep_shapes(8), ids=lambda v: getattr(v, "name", str(v)))
+def test_random_deep_moe(oracle_mod, pl, w, I):
+    """The fused deep MoE (both GMM1 routes) on random small shapes, bit-exact."""
+    idx, wt = W.routing(w)
+    x = W.tokens(w)
+    w1, ws1, w2, ws2 = W.moe_weights(w.E, w.H, I, seed=w.seed)
+    ref = oracle_mod.deep_moe(W.bits(x), idx.numpy(), wt.numpy(), w.R, w.epr, w.dtype,
+                              w1.numpy(), ws1.numpy(), w2.numpy(), ws2.numpy())
+    dev = torch.device("cuda")
+    wts = pl.DeepMoeWeights(w1.to(dev), ws1.to(dev), w2.to(dev), ws2.to(dev))
+    for fused in (False, True):
+        b = pl.DeepMoeBuffers(w.R, w.bs, w.k, w.epr, w.H, I, w.dtype)
+        idx_d, wt_d, x_d = idx.to(dev), wt.to(dev), x.to(dev)
+        pl.run_layout_notify(b, idx_d)
+        pl.run_dispatch_expand(b, x_d, idx_d)
+        pl.run_deep_moe_experts(b, wts, fused_swiglu=fused)
+        pl.run_deep_combine(b, idx_d, wt_d)
+        torch.cuda.synchronize()
+        assert b.status() == 0
+        np.testing.assert_array_equal(_u16(b.out).reshape(ref["out"].shape), ref["out"])
