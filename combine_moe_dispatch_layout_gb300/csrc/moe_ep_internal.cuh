@@ -40,6 +40,11 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 
 // Streaming 16-byte load that does not allocate in L1 (each x / expert-output
 // row is read by exactly one CTA).
+// Brings the cache line holding p into L2 (no register, no completion).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ uint4 ld_stream_16(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -228,6 +228,19 @@ swiglu_quant_warp_kernel(const int32_t* __restrict__ acc, int64_t M, int I, Scal
         ++qm;
       }
       if (qm < m1) load(qm, qc, nxt);
+      {   // and the position after that into L2 (no registers held)
+        int64_t rm = qm;
+        int rc = qc + 32;
+        if (rc >= nch) {
+          rc = lane;
+          ++rm;
+        }
+        if (rm < m1) {
+          const int32_t* row = acc + rm * 2 * int64_t(I);
+          prefetch_l2(row + 8 * rc);
+          prefetch_l2(row + I + 8 * rc);
+        }
+      }
       const int32_t gi[8] = {int32_t(cur.g0.x), int32_t(cur.g0.y), int32_t(cur.g0.z),
                              int32_t(cur.g0.w), int32_t(cur.g1.x), int32_t(cur.g1.y),
                              int32_t(cur.g1.z), int32_t(cur.g1.w)};
