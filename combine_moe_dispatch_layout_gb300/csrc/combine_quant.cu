@@ -164,14 +164,24 @@ combine_quant_kernel(const unsigned char* __restrict__ yq, int64_t y_rows,
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[j] = make_float2(0.0f, 0.0f);
       };
+      // The chunk after that is requested into L2 (no registers held).
+      auto prefetch = [&](int cc) {
+#pragma unroll
+        for (int j = 0; j < KB; ++j) {
+          const unsigned char* p = ref[j].p;
+          if (p != nullptr) prefetch_l2(p + 8 * int64_t(cc));
+        }
+      };
       if (c < c1) load(c, 0, va);
       while (c < c1) {
         if (c + 32 < c1) load(c + 32, 0, vb);
+        if (c + 64 < c1) prefetch(c + 64);
         accumulate(0, va, acc);
         finish(c);
         c += 32;
         if (c >= c1) break;
         if (c + 32 < c1) load(c + 32, 0, va);
+        if (c + 64 < c1) prefetch(c + 64);
         accumulate(0, vb, acc);
         finish(c);
         c += 32;
