@@ -11,7 +11,8 @@
 // gather token g's k rows, it resolves token g+grid's rows (topk_idx ->
 // rank_recv_base / put_offset / send_idx, a chain of dependent loads) and
 // weights into the other half of a double-buffered shared table, so the
-// gather never waits on index arithmetic.  Each compute thread owns 16-byte
+// gather never waits on index arithmetic; for wide rows it also asks L2 for
+// that token's rows with one bulk prefetch each.  Each compute thread owns 16-byte
 // chunks of the hidden dimension and issues the loads of up to 8 expert
 // rows before doing any arithmetic.  The arithmetic is exactly the page's:
 // acc = 0; acc = acc + (y * w), one rounding for the multiply and one for
@@ -36,7 +37,7 @@ combine_kernel(const uint4* __restrict__ y, int64_t y_rows,
                const int32_t* __restrict__ put_offset,
                const int64_t* __restrict__ rank_recv_base, int R, int bs, int k,
                int epr, int H, int64_t T, uint4* __restrict__ out,
-               int32_t* dev_status) {
+               int32_t* dev_status, bool prefetch_next) {
   __shared__ int64_t s_rows[2][MOE_EP_MAX_TOPK];
   __shared__ float s_w[2][MOE_EP_MAX_TOPK];
   const int tid = threadIdx.x, lane = tid & 31;
@@ -54,10 +55,18 @@ combine_kernel(const uint4* __restrict__ y, int64_t y_rows,
     const int buf = it & 1;
     if (producer) {
       const int64_t gn = g + gridDim.x;
-      if (gn < T)
+      if (gn < T) {
         resolve_token(gn, topk_idx, weights, send_idx, put_offset, rank_recv_base,
                       R, bs, k, epr, y_rows, s_rows[buf ^ 1], s_w[buf ^ 1],
                       dev_status, lane);
+        // wide rows: the next token's rows start streaming into L2 while
+        // this one is summed (one bulk prefetch per row, no shared memory
+        // or registers)
+        for (int kk = lane; prefetch_next && kk < k; kk += 32) {
+          const int64_t row = s_rows[buf ^ 1][kk];
+          if (row >= 0) bulk_prefetch_l2(y + row * nch, static_cast<uint32_t>(nch) * 16u);
+        }
+      }
     } else {
       const int64_t* rows = s_rows[buf];
       const float* w = s_w[buf];
@@ -103,6 +112,12 @@ int compute_threads(int nch, int cpt) {
 // k rows are in flight while its CTA gathers them.
 constexpr int64_t kInFlightBytes = 160 * 1024;
 
+// Rows at least this wide (two CTAs per SM) gain from prefetching the next
+// token's rows into L2 (measured: 14 KB rows, dsv3 630 -> 622 us, maxrank
+// 944 -> 924 us); narrower rows, with more CTAs per SM, lose (skew's 8 KB
+// rows 295 -> 318 us, fp16's 4 KB rows 189 -> 200 us).
+constexpr int64_t kPrefetchRowBytes = 12 * 1024;
+
 template <int DT>
 cudaError_t launch_t(const Shape& s, const void* y, int64_t y_rows,
                      const int32_t* topk_idx, const float* weights,
@@ -130,7 +145,7 @@ cudaError_t launch_t(const Shape& s, const void* y, int64_t y_rows,
   combine_kernel<DT><<<static_cast<unsigned>(grid), threads, 0, st>>>(
       static_cast<const uint4*>(y), y_rows, topk_idx, weights, send_idx,
       put_offset, rank_recv_base, s.R, s.bs, s.k, s.epr, s.H, s.T(),
-      static_cast<uint4*>(out), dev_status);
+      static_cast<uint4*>(out), dev_status, int64_t(s.H) * 2 >= kPrefetchRowBytes);
   return cudaGetLastError();
 }
 

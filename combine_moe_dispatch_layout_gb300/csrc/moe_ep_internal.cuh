@@ -40,6 +40,12 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 
 // Streaming 16-byte load that does not allocate in L1 (each x / expert-output
 // row is read by exactly one CTA).
+// Brings `bytes` (a multiple of 16) from the 16-byte aligned p into L2 with
+// one bulk prefetch (no shared memory, no completion to wait for).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Brings the cache line holding p into L2 (no register, no completion).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
