@@ -518,6 +518,8 @@ fused_dispatch_kernel(Params p) {
           mbar_arrive_expect_tx(&mbar[b], xbytes);
           bulk_load(const_cast<unsigned char*>(xsb), p.x + g2 * xbytes, xbytes, &mbar[b]);
           pend[b] = ((it + 2) >> 1) & 1;
+          // as moe_dispatch: the next row after it starts for L2 (INT8 path)
+          if (QUANT && g2 + G < T) bulk_prefetch_l2(p.x + (g2 + G) * xbytes, xbytes);
         }
       }
       continue;
